@@ -1,0 +1,381 @@
+// moe_api.cu -- the C ABI declared in include/moe.h.
+//
+// moe_init validates the layout, makes ONE device allocation that holds the
+// library's copy of the weights and a workspace sized for max_tokens (the
+// pages pre-allocate one pool at init and only do pointer arithmetic per call:
+// pure-C Colibri tutorial, trdm.cn, §2.2 and §3.2; Colibri C + cuBLASLt
+// tutorial, cf-1.com, §2.2 "Unified Memory Pool"), and copies the weights in.
+// moe_forward only launches kernels on the caller's stream.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "moe_internal.cuh"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kTileM = 128;   // rows per tensor-core tile; the dispatch tile list uses it
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Carver {
+  char *base;
+  size_t off = 0;
+  template <class T>
+  T *take(size_t n) {
+    off = align_up(off, kAlign);
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+int validate_layout(const moe_layout *L) {
+  if (!L) return MOE_ERR_ARG;
+  if (L->num_experts < 1 || L->num_experts > moe::kMaxExperts) return MOE_ERR_ROUTING;
+  if (L->top_k < 1 || L->top_k > L->num_experts || L->top_k > moe::kMaxTopK) return MOE_ERR_ROUTING;
+  if (L->router_mode != 0 && L->router_mode != 1) return MOE_ERR_ROUTING;
+  if (!(L->routed_scaling_factor > 0.f)) return MOE_ERR_ROUTING;
+  if (L->hidden < 512 || L->hidden % 512) return MOE_ERR_ARG;
+  if (L->intermediate < 1024 || L->intermediate % 1024) return MOE_ERR_ARG;
+  if (L->n_shared != 0 && L->n_shared != 1) return MOE_ERR_ARG;
+  if (L->n_shared && (L->shared_intermediate < 1024 || L->shared_intermediate % 1024))
+    return MOE_ERR_ARG;
+  if (L->x_dtype != 0 && L->x_dtype != 1) return MOE_ERR_ARG;
+  if (L->max_tokens < 1 || (long long)L->max_tokens * L->top_k > (1LL << 26)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+int validate_weights(const moe_layout *L, const moe_weights *W) {
+  if (!W) return MOE_ERR_ARG;
+  if (!W->router_w || !W->w1_q || !W->w1_s || !W->w3_q || !W->w3_s || !W->w2_q || !W->w2_s)
+    return MOE_ERR_ARG;
+  if (L->router_mode == 1 && !W->router_bias) return MOE_ERR_ARG;
+  if (L->n_shared && (!W->sw1_q || !W->sw1_s || !W->sw3_q || !W->sw3_s || !W->sw2_q || !W->sw2_s))
+    return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+// Test hook: MOE_FAULT_ALLOC_AT=n makes the n-th device allocation of a
+// moe_init call report failure, to exercise the clean-up path.
+bool fault_alloc(int n) {
+  const char *v = getenv("MOE_FAULT_ALLOC_AT");
+  return v && atoi(v) == n;
+}
+
+void carve(moe_handle *h, Carver &c) {
+  const size_t E = h->E, H = h->H, I = h->I, Is = h->Is, S = h->S, k = h->k;
+  const size_t maxT = h->L.max_tokens, A = maxT * k, rows = A + S * maxT;
+  const size_t Imax = I > Is ? I : Is;
+  h->wr_t = c.take<float>(E * H);
+  h->bias = c.take<float>(E);
+  h->ex.w1q = c.take<uint8_t>(E * I * H / 2);
+  h->ex.w3q = c.take<uint8_t>(E * I * H / 2);
+  h->ex.w2q = c.take<uint8_t>(E * H * I / 2);
+  h->ex.w1s = c.take<float>(E * I * H / 64);
+  h->ex.w3s = c.take<float>(E * I * H / 64);
+  h->ex.w2s = c.take<float>(E * H * I / 64);
+  if (S) {
+    h->sh.w1q = c.take<uint8_t>(Is * H / 2);
+    h->sh.w3q = c.take<uint8_t>(Is * H / 2);
+    h->sh.w2q = c.take<uint8_t>(H * Is / 2);
+    h->sh.w1s = c.take<float>(Is * H / 64);
+    h->sh.w3s = c.take<float>(Is * H / 64);
+    h->sh.w2s = c.take<float>(H * Is / 64);
+  }
+  moe::Workspace &w = h->ws;
+  const size_t zrows = maxT > (size_t)moe::kRouterSplitMax * moe::kGemvTokens
+                           ? maxT
+                           : (size_t)moe::kRouterSplitMax * moe::kGemvTokens;
+  w.z_part = c.take<float>(zrows * E);
+  w.idx = c.take<int32_t>(A);
+  w.w = c.take<float>(A);
+  w.counts = c.take<int32_t>(E);
+  w.offsets = c.take<int32_t>(E + 1);
+  w.perm = c.take<int32_t>(A);
+  w.inv = c.take<int32_t>(A);
+  w.active = c.take<int32_t>(E + 1);
+  w.n_active = c.take<int32_t>(1);
+  w.tiles = c.take<int32_t>(A / kTileM + E + maxT / kTileM + 2);
+  w.n_tiles = c.take<int32_t>(2);
+  w.status = c.take<int32_t>(1);
+  w.h = c.take<float>(rows * Imax);
+  w.hb = c.take<__nv_bfloat16>(rows * Imax);
+  w.y = c.take<float>(rows * H);
+  w.x_stage = c.take<char>(maxT * H * h->x_elem);
+  w.out_stage = c.take<float>(maxT * H);
+}
+
+int copy_weights(moe_handle *h, const moe_weights *W) {
+  const size_t E = h->E, H = h->H, I = h->I, Is = h->Is;
+  struct Job {
+    void *dst;
+    const void *src;
+    size_t bytes;
+  } jobs[] = {
+      {(void *)h->ex.w1q, W->w1_q, E * I * H / 2},  {(void *)h->ex.w3q, W->w3_q, E * I * H / 2},
+      {(void *)h->ex.w2q, W->w2_q, E * H * I / 2},  {(void *)h->ex.w1s, W->w1_s, E * I * H / 16},
+      {(void *)h->ex.w3s, W->w3_s, E * I * H / 16}, {(void *)h->ex.w2s, W->w2_s, E * H * I / 16},
+  };
+  for (const Job &j : jobs)
+    if (cudaMemcpy(j.dst, j.src, j.bytes, cudaMemcpyDefault) != cudaSuccess) return MOE_ERR_DEVICE;
+  if (h->S) {
+    Job sj[] = {
+        {(void *)h->sh.w1q, W->sw1_q, Is * H / 2}, {(void *)h->sh.w3q, W->sw3_q, Is * H / 2},
+        {(void *)h->sh.w2q, W->sw2_q, H * Is / 2}, {(void *)h->sh.w1s, W->sw1_s, Is * H / 16},
+        {(void *)h->sh.w3s, W->sw3_s, Is * H / 16}, {(void *)h->sh.w2s, W->sw2_s, H * Is / 16},
+    };
+    for (const Job &j : sj)
+      if (cudaMemcpy(j.dst, j.src, j.bytes, cudaMemcpyDefault) != cudaSuccess)
+        return MOE_ERR_DEVICE;
+  }
+  if (W->router_bias) {
+    if (cudaMemcpy(h->bias, W->router_bias, E * 4, cudaMemcpyDefault) != cudaSuccess)
+      return MOE_ERR_DEVICE;
+  } else if (cudaMemset(h->bias, 0, E * 4) != cudaSuccess) {
+    return MOE_ERR_DEVICE;
+  }
+  // Router: canonical [H][E] -> [E][H] through a temporary buffer.
+  float *tmp = nullptr;
+  if (fault_alloc(2) || cudaMalloc(&tmp, E * H * 4) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NOMEM;
+  }
+  int rc = MOE_OK;
+  if (cudaMemcpy(tmp, W->router_w, E * H * 4, cudaMemcpyDefault) != cudaSuccess ||
+      moe::launch_transpose_router(tmp, h->wr_t, (int)H, (int)E, 0) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    rc = MOE_ERR_DEVICE;
+  cudaFree(tmp);
+  return rc;
+}
+
+int choose_regime(const moe_handle *h, int T) {
+  if (h->regime_opt == 1) return 1;
+  if (h->regime_opt == 2) return 2;
+  if (!moe::tc_path_available()) return 1;
+  return T <= h->small_t_max ? 1 : 2;
+}
+
+int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate,
+                cudaStream_t st) {
+  int regime = choose_regime(h, T);
+  cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
+  if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
+  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, kTileM, st);
+  if (err == cudaSuccess) {
+    if (regime == 1) {
+      err = moe::launch_gemv_w13(h, x, T, st);
+      if (err == cudaSuccess) err = moe::launch_gemv_w2_combine(h, T, out, accumulate, st);
+    } else {
+      err = moe::launch_tc_path(h, x, T, out, accumulate, st);
+    }
+  }
+  h->last_T = T;
+  h->last_regime = regime;
+  h->last_stream = st;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+int check_call(moe_handle *h, const void *x, int T, const void *out) {
+  if (!h || T < 0) return MOE_ERR_ARG;
+  if (T > h->L.max_tokens) return MOE_ERR_NOMEM;
+  if (T > 0 && (!x || !out)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+__attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
+                                                    const moe_weights *weights,
+                                                    moe_handle **out) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  int rc = validate_layout(layout);
+  if (rc) return rc;
+  rc = validate_weights(layout, weights);
+  if (rc) return rc;
+  moe_handle *h = new (std::nothrow) moe_handle();
+  if (!h) return MOE_ERR_NOMEM;
+  h->L = *layout;
+  h->E = layout->num_experts;
+  h->k = layout->top_k;
+  h->H = layout->hidden;
+  h->I = layout->intermediate;
+  h->S = layout->n_shared;
+  h->Is = layout->n_shared ? layout->shared_intermediate : 0;
+  h->x_elem = layout->x_dtype == 1 ? 2 : 4;
+  h->regime_opt = 0;
+  h->small_t_max = 4;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_DEVICE;
+  }
+  Carver sizer{nullptr};
+  carve(h, sizer);
+  h->pool_bytes = align_up(sizer.off, kAlign);
+  if (fault_alloc(1) || cudaMalloc(&h->pool, h->pool_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    h->pool = nullptr;
+    delete h;
+    return MOE_ERR_NOMEM;
+  }
+  Carver c{static_cast<char *>(h->pool)};
+  carve(h, c);
+  rc = copy_weights(h, weights);
+  if (rc == MOE_OK && cudaMemset(h->ws.status, 0, 4) != cudaSuccess) rc = MOE_ERR_DEVICE;
+  if (rc != MOE_OK) {
+    cudaFree(h->pool);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_forward(moe_handle *h, const void *x, int T,
+                                                       float *out, moe_stream_t stream) {
+  int rc = check_call(h, x, T, out);
+  if (rc || T == 0) return rc;
+  return run_forward(h, x, T, out, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+__attribute__((visibility("default"))) int moe_route(moe_handle *h, const void *x, int T,
+                                                     moe_stream_t stream) {
+  int rc = check_call(h, x, T, x);
+  if (rc || T == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
+  if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
+  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, kTileM, st);
+  h->last_T = T;
+  h->last_regime = 0;
+  h->last_stream = st;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+__attribute__((visibility("default"))) int moe_forward_residual(moe_handle *h, const void *x,
+                                                                int T, float *resid,
+                                                                moe_stream_t stream) {
+  int rc = check_call(h, x, T, resid);
+  if (rc || T == 0) return rc;
+  return run_forward(h, x, T, resid, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+__attribute__((visibility("default"))) int moe_forward_host(moe_handle *h, const void *x_host,
+                                                            int T, float *out_host,
+                                                            moe_stream_t stream) {
+  int rc = check_call(h, x_host, T, out_host);
+  if (rc || T == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * h->H * h->x_elem, ob = (size_t)T * h->H * sizeof(float);
+  if (cudaMemcpyAsync(h->ws.x_stage, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  rc = run_forward(h, h->ws.x_stage, T, h->ws.out_stage, false, st);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out_host, h->ws.out_stage, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_rmsnorm_bf16(const float *x, int T, int H,
+                                                            float eps, uint16_t *out,
+                                                            moe_stream_t stream) {
+  if (T < 0 || H <= 0 || !(eps >= 0.f)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return MOE_ERR_ARG;
+  return moe::launch_rmsnorm_bf16(x, T, H, eps, out, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_DEVICE;
+}
+
+__attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int option, int value) {
+  if (!h) return MOE_ERR_ARG;
+  if (option == MOE_OPT_REGIME) {
+    if (value < 0 || value > 2) return MOE_ERR_ARG;
+    h->regime_opt = value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_SMALL_T_MAX) {
+    if (value < 0) return MOE_ERR_ARG;
+    h->small_t_max = value;
+    return MOE_OK;
+  }
+  return MOE_ERR_ARG;
+}
+
+__attribute__((visibility("default"))) int moe_debug_view(moe_handle *h, moe_debug *d) {
+  if (!h || !d) return MOE_ERR_ARG;
+  d->T = h->last_T;
+  d->idx = h->ws.idx;
+  d->w = h->ws.w;
+  d->counts = h->ws.counts;
+  d->offsets = h->ws.offsets;
+  d->perm = h->ws.perm;
+  d->inv = h->ws.inv;
+  d->status = h->ws.status;
+  d->regime = h->last_regime;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_debug_read(moe_handle *h, int field,
+                                                          void *host_dst, size_t bytes) {
+  if (!h || !host_dst) return MOE_ERR_ARG;
+  const size_t A = (size_t)h->last_T * h->k;
+  const void *src = nullptr;
+  size_t need = 0;
+  switch (field) {
+    case MOE_DBG_IDX: src = h->ws.idx; need = A * 4; break;
+    case MOE_DBG_W: src = h->ws.w; need = A * 4; break;
+    case MOE_DBG_COUNTS: src = h->ws.counts; need = (size_t)h->E * 4; break;
+    case MOE_DBG_OFFSETS: src = h->ws.offsets; need = (size_t)(h->E + 1) * 4; break;
+    case MOE_DBG_PERM: src = h->ws.perm; need = A * 4; break;
+    case MOE_DBG_INV: src = h->ws.inv; need = A * 4; break;
+    default: return MOE_ERR_ARG;
+  }
+  if (bytes != need) return MOE_ERR_ARG;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return MOE_ERR_DEVICE;
+  if (need && cudaMemcpy(host_dst, src, need, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_status(moe_handle *h, int32_t *status) {
+  if (!h || !status) return MOE_ERR_ARG;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return MOE_ERR_DEVICE;
+  if (cudaMemcpy(status, h->ws.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) size_t moe_device_bytes(const moe_handle *h) {
+  return h ? h->pool_bytes : 0;
+}
+
+__attribute__((visibility("default"))) void moe_free(moe_handle *h) {
+  if (!h) return;
+  if (h->pool) cudaFree(h->pool);
+  delete h;
+}
+
+__attribute__((visibility("default"))) const char *moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NOMEM: return "out of memory, or T > max_tokens";
+    case MOE_ERR_ROUTING: return "invalid routing layout";
+    case MOE_ERR_DEVICE: return "CUDA error or device status";
+    case MOE_ERR_ARG: return "invalid argument";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// moe_internal.cuh -- handle layout and kernel entry points shared by the
+// library's translation units.  Device code targets sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
+constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
+
+// Device status word codes (sticky until the next forward overwrites them).
+enum Status : int32_t {
+  kStatusOk = 0,
+  kStatusBadExpert = 1,       // a routed id outside [0, E)
+  kStatusTimeout = 2,         // a bounded wait gave up
+  kStatusBadTile = 3,         // a tile outside its expert's range
+};
+
+// Per-expert weight views into the library's device copy (canonical layout).
+struct ExpertWeights {
+  const uint8_t *w1q, *w3q, *w2q;   // [n_experts][rows][K/2]
+  const float *w1s, *w3s, *w2s;     // [n_experts][rows][K/64]
+};
+
+struct Workspace {
+  // routing
+  float *z_part;      // [splits][max_tokens][E] router partial logits
+  int32_t *idx;       // [max_tokens][k]
+  float *w;           // [max_tokens][k]
+  // dispatch
+  int32_t *counts;    // [E]
+  int32_t *offsets;   // [E+1]
+  int32_t *perm;      // [max_tokens*k]
+  int32_t *inv;       // [max_tokens*k]
+  int32_t *active;    // [E+1] ids of experts with tokens (ascending), shared = E last
+  int32_t *n_active;  // [1]
+  int32_t *tiles;     // [max_tiles] packed (expert, m-tile) for the tensor-core path
+  int32_t *n_tiles;   // [2] tile count for W13 and W2 kernels
+  int32_t *status;    // [1]
+  // expert activations
+  float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
+  __nv_bfloat16 *hb;  // [max_tokens*k + S*max_tokens][I_max] bf16 (tensor-core path)
+  float *y;           // [max_tokens*k + S*max_tokens][H] f32 (tensor-core path)
+  // host-call staging
+  void *x_stage;      // [max_tokens][H] (x dtype)
+  float *out_stage;   // [max_tokens][H]
+};
+
+}  // namespace moe
+
+struct moe_handle {
+  moe_layout L;
+  int E, k, H, I, S, Is;
+  size_t x_elem;                 // 4 (f32) or 2 (bf16)
+  // weights (device, library-owned)
+  float *wr_t;                   // [E][H] f32 router weights, transposed
+  float *bias;                   // [E] or nullptr
+  moe::ExpertWeights ex;         // routed experts
+  moe::ExpertWeights sh;         // shared expert (single)
+  moe::Workspace ws;
+  void *pool;                    // one device allocation holding everything
+  size_t pool_bytes;
+  int regime_opt;                // MOE_OPT_REGIME
+  int small_t_max;               // MOE_OPT_SMALL_T_MAX
+  int last_T;
+  int last_regime;
+  cudaStream_t last_stream;
+  int num_sms;
+};
+
+namespace moe {
+
+// router.cu
+cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t s);
+// dispatch.cu
+cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t s);
+// gemv.cu
+cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t s);
+cudaError_t launch_gemv_w2_combine(const moe_handle *h, int T, float *out, bool accumulate,
+                                   cudaStream_t s);
+// ggemm_tc.cu
+bool tc_path_available();
+cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,
+                           bool accumulate, cudaStream_t s);
+// misc.cu
+cudaError_t launch_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
+                                cudaStream_t s);
+cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, cudaStream_t s);
+
+}  // namespace moe

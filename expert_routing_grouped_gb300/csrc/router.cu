@@ -1,0 +1,254 @@
+// router.cu -- step 1-2 of the layer: f32 router logits, then top-k selection
+// with renormalised weights.
+//
+// The router stays f32 (colibrì engine teardown, text-matrix.pages.dev,
+// "System map": norm/router/bias are kept in f32 because they are small and
+// sensitive).  Scoring is softmax (Colibri C + cuBLASLt tutorial, cf-1.com,
+// §2.1 step 2) or sigmoid with a noaux_tc selection bias, n_group = 1, scaled
+// by routed_scaling_factor (teardown "Three key engineering decisions" (1)).
+//
+// Logits are plain f32 FMA (no TF32) so the selection matches an exact
+// reference whenever the top keys are separated by more than f32 rounding.
+// Every reduction runs in a fixed order, so results are bitwise reproducible.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float load_x(const void *x, int x_is_bf16, size_t i) {
+  if (x_is_bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i]);
+  return reinterpret_cast<const float *>(x)[i];
+}
+
+// ---------------------------------------------------------------------------
+// Small T (decode, MTP verify): split-K GEMV.  Block = 8 warps, one expert per
+// warp; blockIdx.y selects a contiguous H range.  x of the range is staged in
+// shared memory as f32.  Writes z_part[split][t][e].
+template <int NT>
+__global__ void __launch_bounds__(256) router_gemv_kernel(
+    const void *__restrict__ x, int x_is_bf16, int T, int H, int E,
+    const float *__restrict__ wr_t, int h_per_split, float *__restrict__ z_part,
+    int zstride) {
+  extern __shared__ float xs[];   // [NT][h_per_split]
+  const int split = blockIdx.y;
+  const int h0 = split * h_per_split;
+  for (int i = threadIdx.x; i < NT * h_per_split; i += blockDim.x) {
+    const int t = i / h_per_split, hh = i - t * h_per_split;
+    xs[i] = (t < T) ? load_x(x, x_is_bf16, (size_t)t * H + h0 + hh) : 0.f;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const float *wrow = wr_t + (size_t)e * H + h0;
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int hh = lane * 4; hh < h_per_split; hh += 128) {
+    const float4 wv = __ldg(reinterpret_cast<const float4 *>(wrow + hh));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float4 xv = *reinterpret_cast<const float4 *>(xs + t * h_per_split + hh);
+      acc[t] = fmaf(xv.x, wv.x, acc[t]);
+      acc[t] = fmaf(xv.y, wv.y, acc[t]);
+      acc[t] = fmaf(xv.z, wv.z, acc[t]);
+      acc[t] = fmaf(xv.w, wv.w, acc[t]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      if (t < T) z_part[((size_t)split * zstride + t) * E + e] = acc[t];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Large T: tiled SIMT SGEMM, z[t][e] = sum_h x[t][h] * wr_t[e][h].
+// Block tile 64 tokens x 64 experts, K step 16, 256 threads, 4x4 per thread.
+constexpr int RG_BT = 64, RG_BE = 64, RG_BK = 16;
+
+__global__ void __launch_bounds__(256) router_gemm_kernel(
+    const void *__restrict__ x, int x_is_bf16, int T, int H, int E,
+    const float *__restrict__ wr_t, float *__restrict__ z) {
+  __shared__ float xs[RG_BK][RG_BT + 4];
+  __shared__ float ws[RG_BK][RG_BE + 4];
+  const int t0 = blockIdx.y * RG_BT, e0 = blockIdx.x * RG_BE;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += RG_BK) {
+    // 64 x 16 elements of each operand, 4 per thread.
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x + r * 256;
+      const int row = i >> 4, kk = i & 15;
+      const int t = t0 + row, e = e0 + row;
+      xs[kk][row] = (t < T) ? load_x(x, x_is_bf16, (size_t)t * H + k0 + kk) : 0.f;
+      ws[kk][row] = (e < E) ? __ldg(wr_t + (size_t)e * H + k0 + kk) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < RG_BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) z[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k per token: one warp per token, expert e lives in lane e % 32, slot e / 32.
+// Keys: softmax mode, l = z + b; sigmoid mode, s = sigmoid(z), key = s + b.
+// k rounds of a warp argmax (larger key first, lower id on ties) give the
+// slots in descending key order.  Weights are renormalised over the selection
+// and times rsf: softmax w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); sigmoid
+// w_j = s_j / sum_i s_i.
+template <int EPL>
+__global__ void __launch_bounds__(256) router_topk_kernel(
+    const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k,
+    int mode, const float *__restrict__ bias, float rsf, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float key[EPL], val[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = -INFINITY;
+    val[i] = 0.f;
+    if (e < E) {
+      float zz = 0.f;
+      for (int s = 0; s < splits; ++s) zz += z_part[((size_t)s * zstride + t) * E + e];
+      const float b = bias ? bias[e] : 0.f;
+      if (mode == 0) {
+        key[i] = zz + b;
+        val[i] = key[i];
+      } else {
+        const float sc = 1.0f / (1.0f + expf(-zz));
+        val[i] = sc;
+        key[i] = sc + b;
+      }
+    }
+  }
+  int my_idx = -1;
+  float my_val = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bk = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (key[i] > bk) {   // ascending i: first maximum has the lowest id
+        bk = key[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ok > bk || (ok == bk && oe < be)) {
+        bk = ok;
+        be = oe;
+      }
+    }
+    // Owner removes the winner and broadcasts its value.
+    float v = 0.f;
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i == be) {
+          v = val[i];
+          key[i] = -INFINITY;
+        }
+    }
+    v = __shfl_sync(0xffffffffu, v, be & 31);
+    if (lane == j) {
+      my_idx = be;
+      my_val = v;
+    }
+  }
+  // Renormalise over the selection, summing in slot order.
+  const float top = __shfl_sync(0xffffffffu, my_val, 0);
+  float num = 0.f;
+  if (lane < k) num = (mode == 0) ? expf(my_val - top) : my_val;
+  float den = 0.f;
+  for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
+  if (lane < k) {
+    idx_out[(size_t)t * k + lane] = my_idx;
+    w_out[(size_t)t * k + lane] = num / den * rsf;
+  }
+}
+
+int router_splits(int T, int E, int H, int num_sms) {
+  if (T > 4) return 1;
+  const int blocks_e = (E + 7) / 8;
+  int s = 1;
+  // Split H until there are about two blocks per SM, keeping 128-float slices.
+  while (s < kRouterSplitMax && blocks_e * s < 2 * num_sms && (H % (2 * s * 128)) == 0) s *= 2;
+  return s;
+}
+
+}  // namespace
+
+cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t st) {
+  const int E = h->E, H = h->H, k = h->k;
+  const int xb = h->L.x_dtype == 1;
+  const int splits = router_splits(T, E, H, h->num_sms);
+  if (T <= 4) {
+    const int hps = H / splits;
+    const dim3 grid((E + 7) / 8, splits);
+    const size_t smem = (size_t)4 * hps * sizeof(float);
+    if (smem > 48 * 1024) {
+      cudaError_t err = cudaFuncSetAttribute(router_gemv_kernel<4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+    }
+    router_gemv_kernel<4><<<grid, 256, smem, st>>>(x, xb, T, H, E, h->wr_t, hps, h->ws.z_part,
+                                                   kGemvTokens);
+  } else {
+    const dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT);
+    router_gemm_kernel<<<grid, 256, 0, st>>>(x, xb, T, H, E, h->wr_t, h->ws.z_part);
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int zstride = (T <= 4) ? kGemvTokens : T;
+  const int epl = (E + 31) / 32;
+  const dim3 g2((T + 7) / 8);
+#define MOE_TOPK(N)                                                                          \
+  router_topk_kernel<N><<<g2, 256, 0, st>>>(h->ws.z_part, splits, zstride, T, E, k,          \
+                                            h->L.router_mode, h->bias,                      \
+                                            h->L.routed_scaling_factor, h->ws.idx, h->ws.w)
+  if (epl <= 1) MOE_TOPK(1);
+  else if (epl <= 2) MOE_TOPK(2);
+  else if (epl <= 4) MOE_TOPK(4);
+  else if (epl <= 8) MOE_TOPK(8);
+  else if (epl <= 16) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,205 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE-layer forward library, libmoe.so.
+ *
+ * One call runs one Mixture-of-Experts layer over T tokens on one GPU:
+ *
+ *   1. router   z = x . Wr (f32), then softmax top-k, or sigmoid scores with a
+ *               noaux_tc selection bias (n_group = 1); the k selected weights
+ *               are renormalised and multiplied by routed_scaling_factor.
+ *               (colibrì engine teardown, text-matrix.pages.dev, "Three key
+ *               engineering decisions" (1): sigmoid + noaux_tc with
+ *               routed_scaling_factor; "System map": router, norm and bias f32.
+ *               Colibri C + cuBLASLt tutorial, cf-1.com, §2.1 step 2: linear
+ *               layer + softmax -> top-k ids and weights.)
+ *   2. dispatch a counting sort that groups the T*k assignments by expert:
+ *               per-expert counts, prefix-sum offsets, a permutation, and no
+ *               allocation (tutorial cf-1.com §3.3 Step 3; pure-C Colibri
+ *               tutorial, trdm.cn, §2.2: a pre-allocated pool, only pointer
+ *               arithmetic at run time).
+ *   3. experts  SwiGLU FFN per expert over its group, y = W2 (silu(W1 x) * W3 x),
+ *               with int4 weights carrying one f32 scale per 64 weights along K
+ *               (gs64; teardown "Three key engineering decisions" (1)), plus an
+ *               always-applied shared expert (teardown "System map", tier 1).
+ *               Empty experts are skipped (tutorial cf-1.com §3.3 Step 4).
+ *   4. combine  out[t] = sum_j w[t][j] * y(t, j) + y_shared(t), in a fixed order,
+ *               without atomics (tutorial cf-1.com §3.3 Step 5).
+ *
+ * The API follows the pages' engine interface -- init with a maximum batch,
+ * forward, free; batch 0 is a dry run; negative return codes; one instance per
+ * thread (pure-C Colibri tutorial, trdm.cn, §4.2 and §5.1-5.2) -- with the
+ * layout and the CUDA stream made explicit.
+ *
+ * Canonical weight layout (what moe_init reads; host or device memory):
+ *   router_w     [H][E]     f32, row h holds the E logits' weights
+ *   router_bias  [E]        f32: softmax mode, an additive logit offset (may be
+ *                           NULL); sigmoid mode, the noaux_tc selection bias
+ *                           (required; it enters selection only)
+ *   w1_q, w3_q   [E][I][H/2] packed int4: byte b of a row holds K indices 2b
+ *                           (low nibble) and 2b+1 (high nibble); a nibble is a
+ *                           two's-complement value in [-8, 7]
+ *   w1_s, w3_s   [E][I][H/64] f32 gs64 scales: weight k of a row is q_k * s[k/64]
+ *   w2_q         [E][H][I/2] packed int4, w2_s [E][H][I/64] f32
+ *   sw*_q/_s     the shared expert's W1/W3 [Is][H/2],[Is][H/64] and W2
+ *                [H][Is/2],[H][Is/64]; NULL when n_shared == 0
+ * Experts are contiguous by id (tutorial cf-1.com §3.1: base + id * size).
+ *
+ * Numerics.  Routing, dispatch and the small-T expert path (T <= 4 by default)
+ * compute in f32.  The large-T expert path feeds the tensor cores with
+ * bf16(q * s) weights and bf16 activations and accumulates in f32.  The
+ * output is f32.  Results are bitwise identical from run to run.
+ *
+ * Return codes (extending the pages' 0 / -1 / -2 / -3):
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_NOMEM (-1)    /* out of memory at init, or T > max_tokens        */
+#define MOE_ERR_ROUTING (-2)  /* invalid routing layout: top_k < 1 or > E,
+                                 E > 1024, unknown router_mode                  */
+#define MOE_ERR_DEVICE (-3)   /* CUDA error, or a nonzero device status word     */
+#define MOE_ERR_ARG (-4)      /* NULL pointer, a size not a multiple of 64,
+                                 unsupported dtype, bad option                  */
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef struct moe_layout {
+  int32_t num_experts;           /* E, 1..1024                                   */
+  int32_t top_k;                 /* k, 1..min(E, 32)                             */
+  int32_t hidden;                /* H, a multiple of 512                         */
+  int32_t intermediate;          /* I, a multiple of 1024 (routed experts)       */
+  int32_t n_shared;              /* 0 or 1                                       */
+  int32_t shared_intermediate;   /* I of the shared expert (multiple of 1024)    */
+  int32_t router_mode;           /* 0 softmax, 1 sigmoid + noaux_tc, n_group 1   */
+  float routed_scaling_factor;   /* rsf (1.0 for plain softmax routers)          */
+  int32_t x_dtype;               /* 0 f32, 1 bf16                                */
+  int32_t max_tokens;            /* largest T a forward call may pass (>= 1)     */
+} moe_layout;
+
+typedef struct moe_weights {
+  const float *router_w;
+  const float *router_bias;
+  const uint8_t *w1_q;
+  const float *w1_s;
+  const uint8_t *w3_q;
+  const float *w3_s;
+  const uint8_t *w2_q;
+  const float *w2_s;
+  const uint8_t *sw1_q;
+  const float *sw1_s;
+  const uint8_t *sw3_q;
+  const float *sw3_s;
+  const uint8_t *sw2_q;
+  const float *sw2_s;
+} moe_weights;
+
+typedef struct moe_handle moe_handle;
+
+/* Device pointers into the handle's workspace, valid until the next forward
+ * on the handle.  They describe the last forward call. */
+typedef struct moe_debug {
+  int32_t T;               /* tokens of the last call                           */
+  const int32_t *idx;      /* [T][k] selected experts, slots by descending key  */
+  const float *w;          /* [T][k] renormalised weights times rsf             */
+  const int32_t *counts;   /* [E] assignments per expert                        */
+  const int32_t *offsets;  /* [E+1] exclusive prefix sum of counts             */
+  const int32_t *perm;     /* [T*k] grouped position -> assignment t*k+j        */
+  const int32_t *inv;      /* [T*k] assignment -> grouped position              */
+  const int32_t *status;   /* one int32 device status word (0 = ok)             */
+  int32_t regime;          /* 1 small-T GEMV path, 2 tensor-core path           */
+} moe_debug;
+
+/*
+ * Validates the layout, allocates all device memory the handle will ever use
+ * (repacked weights and a workspace sized for max_tokens), and copies the
+ * weights in.  Weight pointers may be host or device memory; they are not
+ * retained.  On failure *out is NULL and nothing is leaked.
+ * Returns MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_ARG or MOE_ERR_DEVICE.
+ */
+int moe_init(const moe_layout *layout, const moe_weights *weights, moe_handle **out);
+
+/*
+ * out[T][H] (f32, device) = MoE(x), x [T][H] device (f32 or bf16 per layout).
+ * Asynchronous on `stream`; no allocation, no host synchronisation.
+ * T == 0 validates the arguments and launches nothing (dry run; x and out may
+ * then be NULL).  T > max_tokens returns MOE_ERR_NOMEM.  A handle serves one
+ * stream at a time and is not thread-safe.
+ */
+int moe_forward(moe_handle *h, const void *x, int T, float *out, moe_stream_t stream);
+
+/* Steps 1-2 only: routes x [T][H] (device) and groups the assignments by
+ * expert, leaving idx, w, counts, offsets, perm and inv in the workspace (read
+ * them with moe_debug_view / moe_debug_read).  Lets a caller learn which
+ * experts the next call will stream before running it. */
+int moe_route(moe_handle *h, const void *x, int T, moe_stream_t stream);
+
+/* As moe_forward, but adds the layer output into resid[T][H] (f32, device):
+ * resid += MoE(x).  The residual add is fused into the combine step. */
+int moe_forward_residual(moe_handle *h, const void *x, int T, float *resid,
+                         moe_stream_t stream);
+
+/*
+ * End-to-end call with HOST buffers: copies x (host) into the handle's
+ * workspace, runs the layer, copies the result to out (host), and waits for
+ * the stream.  Pinned host memory gives the fastest copies.
+ */
+int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
+                     moe_stream_t stream);
+
+/*
+ * Pre-norm between stacked layers: out_bf16[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)),
+ * computed in f32 with no learned gain (the pages normalise with RMSNorm before
+ * the MoE layer: tutorial cf-1.com §2.1 step 1; the norm stays f32: teardown
+ * "System map").  x [T][H] f32 device, out [T][H] bf16 bits device.
+ */
+int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
+                     moe_stream_t stream);
+
+/* Chooses the expert path: 0 automatic (T <= small_t_max -> GEMV path,
+ * else tensor cores), 1 always GEMV, 2 always tensor cores. */
+#define MOE_OPT_REGIME 1
+/* Largest T that the automatic choice sends to the GEMV path (default 4). */
+#define MOE_OPT_SMALL_T_MAX 2
+int moe_set_option(moe_handle *h, int option, int value);
+
+/* Fills *d with device pointers describing the last forward call. */
+int moe_debug_view(moe_handle *h, moe_debug *d);
+
+/* Fields of moe_debug_read. */
+#define MOE_DBG_IDX 0      /* int32 [T][k]  */
+#define MOE_DBG_W 1        /* f32   [T][k]  */
+#define MOE_DBG_COUNTS 2   /* int32 [E]     */
+#define MOE_DBG_OFFSETS 3  /* int32 [E+1]   */
+#define MOE_DBG_PERM 4     /* int32 [T*k]   */
+#define MOE_DBG_INV 5      /* int32 [T*k]   */
+/* Synchronises the handle's last stream and copies one field of the last
+ * forward call into host memory; `bytes` must equal the field's size for the
+ * last call's T (MOE_ERR_ARG otherwise). */
+int moe_debug_read(moe_handle *h, int field, void *host_dst, size_t bytes);
+
+/* Synchronises the handle's last stream and returns its device status word
+ * (0 when every kernel completed normally). */
+int moe_status(moe_handle *h, int32_t *status);
+
+/* Bytes of device memory the handle owns (weights + workspace). */
+size_t moe_device_bytes(const moe_handle *h);
+
+/* Releases everything the handle owns; NULL is a no-op. */
+void moe_free(moe_handle *h);
+
+/* Text for a return code. */
+const char *moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -36,7 +36,7 @@ def build_dev(force=False):
         subprocess.check_call([nvcc, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
                                "-Xcompiler", "-fvisibility=hidden",
                                "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-                               "-o", DEV_SO, srcs[0]])
+                               "-cudart", "static", "-o", DEV_SO, srcs[0]])
     return DEV_SO
 
 

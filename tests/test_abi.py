@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/moe.h declares, and rejects bad arguments on the host before any CUDA
+call (the pages' return codes: pure-C Colibri tutorial, trdm.cn, §4.2)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for must in ("moe_init", "moe_forward", "moe_free"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    import expert_routing_grouped_gb300 as moe
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(moe.EXPORTS)
+
+
+def _layout(**kw):
+    import expert_routing_grouped_gb300 as moe
+    base = dict(num_experts=8, top_k=2, hidden=512, intermediate=1024, n_shared=0,
+                shared_intermediate=0, router_mode=0, routed_scaling_factor=1.0, x_dtype=0,
+                max_tokens=16)
+    base.update(kw)
+    return moe.MoeLayout(**base)
+
+
+def _init(layout, weights=True):
+    import expert_routing_grouped_gb300 as moe
+    dummy = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    W = moe.MoeWeights(**({n: dummy.value for n, _ in moe.MoeWeights._fields_} if weights else {}))
+    h = ctypes.c_void_p(1234)
+    rc = moe.lib.moe_init(ctypes.byref(layout), ctypes.byref(W), ctypes.byref(h))
+    return rc, h
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(top_k=0), -2), (dict(top_k=9), -2), (dict(num_experts=0), -2),
+    (dict(num_experts=2000, top_k=2), -2), (dict(router_mode=3), -2),
+    (dict(routed_scaling_factor=0.0), -2), (dict(top_k=33, num_experts=64), -2),
+    (dict(hidden=500), -4), (dict(hidden=0), -4), (dict(intermediate=1000), -4),
+    (dict(n_shared=1, shared_intermediate=0), -4), (dict(n_shared=2), -4),
+    (dict(x_dtype=5), -4), (dict(max_tokens=0), -4),
+])
+def test_init_rejects_bad_layout(kw, code):
+    rc, h = _init(_layout(**kw))
+    assert rc == code
+    assert h.value is None
+
+
+def test_init_rejects_missing_weights():
+    rc, h = _init(_layout(), weights=False)
+    assert rc == -4 and h.value is None
+
+
+def test_init_sigmoid_needs_bias():
+    import expert_routing_grouped_gb300 as moe
+    W = moe.MoeWeights(**{n: 16 for n, _ in moe.MoeWeights._fields_})
+    W.router_bias = None
+    h = ctypes.c_void_p()
+    rc = moe.lib.moe_init(ctypes.byref(_layout(router_mode=1)), ctypes.byref(W), ctypes.byref(h))
+    assert rc == -4
+
+
+def test_null_handle_calls():
+    import expert_routing_grouped_gb300 as moe
+    assert moe.lib.moe_forward(None, None, 1, None, None) == -4
+    assert moe.lib.moe_forward_host(None, None, 1, None, None) == -4
+    assert moe.lib.moe_set_option(None, 1, 0) == -4
+    assert moe.lib.moe_debug_view(None, None) == -4
+    assert moe.lib.moe_device_bytes(None) == 0
+    moe.lib.moe_free(None)
+    assert moe.lib.moe_rmsnorm_bf16(None, 0, 64, 1e-6, None, None) == 0     # dry run
+    assert moe.lib.moe_rmsnorm_bf16(None, 2, 64, 1e-6, None, None) == -4
+
+
+def test_strerror():
+    import expert_routing_grouped_gb300 as moe
+    assert moe.lib.moe_strerror(0) == b"ok"
+    assert b"max_tokens" in moe.lib.moe_strerror(-1)
+    assert moe.lib.moe_strerror(-2) == b"invalid routing layout"

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path through the C ABI against the f64 oracle on the
+same seeded inputs.
+
+Bars: routing ids, counts, offsets, perm and inv bit-exact (inputs keep the
+top-(k+1) keys >= 1e-4 apart); weights within 1e-6 relative; the small-T GEMV
+path's output within relative L2 1e-4 of the oracle; repeated calls bitwise
+identical."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.workloads import Workload
+from gpu_inputs import make_layer, oracle_layer, rel_l2, to_device_x
+from inputs import margin_x
+
+pytestmark = pytest.mark.gpu
+
+GEMV_TOL = 1e-4
+W_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    import expert_routing_grouped_gb300  # noqa: F401  (fails loudly if the library is missing)
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+_layers = {}
+
+
+def get_layer(wl, max_tokens, dev, layer=0):
+    key = (wl.name, layer, max_tokens)
+    if key not in _layers:
+        for k in list(_layers):          # keep one big layer resident at a time
+            _layers.pop(k)[0].close()
+        _layers[key] = make_layer(wl, layer, max_tokens, dev)
+    return _layers[key]
+
+
+def run_and_compare(wl, T, dev, regime=None, layer=0):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    h, Wr, bias = get_layer(wl, max(T, 4), dev, layer)
+    if regime is not None:
+        h.set_option(moe.MOE_OPT_REGIME, regime)
+    x, _ = margin_x(wl, T, Wr, bias)
+    ref = oracle_layer(wl, layer, x, Wr, bias)
+    xd = to_device_x(wl, x, dev)
+    out = torch.full((T, wl.H), float("nan"), device=dev)
+    h.forward(xd, T, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert h.status() == 0
+    idx = h.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k)
+    w = h.debug_read(moe.MOE_DBG_W).reshape(T, wl.k)
+    assert np.array_equal(idx, ref["idx"])
+    assert np.max(np.abs(w - ref["w"]) / np.abs(ref["w"])) < W_TOL
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_COUNTS), ref["counts"])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_OFFSETS), ref["offsets"])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM), ref["perm"])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_INV), ref["inv"])
+    assert np.all(np.isfinite(got))
+    return got, ref, h, xd
+
+
+def test_device_generator_matches_host(dev):
+    import torch
+    per = 4096
+    t = torch.empty(3 * per, dtype=torch.uint8, device=dev)
+    synth.dev_fill_int4(7, 2, synth.T_W2Q, 5, per, 3, t.data_ptr())
+    s = torch.empty(3 * 64, dtype=torch.float32, device=dev)
+    synth.dev_fill_scales(7, 2, synth.T_W2S, 5, 64, 3, s.data_ptr())
+    torch.cuda.synchronize()
+    for e in range(3):
+        assert np.array_equal(t[e * per:(e + 1) * per].cpu().numpy(),
+                              synth.int4(7, 2, synth.T_W2Q, 5 + e, per))
+        assert np.array_equal(s[e * 64:(e + 1) * 64].cpu().numpy(),
+                              synth.scales(7, 2, synth.T_W2S, 5 + e, 64))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("olmoe", 1), ("olmoe", 3),
+                                    ("mixtral", 1), ("mixtral", 4), ("glm_decode", 1),
+                                    ("glm_decode", 2), ("glm_decode", 4)])
+def test_gemv_path_parity(dev, name, T):
+    wl = synth.BY_NAME[name]
+    got, ref, _, _ = run_and_compare(wl, T, dev)
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+
+
+def test_gemv_path_parity_olmoe_64(dev):
+    """OLMoE-shaped T=64 (Zipf routing) forced onto the GEMV path."""
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["olmoe"]
+    got, ref, h, _ = run_and_compare(wl, 64, dev, regime=moe.REGIME_GEMV)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+
+
+@pytest.mark.parametrize("name,T", [("glm_prefill", 4096), ("mixtral", 512), ("olmoe", 64)])
+def test_routing_and_dispatch_full_size(dev, name, T):
+    """moe_route at full size: ids, weights and the grouping bit-exact."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME[name]
+    h, Wr, bias = get_layer(wl, T, dev)
+    x, _ = margin_x(wl, T, Wr, bias)
+    L = oracle.layout(wl)
+    idx, w, _, _ = oracle.route(L, oracle.weights(L, Wr, bias), x)
+    counts, offsets, perm, inv = oracle.dispatch(idx, wl.E)
+    h.route(to_device_x(wl, x, dev), T)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k), idx)
+    gw = h.debug_read(moe.MOE_DBG_W).reshape(T, wl.k)
+    assert np.max(np.abs(gw - w) / w) < W_TOL
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_COUNTS), counts)
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_OFFSETS), offsets)
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM), perm)
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_INV), inv)
+    if name == "glm_prefill":
+        assert counts.max() > 5 * counts.mean()    # the heavy Zipf imbalance is present
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("glm_decode", 4)])
+def test_repeated_calls_bitwise_identical(dev, name, T):
+    import torch
+    wl = synth.BY_NAME[name]
+    got, _, h, xd = run_and_compare(wl, T, dev)
+    for _ in range(3):
+        out = torch.empty(T, wl.H, device=dev)
+        h.forward(xd, T, out)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), got)
+
+
+def test_dry_run_and_limits(dev):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["tiny"]
+    h, _, _ = get_layer(wl, 16, dev)
+    assert moe.lib.moe_forward(h.handle, None, 0, None, None) == 0        # dry run
+    x = torch.zeros(17, wl.H, device=dev)
+    out = torch.zeros(17, wl.H, device=dev)
+    assert moe.lib.moe_forward(h.handle, x.data_ptr(), 17, out.data_ptr(), None) == -1
+    assert moe.lib.moe_forward(h.handle, None, 3, out.data_ptr(), None) == -4
+    assert moe.lib.moe_set_option(h.handle, 99, 0) == -4
+
+
+def test_forward_host_and_residual(dev):
+    import torch
+    wl = synth.BY_NAME["glm_decode"]
+    T = 3
+    got, ref, h, xd = run_and_compare(wl, T, dev)
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+    x_host = xd.cpu().numpy()
+    out_host = np.zeros((T, wl.H), np.float32)
+    h.forward_host(x_host, T, out_host)
+    assert np.array_equal(out_host, got)
+    resid = torch.from_numpy(np.arange(T * wl.H, dtype=np.float32).reshape(T, wl.H) * 1e-3).to(dev)
+    base = resid.cpu().numpy().copy()
+    h.forward_residual(xd, T, resid)
+    torch.cuda.synchronize()
+    assert np.array_equal(resid.cpu().numpy(), (base + got).astype(np.float32))
+
+
+def test_rmsnorm_bf16_within_one_ulp(dev):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    rng = np.random.default_rng(0)
+    x = (rng.normal(0, 5, (5, 6144))).astype(np.float32)
+    out = torch.empty(5, 6144, dtype=torch.int16, device=dev)
+    moe.rmsnorm_bf16(torch.from_numpy(x).to(dev), 5, 6144, 1e-6, out)
+    torch.cuda.synchronize()
+    got = synth.bf16_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+    ref = oracle.rmsnorm(x, 1e-6)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
+    assert np.all(np.abs(got - ref) <= ulp)
+
+
+@pytest.mark.parametrize("E,k,mode", [(4, 4, 0), (1, 1, 0), (4, 4, 1), (16, 1, 1)])
+def test_edge_layouts(dev, E, k, mode):
+    """k = E (the selection is every expert), a single expert, top-1."""
+    wl = Workload("edge%d_%d_%d" % (E, k, mode), H=512, E=E, k=k, I=1024,
+                  n_shared=mode, I_shared=1024 if mode else 0, router_mode=mode,
+                  rsf=2.5 if mode else 1.0, x_dtype=1, tokens=(5,), seed=40 + E + k,
+                  bias="normal" if mode else "none", bias_sigma=0.1)
+    got, ref, _, _ = run_and_compare(wl, 5, dev)
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+
+
+def test_init_fault_injection_leaks_nothing(dev):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    from gpu_inputs import device_weights
+    wl = synth.BY_NAME["olmoe"]
+    t, _, _ = device_weights(wl, 0, dev)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for n in ("1", "2"):
+        os.environ["MOE_FAULT_ALLOC_AT"] = n
+        try:
+            with pytest.raises(moe.MoeError) as ei:
+                moe.MoELayer(moe.layout_for(wl, 64), t)
+            assert ei.value.code == moe.MOE_ERR_NOMEM
+        finally:
+            del os.environ["MOE_FAULT_ALLOC_AT"]
+    torch.cuda.synchronize()
+    assert abs(torch.cuda.mem_get_info()[0] - free0) < (64 << 20)
+    h = moe.MoELayer(moe.layout_for(wl, 64), t)
+    assert h.device_bytes() > 0
+    h.close()
