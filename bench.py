@@ -1,0 +1,431 @@
+"""Benchmark of the MoE-layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload both|prefill|decode]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+Workloads (seeded synthetic inputs, no dataset, no trained weights):
+  prefill  one GLM-5.2-style layer (H 6144, 256 routed experts + 1 shared,
+           top-8, I 2048, sigmoid + noaux_tc, rsf 2.5, int4 gs64) on a batch of
+           T = 4096 tokens with Zipf(1.2) expert loads.  Step = one layer pass.
+  decode   the GLM-5.2-style decode stack: 8 such layers with an f32 residual and
+           an RMS pre-norm between layers, T = 1 token.  Step = the 8 layers.
+With --workload both (default) the JSON line's headline is the prefill step and
+a "decode" object carries the decode step.  Metric: MoE-layer tokens/s.
+
+Multi-GPU (torchrun): replicas only -- each rank runs its own replica, no data
+is exchanged; value = tokens of all ranks / max time over ranks.
+
+--impl reference times the f64 oracle (plain C, one host core) on a bounded
+sample of the same workload: the slow reference arm.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# --------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- helpers --
+
+def distinct_active(idx_rows, n_shared):
+    return len(np.unique(idx_rows)) + n_shared
+
+
+def layer_bytes(wl, n_active, T):
+    """Algorithmic bytes of one layer: activated experts' packed int4 + gs64
+    scales, router, bias, x (bf16) and out (f32)."""
+    return (n_active * 3 * wl.H * wl.I * 9 // 16 + wl.H * wl.E * 4 + wl.E * 4
+            + T * wl.H * 2 + T * wl.H * 4)
+
+
+def layer_flops(wl, T):
+    return 2 * T * (wl.k + wl.n_shared) * 3 * wl.H * wl.I + 2 * T * wl.H * wl.E
+
+
+# -------------------------------------------------------------- prefill --
+
+def bench_prefill(dev, steps, warmup, stream):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_inputs import make_layer
+    wl = synth.BY_NAME["glm_prefill"]
+    T = 4096
+    layer, Wr, bias = make_layer(wl, 0, T, dev)
+    x = synth.x_rows(wl, T)
+    xd = torch.from_numpy(x).to(dev)
+    out = torch.empty(T, wl.H, device=dev)
+    layer.set_option(moe.MOE_OPT_PROFILE, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            layer.forward(xd, T, out, stream)
+    torch.cuda.synchronize()
+    regime = layer.debug_view().regime
+    counts = layer.debug_read(moe.MOE_DBG_COUNTS)
+    launches0 = layer.debug_view().launches
+    stage = {}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            evs[i][0].record(stream)
+            layer.forward(xd, T, out, stream)
+            evs[i][1].record(stream)
+            for name, ms in layer.stage_times():     # synchronises each step
+                stage.setdefault(name, []).append(ms)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    launches = layer.debug_view().launches - launches0
+    # e2e: host buffers through the C ABI, copies inside the timed region
+    xh = torch.from_numpy(x).pin_memory()
+    oh = torch.empty(T, wl.H, dtype=torch.float32).pin_memory()
+    layer.set_option(moe.MOE_OPT_PROFILE, 0)
+    for _ in range(2):
+        layer.forward_host(xh, T, oh, stream)
+    torch.cuda.synchronize()
+    e2e = []
+    for _ in range(max(3, steps // 2)):
+        t1 = time.perf_counter()
+        layer.forward_host(xh, T, oh, stream)   # synchronises
+        e2e.append(time.perf_counter() - t1)
+    res = dict(wl=wl, T=T, step_ms=step_ms, stage={k: statistics.mean(v) for k, v in stage.items()},
+               launches=launches, regime=regime, counts=counts, clocks=clk.summary(),
+               e2e_s=statistics.median(e2e), h2d=x.nbytes, d2h=T * wl.H * 4, wall=wall)
+    layer.close()
+    del xd, out
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------- decode --
+
+def bench_decode(dev, steps, warmup, stream, T=1):
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_inputs import make_layer
+    wl = synth.BY_NAME["glm_decode"]
+    layers = [make_layer(wl, l, 4, dev)[0] for l in range(wl.layers)]
+    x = synth.x_rows(wl, T)
+    x32 = torch.from_numpy(synth.bf16_to_f32(x)).to(dev)
+    resid = torch.empty(T, wl.H, device=dev)
+    u = torch.empty(T, wl.H, dtype=torch.int16, device=dev)
+
+    def step():
+        resid.copy_(x32)
+        for lay in layers:
+            moe.rmsnorm_bf16(resid, T, wl.H, 1e-6, u, stream)
+            lay.forward_residual(u, T, resid, stream)
+
+    for lay in layers:
+        lay.set_option(moe.MOE_OPT_PROFILE, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    n_active = []
+    for lay in layers:
+        idx = lay.debug_read(moe.MOE_DBG_IDX)
+        n_active.append(distinct_active(idx, wl.n_shared))
+    launches0 = sum(l.debug_view().launches for l in layers)
+    stage = {}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        with ClockSampler(dev.index or 0) as clk:
+            for i in range(steps):
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
+                torch.cuda.synchronize()
+                for lay in layers:
+                    for name, ms in lay.stage_times():
+                        stage.setdefault(name, []).append(ms)
+            torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    launches = sum(l.debug_view().launches for l in layers) - launches0 + steps * wl.layers
+    # e2e: pinned host x -> device, the stack, result -> host, per step
+    xh = torch.from_numpy(synth.bf16_to_f32(x)).pin_memory()
+    oh = torch.empty(T, wl.H).pin_memory()
+    for lay in layers:
+        lay.set_option(moe.MOE_OPT_PROFILE, 0)
+    e2e = []
+    with torch.cuda.stream(stream):
+        for i in range(max(3, steps // 2) + 2):
+            t1 = time.perf_counter()
+            x32.copy_(xh, non_blocking=True)
+            step()
+            oh.copy_(resid, non_blocking=True)
+            stream.synchronize()
+            if i >= 2:
+                e2e.append(time.perf_counter() - t1)
+    res = dict(wl=wl, T=T, step_ms=step_ms,
+               stage={k: statistics.mean(v) for k, v in stage.items()},
+               launches=launches, n_active=n_active, clocks=clk.summary(),
+               e2e_s=statistics.median(e2e), h2d=T * wl.H * 4, d2h=T * wl.H * 4)
+    for lay in layers:
+        lay.close()
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------- cpu baseline --
+
+def oracle_sample(wl, rows, x):
+    """Time the oracle as it stands on x[rows] of the workload (layer 0)."""
+    import oracle
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from inputs import oracle_weights_for
+    Wr = synth.router_w(wl)
+    bias = synth.router_bias(wl)
+    t0 = time.perf_counter()
+    L = oracle.layout(wl)
+    idx, _, _, _ = oracle.route(L, oracle.weights(L, Wr, bias), x[rows])
+    L, W, _, _ = oracle_weights_for(wl, 0, Wr, bias, np.unique(idx))
+    oracle.moe_forward(L, W, x[rows])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, T, n_tokens, layers_per_step=1):
+    import synth
+    x = synth.x_rows(wl, T)
+    rows = np.arange(n_tokens)
+    dt = oracle_sample(wl, rows, x)
+    return {"value": n_tokens / (dt * layers_per_step), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": "oracle f64 (plain C, 1 thread) on tokens 0..%d of the %s batch through "
+                      "one layer (routing, dispatch, expert FFNs incl. host weight generation, "
+                      "combine): %.1f s, scaled to %d layer(s) per step"
+                      % (n_tokens - 1, wl.name, dt, layers_per_step)}
+
+
+# ------------------------------------------------------------------ main --
+
+def roofline_tc(res, pk, src):
+    wl, T = res["wl"], res["T"]
+    rows = T * wl.k + wl.n_shared * T
+    fl = 2 * rows * wl.H * 2 * wl.I
+    ms = res["stage"].get("w13")
+    if not ms:
+        return None
+    ach = fl / (ms * 1e-3) / 1e12
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    return {"kernel": "ggemm_w13_tc", "bound": "tensor", "achieved": round(ach, 1),
+            "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+            "peak_source": "%s bf16_tflops_sustained" % src,
+            "per_launch": "2*(T*k+T)*H*2I = %.3g FLOP" % fl}
+
+
+def roofline_gemv(res, pk, src):
+    wl, T = res["wl"], res["T"]
+    ms = res["stage"].get("w13")
+    if not ms:
+        return None
+    na = statistics.mean(res["n_active"])
+    by = na * 2 * wl.H * wl.I * 9 // 16 + T * wl.H * 2
+    ach = by / (ms * 1e-3) / 1e9
+    return {"kernel": "gemv_w13", "bound": "hbm", "achieved": round(ach, 1),
+            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+            "traffic": None, "peak_source": "%s hbm_gbs" % src,
+            "per_launch": "%.1f activated experts x 2*H*I*0.5625 B + x" % na}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="both", choices=["both", "prefill", "decode"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    import synth
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = synth.BY_NAME["glm_prefill" if args.workload != "decode" else "glm_decode"]
+        T = 4096 if wl.name == "glm_prefill" else 1
+        x = synth.x_rows(wl, T)
+        for _ in range(min(args.warmup, 1)):
+            oracle_sample(wl, np.arange(1), x)
+        times = [oracle_sample(wl, np.arange(1), x) for _ in range(args.steps)]
+        v = 1.0 / statistics.mean(times)
+        line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": v,
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "sample_tokens_per_step": 1},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": "1 token of the %s batch per step" % wl.name},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import expert_routing_grouped_gb300 as moe  # noqa: F401  (no fallback: fails if unbuilt)
+    stream = torch.cuda.Stream()
+    pk, src = peaks()
+
+    do_prefill = args.workload in ("both", "prefill")
+    do_decode = args.workload in ("both", "decode")
+    pre = dec = None
+    if do_prefill:
+        pre = bench_prefill(dev, args.steps, args.warmup, stream)
+        if pre["regime"] != 2 and args.workload == "both":
+            pre = None          # tensor-core path unavailable: decode becomes the headline
+    if do_decode:
+        dec = bench_decode(dev, args.steps, args.warmup, stream)
+
+    def reduce_max(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    head = pre if pre is not None else dec
+    ms = reduce_max(statistics.mean(head["step_ms"]))
+    tokens = head["T"] * world
+    value = tokens / (ms * 1e-3)
+    line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if head is pre else "f32", "data": "synthetic",
+            "config": {"workload": head["wl"].name, "T": head["T"],
+                       "layers_per_step": 1 if head is pre else head["wl"].layers,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (weights %.1f GB per step)"
+                             % ((layer_bytes(head["wl"], head["wl"].E + 1, head["T"]) if head is pre
+                                 else sum(layer_bytes(head["wl"], a, head["T"]) for a in head["n_active"])) / 1e9)},
+            "gpu_launches": int(head["launches"]),
+            "stage_ms": {k: round(v, 4) for k, v in head["stage"].items()},
+            "clocks": head["clocks"],
+            "e2e": {"value": head["T"] * world / reduce_max(head["e2e_s"]), "unit": "tokens/s",
+                    "h2d_bytes_per_step": head["h2d"], "d2h_bytes_per_step": head["d2h"]}}
+    line["roofline"] = roofline_tc(head, pk, src) if head is pre else roofline_gemv(head, pk, src)
+    if head is pre:
+        c = head["counts"]
+        line["config"]["expert_loads"] = {"max": int(c.max()), "empty": int((c == 0).sum()),
+                                          "cv": round(float(c.std() / c.mean()), 3)}
+        line["tflops"] = layer_flops(head["wl"], head["T"]) / (ms * 1e-3) / 1e12
+    if dec is not None and head is not dec:
+        dms = statistics.mean(dec["step_ms"])
+        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
+        line["decode"] = {"workload": "glm_decode x%d layers" % dec["wl"].layers, "T": dec["T"],
+                          "tokens_per_s": dec["T"] / (dms * 1e-3), "ms_per_step": dms,
+                          "us_per_layer": 1e3 * dms / dec["wl"].layers,
+                          "hbm_gbs": byts / (dms * 1e-3) / 1e9,
+                          "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
+                          "roofline": roofline_gemv(dec, pk, src)}
+    elif head is dec:
+        dms = ms
+        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
+        line["hbm_gbs"] = byts / (dms * 1e-3) / 1e9
+        line["hbm_frac"] = line["hbm_gbs"] / pk["hbm_gbs"]
+        line["us_per_layer"] = 1e3 * dms / dec["wl"].layers
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(head["wl"], head["T"], 8 if head is pre else 1,
+                                            1 if head is pre else head["wl"].layers)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

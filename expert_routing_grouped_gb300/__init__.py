@@ -12,7 +12,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_DEVICE, MOE_ERR_ARG = 0, -1, -2, -3, -4
-MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX = 1, 2
+MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE = 1, 2, 3
 REGIME_AUTO, REGIME_GEMV, REGIME_TC = 0, 1, 2
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 X_F32, X_BF16 = 0, 1
@@ -21,7 +21,7 @@ MOE_DBG_IDX, MOE_DBG_W, MOE_DBG_COUNTS, MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_I
 
 EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual", "moe_forward_host",
            "moe_rmsnorm_bf16", "moe_set_option", "moe_debug_view", "moe_debug_read",
-           "moe_status", "moe_device_bytes", "moe_free", "moe_strerror")
+           "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror")
 
 
 class MoeLayout(ctypes.Structure):
@@ -42,7 +42,8 @@ class MoeDebug(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("idx", ctypes.c_void_p), ("w", ctypes.c_void_p),
                 ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
                 ("perm", ctypes.c_void_p), ("inv", ctypes.c_void_p),
-                ("status", ctypes.c_void_p), ("regime", ctypes.c_int32)]
+                ("status", ctypes.c_void_p), ("regime", ctypes.c_int32),
+                ("launches", ctypes.c_int64)]
 
 
 def _load():
@@ -61,6 +62,7 @@ def _load():
         "moe_set_option": (i, [P, i, i]),
         "moe_debug_view": (i, [P, P]),
         "moe_debug_read": (i, [P, i, P, ctypes.c_size_t]),
+        "moe_stage_times": (i, [P, P, P, i, P]),
         "moe_status": (i, [P, P]),
         "moe_device_bytes": (ctypes.c_size_t, [P]),
         "moe_free": (None, [P]),
@@ -152,6 +154,14 @@ class MoELayer:
         a = np.zeros(n, np.float32 if field == MOE_DBG_W else np.int32)
         _check(lib.moe_debug_read(self._handle, field, a.ctypes.data, a.nbytes), "moe_debug_read")
         return a
+
+    def stage_times(self):
+        """[(stage name, ms)] of the last forward (needs MOE_OPT_PROFILE = 1)."""
+        ms = (ctypes.c_float * 8)()
+        names = (ctypes.c_char_p * 8)()
+        n = ctypes.c_int()
+        _check(lib.moe_stage_times(self._handle, ms, names, 8, ctypes.byref(n)), "moe_stage_times")
+        return [(names[i].decode(), ms[i]) for i in range(n.value)]
 
     def status(self):
         s = ctypes.c_int32()

@@ -159,16 +159,33 @@ int choose_regime(const moe_handle *h, int T) {
   return T <= h->small_t_max ? 1 : 2;
 }
 
+// Records the boundary after a stage when tracing is on.
+void mark(moe_handle *h, const char *name, cudaStream_t st) {
+  if (!h->profile || h->n_ev > moe_handle::kMaxStages) return;
+  if (h->n_ev > 0) h->stage_names[h->n_ev - 1] = name;
+  cudaEventRecord(h->ev[h->n_ev++], st);
+}
+
 int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate,
                 cudaStream_t st) {
   int regime = choose_regime(h, T);
+  h->n_ev = 0;
   cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
+  mark(h, nullptr, st);
   if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
+  h->launches += 2;
+  mark(h, "router", st);
   if (err == cudaSuccess) err = moe::launch_dispatch(h, T, kTileM, st);
+  h->launches += 1;
+  mark(h, "dispatch", st);
   if (err == cudaSuccess) {
     if (regime == 1) {
       err = moe::launch_gemv_w13(h, x, T, st);
+      h->launches += 1;
+      mark(h, "w13", st);
       if (err == cudaSuccess) err = moe::launch_gemv_w2_combine(h, T, out, accumulate, st);
+      h->launches += 1;
+      mark(h, "w2+combine", st);
     } else {
       err = moe::launch_tc_path(h, x, T, out, accumulate, st);
     }
@@ -310,6 +327,16 @@ __attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int opt
     h->small_t_max = value;
     return MOE_OK;
   }
+  if (option == MOE_OPT_PROFILE) {
+    if (value != 0 && value != 1) return MOE_ERR_ARG;
+    if (value && !h->ev[0]) {
+      for (int i = 0; i <= moe_handle::kMaxStages; ++i)
+        if (cudaEventCreate(&h->ev[i]) != cudaSuccess) return MOE_ERR_DEVICE;
+    }
+    h->profile = value;
+    h->n_ev = 0;
+    return MOE_OK;
+  }
   return MOE_ERR_ARG;
 }
 
@@ -324,6 +351,7 @@ __attribute__((visibility("default"))) int moe_debug_view(moe_handle *h, moe_deb
   d->inv = h->ws.inv;
   d->status = h->ws.status;
   d->regime = h->last_regime;
+  d->launches = h->launches;
   return MOE_OK;
 }
 
@@ -349,6 +377,21 @@ __attribute__((visibility("default"))) int moe_debug_read(moe_handle *h, int fie
   return MOE_OK;
 }
 
+__attribute__((visibility("default"))) int moe_stage_times(moe_handle *h, float *ms,
+                                                           const char **names, int max, int *n) {
+  if (!h || !ms || !n || max < 0) return MOE_ERR_ARG;
+  *n = 0;
+  if (!h->profile || h->n_ev < 2) return MOE_OK;
+  if (cudaEventSynchronize(h->ev[h->n_ev - 1]) != cudaSuccess) return MOE_ERR_DEVICE;
+  const int stages = h->n_ev - 1;
+  for (int i = 0; i < stages && i < max; ++i) {
+    if (cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]) != cudaSuccess) return MOE_ERR_DEVICE;
+    if (names) names[i] = h->stage_names[i];
+  }
+  *n = stages < max ? stages : max;
+  return MOE_OK;
+}
+
 __attribute__((visibility("default"))) int moe_status(moe_handle *h, int32_t *status) {
   if (!h || !status) return MOE_ERR_ARG;
   if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return MOE_ERR_DEVICE;
@@ -364,6 +407,8 @@ __attribute__((visibility("default"))) size_t moe_device_bytes(const moe_handle 
 __attribute__((visibility("default"))) void moe_free(moe_handle *h) {
   if (!h) return;
   if (h->pool) cudaFree(h->pool);
+  for (int i = 0; i <= moe_handle::kMaxStages; ++i)
+    if (h->ev[i]) cudaEventDestroy(h->ev[i]);
   delete h;
 }
 

@@ -73,6 +73,13 @@ struct moe_handle {
   int last_regime;
   cudaStream_t last_stream;
   int num_sms;
+  // tracing
+  int profile;                   // MOE_OPT_PROFILE
+  static constexpr int kMaxStages = 8;
+  cudaEvent_t ev[kMaxStages + 1];
+  int n_ev;                      // events recorded by the last forward
+  const char *stage_names[kMaxStages];
+  long long launches;            // kernels launched since init
 };
 
 namespace moe {

@@ -115,6 +115,7 @@ typedef struct moe_debug {
   const int32_t *inv;      /* [T*k] assignment -> grouped position              */
   const int32_t *status;   /* one int32 device status word (0 = ok)             */
   int32_t regime;          /* 1 small-T GEMV path, 2 tensor-core path           */
+  int64_t launches;        /* kernels launched by this handle since moe_init    */
 } moe_debug;
 
 /*
@@ -168,6 +169,9 @@ int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
 #define MOE_OPT_REGIME 1
 /* Largest T that the automatic choice sends to the GEMV path (default 4). */
 #define MOE_OPT_SMALL_T_MAX 2
+/* 1: record a CUDA event on the forward's stream at every stage boundary
+ * (read the stage times with moe_stage_times); 0 (default): no events. */
+#define MOE_OPT_PROFILE 3
 int moe_set_option(moe_handle *h, int option, int value);
 
 /* Fills *d with device pointers describing the last forward call. */
@@ -184,6 +188,12 @@ int moe_debug_view(moe_handle *h, moe_debug *d);
  * forward call into host memory; `bytes` must equal the field's size for the
  * last call's T (MOE_ERR_ARG otherwise). */
 int moe_debug_read(moe_handle *h, int field, void *host_dst, size_t bytes);
+
+/* Stage times of the last forward with MOE_OPT_PROFILE on (synchronises).
+ * Small-T path: router, dispatch, w13, w2+combine.  Tensor-core path: router,
+ * dispatch, gather, w13, w2, combine.  Writes up to `max` values in ms and the
+ * stage count to *n; names[i] (optional) receives static strings. */
+int moe_stage_times(moe_handle *h, float *ms, const char **names, int max, int *n);
 
 /* Synchronises the handle's last stream and returns its device status word
  * (0 when every kernel completed normally). */

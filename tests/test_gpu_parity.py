@@ -2,9 +2,11 @@
 same seeded inputs.
 
 Bars: routing ids, counts, offsets, perm and inv bit-exact (inputs keep the
-top-(k+1) keys >= 1e-4 apart); weights within 1e-6 relative; the small-T GEMV
-path's output within relative L2 1e-4 of the oracle; repeated calls bitwise
-identical."""
+top-(k+1) keys >= 1e-4 apart); weights within 5e-5 relative (the f32 logit of
+an H-long dot product carries about sqrt(H) * 2^-24 * |z| of rounding, up to
+~2e-5 at H = 6144, and a logit error d changes exp(l_j - l_0) by a relative d);
+the small-T GEMV path's output within relative L2 1e-4 of the oracle; repeated
+calls bitwise identical."""
 import os
 
 import numpy as np
@@ -19,7 +21,7 @@ from inputs import margin_x
 pytestmark = pytest.mark.gpu
 
 GEMV_TOL = 1e-4
-W_TOL = 1e-6
+W_TOL = 5e-5
 
 
 @pytest.fixture(scope="module")
