@@ -117,14 +117,24 @@ def layer_flops(wl, T):
     return 2 * T * (wl.k + wl.n_shared) * 3 * wl.H * wl.I + 2 * T * wl.H * wl.E
 
 
+def make_layer(wl, layer, max_tokens, dev):
+    """moe_init on device-generated synthetic weights; canonical copies freed after."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    from synth.device import device_weights
+    t, Wr, bias = device_weights(wl, layer, dev)
+    h = moe.MoELayer(moe.layout_for(wl, max_tokens), t)
+    del t
+    torch.cuda.empty_cache()
+    return h, Wr, bias
+
+
 # -------------------------------------------------------------- prefill --
 
 def bench_prefill(dev, steps, warmup, stream):
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_inputs import make_layer
     wl = synth.BY_NAME["glm_prefill"]
     T = 4096
     layer, Wr, bias = make_layer(wl, 0, T, dev)
@@ -182,8 +192,6 @@ def bench_decode(dev, steps, warmup, stream, T=1):
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_inputs import make_layer
     wl = synth.BY_NAME["glm_decode"]
     layers = [make_layer(wl, l, 4, dev)[0] for l in range(wl.layers)]
     x = synth.x_rows(wl, T)

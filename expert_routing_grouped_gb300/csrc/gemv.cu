@@ -30,22 +30,21 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return r;
 }
 
-// Exact int4 -> f32 for the 8 nibbles of one word (nibble i = bits 4i..4i+3,
-// K index 8*word + i).  Two's complement becomes offset binary by flipping
-// each nibble's top bit; nibble i (i <= 4) is OR-ed into the mantissa of
-// 2^(23-4i), whose unit in the last place is then exactly 1, and the float
-// minus (2^(23-4i) + 8) is the signed value.  Nibbles 5-7 are shifted down
-// first.
+// Exact int4 -> f32 for the 8 weights of one word of the library layout
+// (K indices 8w+0,2,4,6 at bits 0-15, 8w+1,3,5,7 at bits 16-31, offset binary).
+// A nibble at bits 4p..4p+3 (p <= 4) is OR-ed into the mantissa of 2^(23-4p),
+// whose unit in the last place is then exactly 1, and the float minus
+// (2^(23-4p) + 8) is the signed value.  Nibbles above bit 19 are shifted down
+// by 12 first.  q[j] is the weight of K index 8w+j.
 __device__ __forceinline__ void dequant8(uint32_t w, float q[8]) {
-  w ^= 0x88888888u;
   const uint32_t v = w >> 12;
   q[0] = __uint_as_float((w & 0x0000000Fu) | 0x4B000000u) - 8388616.0f;  // 2^23 + 8
-  q[1] = __uint_as_float((w & 0x000000F0u) | 0x49000000u) - 524296.0f;   // 2^19 + 8
-  q[2] = __uint_as_float((w & 0x00000F00u) | 0x47000000u) - 32776.0f;    // 2^15 + 8
-  q[3] = __uint_as_float((w & 0x0000F000u) | 0x45000000u) - 2056.0f;     // 2^11 + 8
-  q[4] = __uint_as_float((w & 0x000F0000u) | 0x43000000u) - 136.0f;      // 2^7 + 8
-  q[5] = __uint_as_float((v & 0x00000F00u) | 0x47000000u) - 32776.0f;
-  q[6] = __uint_as_float((v & 0x0000F000u) | 0x45000000u) - 2056.0f;
+  q[2] = __uint_as_float((w & 0x000000F0u) | 0x49000000u) - 524296.0f;   // 2^19 + 8
+  q[4] = __uint_as_float((w & 0x00000F00u) | 0x47000000u) - 32776.0f;    // 2^15 + 8
+  q[6] = __uint_as_float((w & 0x0000F000u) | 0x45000000u) - 2056.0f;     // 2^11 + 8
+  q[1] = __uint_as_float((w & 0x000F0000u) | 0x43000000u) - 136.0f;      // 2^7 + 8
+  q[3] = __uint_as_float((v & 0x00000F00u) | 0x47000000u) - 32776.0f;
+  q[5] = __uint_as_float((v & 0x0000F000u) | 0x45000000u) - 2056.0f;
   q[7] = __uint_as_float((v & 0x000F0000u) | 0x43000000u) - 136.0f;
 }
 
@@ -121,32 +120,29 @@ __global__ void __launch_bounds__(256) gemv_w13_kernel(
 
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     int e, n;
-    const uint8_t *q1, *q3;
-    const float *s1, *s3;
+    const uint8_t *q13;
+    const float *s13;
     int p0, cnt;
     if (item < n_routed * slabs_r) {
       e = active[item / slabs_r];
       n = (item % slabs_r) * W13_WARPS + warp;
-      q1 = ex.w1q + (size_t)e * I * (H / 2);
-      q3 = ex.w3q + (size_t)e * I * (H / 2);
-      s1 = ex.w1s + (size_t)e * I * (H / 64);
-      s3 = ex.w3s + (size_t)e * I * (H / 64);
+      q13 = ex.w13q + (size_t)e * 2 * I * (H / 2);
+      s13 = ex.w13s + (size_t)e * 2 * I * (H / 64);
       p0 = offsets[e];
       cnt = offsets[e + 1] - p0;
     } else {
       e = E;
       n = (item - n_routed * slabs_r) * W13_WARPS + warp;
-      q1 = sh.w1q;
-      q3 = sh.w3q;
-      s1 = sh.w1s;
-      s3 = sh.w3s;
+      q13 = sh.w13q;
+      s13 = sh.w13s;
       p0 = A;
       cnt = T;
     }
-    const uint8_t *r1 = q1 + (size_t)n * (H / 2);
-    const uint8_t *r3 = q3 + (size_t)n * (H / 2);
-    const float *rs1 = s1 + (size_t)n * (H / 64);
-    const float *rs3 = s3 + (size_t)n * (H / 64);
+    const size_t row1 = w13_row_of(n, 0), row3 = w13_row_of(n, 1);
+    const uint8_t *r1 = q13 + row1 * (H / 2);
+    const uint8_t *r3 = q13 + row3 * (H / 2);
+    const float *rs1 = s13 + row1 * (H / 64);
+    const float *rs3 = s13 + row3 * (H / 64);
     for (int b0 = 0; b0 < cnt; b0 += kGemvTokens) {
       const int nb = min(kGemvTokens, cnt - b0);
       size_t xoff[kGemvTokens];

@@ -1,12 +1,725 @@
-// ggemm_tc.cu -- steps 4-5 of the layer for large T on the tensor cores.
+// ggemm_tc.cu -- steps 4-5 of the layer for large T (prefill) on the 5th-gen
+// tensor cores: grouped GEMMs over the experts' token groups.
+//
+// Only this regime is a dense contraction: per expert, a group of tokens times
+// its int4 weights (the pages' per-expert mini-batch GEMM -- pure-C Colibri
+// tutorial, trdm.cn, §2.2 "third"; Colibri C + cuBLASLt tutorial, cf-1.com,
+// §3.3 Step 4, one GEMM per non-empty expert).  Here every expert, token
+// block and weight-row block is one tile of ONE persistent kernel per matrix:
+//
+//   ggemm_w13:  D[128 weight rows][N tokens] = W13_tile . x_grouped^T, the 128
+//               rows being 64 features' W1 and W3 rows interleaved by 16, so
+//               SwiGLU h = silu(g) * u pairs lanes l and l+16 of one warp;
+//               h is written as bf16 in grouped order.
+//   ggemm_w2:   D[128 output rows][N tokens] = W2_tile . h^T; the epilogue
+//               scales each token's column by its routing weight and writes
+//               y[grouped row][o] in f32.
+//
+// Per CTA (one per SM, 16 warps):
+//   warp 0      TMA producer: raw int4 weight tiles (128 rows x 256 K) and
+//               bf16 token tiles (256 rows x 64 K), both 128-byte swizzled.
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
+//               f32 accumulate) M=128, N=16..256, K=16 by one thread, commits
+//               to mbarriers; two 256-column accumulators in TMEM so the
+//               epilogue of one tile overlaps the main loop of the next.
+//   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
+//   warps 8-15  dequant: raw int4 -> bf16(q * s) into the UMMA operand layout
+//               (K-major, 128-byte swizzle), one row-half per thread.
+// Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
+// the device status word, flags the CTA to stop, and the kernel drains its
+// outstanding copies and MMAs (bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "moe_internal.cuh"
 
 namespace moe {
+namespace {
 
-bool tc_path_available() { return false; }
+constexpr int BM = 128;          // weight rows per tile (MMA M)
+constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
+constexpr int BK = 64;           // K per bf16 stage (128 bytes of a row)
+constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
+constexpr int NA = 3;            // bf16 A/B stages
+constexpr int NR = 2;            // raw stages
+constexpr int kThreads = 512;
+constexpr int kEpiWarp0 = 4;
+constexpr int kDeqWarp0 = 8;
+constexpr int kDeqThreads = 256;
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 
-cudaError_t launch_tc_path(const moe_handle *, const void *, int, float *, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
+struct __align__(1024) SmemTC {
+  uint8_t raw[NR][BM * 128];     // 2 x 16 KB
+  uint8_t a[NA][BM * 128];       // 3 x 16 KB
+  uint8_t b[NA][BN * 128];       // 3 x 32 KB
+  uint64_t raw_full[NR], raw_empty[NR];
+  uint64_t a_full[NA], b_full[NA], ab_empty[NA];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TcParams {
+  CUtensorMap map_w;       // raw weights of the routed experts [E * rows][K/2] u8
+  CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
+  CUtensorMap map_b;       // bf16 token operand [R][K]
+  const float *scale;      // routed scales [E * rows][K/64]
+  const float *scale_s;    // shared scales [rows_s][K/64]
+  int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
+  int K;                   // reduction length (H for W13, I for W2)
+  int K_s;                 // the shared expert's reduction length (H, or Is for W2)
+  int rows;                // weight rows per routed expert (2I or H)
+  int rows_s;              // weight rows of the shared expert (2Is or H)
+  int E, A, T;
+  const int32_t *blocks;   // token blocks (expert << 16 | block index)
+  const int32_t *n_blocks;
+  const int32_t *offsets;  // [E+1]
+  __nv_bfloat16 *hb;       // W13 output [R][h_stride]
+  int h_stride;
+  float *y;                // W2 output [R][H]
+  int H;
+  const float *wperm;      // [R]
+  int32_t *status;
+};
+
+// --------------------------------------------------------------- PTX glue --
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false if the CTA is stopping or the wait timed out (then the
+// status word and the CTA's abort flag are set).
+__device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
+                                      int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*reinterpret_cast<volatile int *>(&sm->abort)) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        atomicExch(reinterpret_cast<int *>(&sm->abort), 1);
+        atomicExch(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), start address in 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
+  d |= (uint64_t)1 << 16;                            // leading byte offset (unused: 16 B)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset
+  d |= (uint64_t)1 << 46;                            // descriptor version
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), f32 accumulator.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4)                          // D format f32
+         | (1u << 7)                        // A format bf16
+         | (1u << 10)                       // B format bf16
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive columns: thread i gets lane (quadrant base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------- dequant --
+
+// bf16x2 arithmetic on raw 32-bit registers.
+__device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t lop_nib(uint32_t w) {
+  uint32_t d;
+  // (w & 0x000F000F) | 0x43004300: two offset-binary nibbles into bf16 128 + n.
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(d) : "r"(w));
+  return d;
+}
+
+// 8 weights of one library-layout word -> 4 bf16x2 words of bf16(q * s), with
+// s = s_hi + s_lo split into two bf16 (q * s_hi is exact inside the fused
+// multiply-add, q * s_lo contributes below bf16 resolution).
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_hi2, uint32_t s_lo2,
+                                             uint32_t out[4]) {
+  const uint32_t c136 = 0x43084308u;   // bf16x2 (136, 136)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
+    out[i] = hfma2_bf16(q, s_hi2, hmul2_bf16(q, s_lo2));
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_splat(__nv_bfloat16 v) {
+  const uint16_t b = __bfloat16_as_ushort(v);
+  return (uint32_t)b | ((uint32_t)b << 16);
+}
+
+// --------------------------------------------------------------- tiles --
+
+struct Tile {
+  int e, p0, nvalid, wrow0, shared, K;
+};
+
+__device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int n_blocks, Tile &tl) {
+  const int blk = t / n_fb, fb = t - blk * n_fb;
+  if (blk >= n_blocks) return false;
+  const int packed = p.blocks[blk];
+  const int e = packed >> 16, tb = packed & 0xFFFF;
+  tl.e = e;
+  tl.shared = (e >= p.E);
+  int cnt;
+  if (!tl.shared) {
+    const int o0 = p.offsets[e];
+    cnt = p.offsets[e + 1] - o0;
+    tl.p0 = o0 + tb * BN;
+    tl.wrow0 = e * p.rows + fb * BM;
+    tl.K = p.K;
+  } else {
+    cnt = p.T;
+    tl.p0 = p.A + tb * BN;
+    tl.wrow0 = fb * BM;
+    tl.K = p.K_s;
+  }
+  tl.nvalid = min(BN, cnt - tb * BN);
+  // A block of the shared expert past its rows (when rows_s < rows) has no work.
+  if (tl.shared && fb * BM >= p.rows_s) tl.nvalid = 0;
+  return true;
+}
+
+// --------------------------------------------------------------- kernel --
+
+__global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemTC *sm = reinterpret_cast<SmemTC *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_blocks = *p.n_blocks;
+  const int n_fb = p.rows / BM;
+  const int n_tiles = n_blocks * n_fb;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(&sm->raw_full[i], 1);
+      mbar_init(&sm->raw_empty[i], kDeqThreads);
+    }
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&sm->a_full[i], kDeqThreads / 2);
+      mbar_init(&sm->b_full[i], 1);
+      mbar_init(&sm->ab_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm->acc_full[i], 1);
+      mbar_init(&sm->acc_empty[i], 128);
+    }
+    sm->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&sm->tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t rk = 0, kb = 0;
+      int last_raw_par[NR] = {-1, -1}, last_b_par[NA] = {-1, -1, -1};
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        Tile tl;
+        if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+        const CUtensorMap *mw = tl.shared ? &p.map_ws : &p.map_w;
+        for (int r = 0; ok && r < tl.K / RK; ++r) {
+          const int s = rk % NR;
+          const uint32_t ph = (rk / NR) & 1;
+          if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
+          mbar_expect_tx(&sm->raw_full[s], BM * 128);
+          tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
+          last_raw_par[s] = ph;
+          ++rk;
+          for (int j = 0; j < RK / BK; ++j) {
+            const int s2 = kb % NA;
+            const uint32_t ph2 = (kb / NA) & 1;
+            if (!(ok = wait_bar(&sm->ab_empty[s2], ph2 ^ 1, sm, p.status))) break;
+            mbar_expect_tx(&sm->b_full[s2], BN * 128);
+            tma_load_2d(sm->b[s2], &p.map_b, (r * (RK / BK) + j) * BK, tl.p0, &sm->b_full[s2]);
+            last_b_par[s2] = ph2;
+            ++kb;
+          }
+        }
+      }
+      // Drain: every copy this thread issued has landed before the CTA exits.
+      const unsigned long long t0 = globaltimer();
+      for (int s = 0; s < NR; ++s)
+        while (last_raw_par[s] >= 0 && !mbar_try_wait(&sm->raw_full[s], last_raw_par[s]) &&
+               globaltimer() - t0 < kWaitNs) {
+        }
+      for (int s = 0; s < NA; ++s)
+        while (last_b_par[s] >= 0 && !mbar_try_wait(&sm->b_full[s], last_b_par[s]) &&
+               globaltimer() - t0 < kWaitNs) {
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kb = 0, it = 0;
+      int last_acc = -1;
+      uint32_t last_acc_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        Tile tl;
+        if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+        const int buf = it & 1;
+        if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
+        tc_fence_after();
+        const int n_mma = (tl.nvalid + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(BM, n_mma);
+        const uint32_t d = tmem + buf * BN;
+        for (int k = 0; k < tl.K / BK; ++k) {
+          const int s = kb % NA;
+          const uint32_t ph = (kb / NA) & 1;
+          if (!(ok = wait_bar(&sm->a_full[s], ph, sm, p.status))) break;
+          if (!(ok = wait_bar(&sm->b_full[s], ph, sm, p.status))) break;
+          tc_fence_after();
+          const uint64_t da = sw128_desc(smem_u32(sm->a[s]));
+          const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                     (k | kk) ? 1u : 0u);
+          mma_commit(&sm->ab_empty[s]);
+          ++kb;
+        }
+        if (!ok) break;
+        mma_commit(&sm->acc_full[buf]);
+        last_acc = buf;
+        last_acc_par = (it >> 1) & 1;
+        ++it;
+      }
+      // Drain: the last commit covers every MMA issued before it.
+      if (last_acc >= 0) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&sm->acc_full[last_acc], last_acc_par) &&
+               globaltimer() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    // ------------------------------------------------------ epilogue
+    const int q = warp - kEpiWarp0;       // TMEM lane quadrant
+    const int row = q * 32 + lane;        // weight row of the tile
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      Tile tl;
+      if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+      const int buf = it & 1;
+      if (!wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status)) break;
+      tc_fence_after();
+      const int fb = (tl.wrow0 - (tl.shared ? 0 : tl.e * p.rows)) / BM;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
+      for (int c0 = 0; c0 < tl.nvalid; c0 += 32) {
+        float v[32];
+        tmem_ld32(tbase + c0, v);
+        if (p.mode == 0) {
+          // lanes 0-15: g of features fb*64 + 16q + lane; lanes 16-31: u of the same.
+          const int feat = fb * 64 + q * 16 + (lane & 15);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float u = __shfl_xor_sync(0xffffffffu, v[j], 16);
+            if (lane < 16 && c0 + j < tl.nvalid) {
+              const float g = v[j];
+              const float hval = g / (1.0f + expf(-g)) * u;
+              p.hb[(size_t)(tl.p0 + c0 + j) * p.h_stride + feat] = __float2bfloat16_rn(hval);
+            }
+          }
+        } else {
+          const int o = fb * BM + row;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < tl.nvalid) {
+              const int pr = tl.p0 + c0 + j;
+              p.y[(size_t)pr * p.H + o] = v[j] * p.wperm[pr];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm->acc_empty[buf]);
+      ++it;
+    }
+  } else if (warp >= kDeqWarp0) {
+    // ------------------------------------------------------ dequant
+    const int dt = threadIdx.x - kDeqWarp0 * 32;   // 0..255
+    const int half = dt >> 7;                       // K half of a raw stage
+    const int r = dt & 127;                         // tile row
+    uint32_t rk = 0, kb = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      Tile tl;
+      if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+      const float *srow = (tl.shared ? p.scale_s : p.scale) + (size_t)tl.wrow0 * (tl.K / 64) +
+                          (size_t)r * (tl.K / 64);
+      for (int rr = 0; rr < tl.K / RK; ++rr) {
+        const int s = rk % NR;
+        const float2 sc = *reinterpret_cast<const float2 *>(srow + rr * (RK / 64) + half * 2);
+        if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
+        const uint8_t *rrow = sm->raw[s] + r * 128;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = half * 2 + jj;                 // A block within the raw stage
+          const uint32_t kbj = kb + j;
+          const int s2 = kbj % NA;
+          // Raw 16-byte chunks 2j, 2j+1 of this row (128-byte swizzle: chunk c at c ^ (r & 7)).
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (r & 7)) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (r & 7)) << 4));
+          const float sv = jj ? sc.y : sc.x;
+          const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
+          const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
+          const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
+          if (!(ok = wait_bar(&sm->ab_empty[s2], ((kbj / NA) & 1) ^ 1, sm, p.status))) break;
+          uint8_t *arow = sm->a[s2] + r * 128;
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int wv = 0; wv < 8; ++wv) {   // word wv -> output chunk wv (8 bf16)
+            uint32_t o[4];
+            dequant_word(words[wv], shi2, slo2, o);
+            *reinterpret_cast<uint4 *>(arow + ((wv ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          fence_proxy_async();
+          mbar_arrive(&sm->a_full[s2]);
+        }
+        if (!ok) break;
+        mbar_arrive(&sm->raw_empty[s]);
+        ++rk;
+        kb += RK / BK;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+// ---------------------------------------------------- gather and combine --
+
+// xp[p] = bf16(x[token of grouped row p]); wperm[p] = routing weight (shared 1).
+__global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x, int x_is_bf16,
+                                                     int T, int H, int k, int n_shared,
+                                                     const int32_t *__restrict__ perm,
+                                                     const float *__restrict__ w,
+                                                     __nv_bfloat16 *__restrict__ xp,
+                                                     float *__restrict__ wperm) {
+  const int A = T * k, R = A + n_shared * T;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int pr = warp; pr < R; pr += nwarps) {
+    int t;
+    float wt;
+    if (pr < A) {
+      const int a = perm[pr];
+      t = a / k;
+      wt = w[a];
+    } else {
+      t = pr - A;
+      wt = 1.0f;
+    }
+    if (lane == 0) wperm[pr] = wt;
+    if (x_is_bf16) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H);
+      uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pr * H);
+      for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+    } else {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          reinterpret_cast<const float *>(x) + (size_t)t * H);
+      __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(xp + (size_t)pr * H);
+      for (int i = lane; i < H / 4; i += 32) {
+        const float4 f = __ldg(src + i);
+        dst[2 * i] = __floats2bfloat162_rn(f.x, f.y);
+        dst[2 * i + 1] = __floats2bfloat162_rn(f.z, f.w);
+      }
+    }
+  }
+}
+
+// out[t] (+)= sum_j y[inv[t*k+j]] + y_shared[t]: slot order, then the shared
+// expert; one owner per element, no atomics (tutorial cf-1.com §3.3 Step 5).
+__global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n_shared,
+                                                      const int32_t *__restrict__ inv,
+                                                      const float *__restrict__ y,
+                                                      float *__restrict__ out, int accumulate) {
+  const int A = T * k;
+  const int per_t = H / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * per_t;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per_t), c = (int)(i - (long long)t * per_t);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)inv[t * k + j] * H) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (n_shared) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)(A + t) * H) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    float4 *o = reinterpret_cast<float4 *>(out + (size_t)t * H) + c;
+    if (accumulate) {
+      const float4 prev = *o;
+      acc.x += prev.x;
+      acc.y += prev.y;
+      acc.z += prev.z;
+      acc.w += prev.w;
+    }
+    *o = acc;
+  }
+}
+
+// ---------------------------------------------------------- host side --
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D map over a row-major [rows][cols] array, box [box_rows][box_cols], 128B swizzle.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, uint64_t cols,
+              uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_elems * elem};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
+
+}  // namespace
+
+bool tc_path_available() { return get_encode() != nullptr; }
+
+cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
+                           cudaStream_t st) {
+  const moe::Workspace &w = h->ws;
+  const int E = h->E, H = h->H, I = h->I, k = h->k, S = h->S;
+  const int Is = S ? h->Is : I;
+  const int A = T * k, R = A + S * T;
+  const int maxR = h->L.max_tokens * k + S * h->L.max_tokens;
+  const int h_stride = I > Is ? I : Is;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  gather_kernel<<<h->num_sms * 4, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm, w.w,
+                                                w.xp, w.wperm);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  moe_handle *hm = const_cast<moe_handle *>(h);
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "gather";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  hm->launches += 1;
+
+  TcParams p{};
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // ---- W13
+  bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
+  ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
+                      (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
+  ok = ok && make_map(&p.map_b, w.xp, BF, 2, H, (uint64_t)maxR, H, BK, BN);
+  if (!ok) return cudaErrorInvalidValue;
+  p.scale = h->ex.w13s;
+  p.scale_s = S ? h->sh.w13s : h->ex.w13s;
+  p.mode = 0;
+  p.K = H;
+  p.K_s = H;
+  p.rows = 2 * I;
+  p.rows_s = 2 * Is;
+  p.E = E;
+  p.A = A;
+  p.T = T;
+  p.blocks = w.tiles;
+  p.n_blocks = w.n_tiles;
+  p.offsets = w.offsets;
+  p.hb = w.hb;
+  p.h_stride = h_stride;
+  p.y = w.y;
+  p.H = H;
+  p.wperm = w.wperm;
+  p.status = w.status;
+  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "w13";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  hm->launches += 1;
+  // ---- W2: A = W2 rows [H] over K = I, B = h [R][h_stride]
+  ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
+  ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
+                      BM);
+  ok = ok && make_map(&p.map_b, w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK, BN);
+  if (!ok) return cudaErrorInvalidValue;
+  p.scale = h->ex.w2s;
+  p.scale_s = S ? h->sh.w2s : h->ex.w2s;
+  p.mode = 1;
+  p.K = I;
+  p.K_s = Is;
+  p.rows = H;
+  p.rows_s = H;
+  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "w2";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  hm->launches += 1;
+  combine_kernel<<<h->num_sms * 8, 256, 0, st>>>(T, H, k, S, w.inv, w.y, out, accumulate ? 1 : 0);
+  hm->launches += 1;
+  err = cudaGetLastError();
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "combine";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  (void)R;
+  return err;
 }
 
 }  // namespace moe

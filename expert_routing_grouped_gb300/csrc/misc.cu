@@ -23,28 +23,139 @@ __global__ void transpose_kernel(const float *__restrict__ src, float *__restric
 
 // out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)); the norm is computed in f32
 // (the pages keep norms in f32: colibrì engine teardown, text-matrix.pages.dev,
-// "System map").  One block per token; fixed reduction order.
-__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float *__restrict__ x, int H,
-                                                           float eps,
-                                                           __nv_bfloat16 *__restrict__ out) {
-  __shared__ float part[8];
+// "System map").  One 1024-thread block per token, 16-byte loads, a fixed
+// reduction order.
+__global__ void __launch_bounds__(1024) rmsnorm_bf16_kernel(const float *__restrict__ x, int H,
+                                                            float eps,
+                                                            __nv_bfloat16 *__restrict__ out) {
+  __shared__ float part[32];
   const int t = blockIdx.x;
-  const float *row = x + (size_t)t * H;
+  const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+  const int n4 = H / 4;
+  float4 v[2];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(row[i], row[i], ss);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = threadIdx.x + r * 1024;
+    v[r] = (i < n4) ? row[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss = fmaf(v[r].x, v[r].x, ss);
+    ss = fmaf(v[r].y, v[r].y, ss);
+    ss = fmaf(v[r].z, v[r].z, ss);
+    ss = fmaf(v[r].w, v[r].w, ss);
+  }
+  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {   // H > 8192
+    const float4 f = row[i];
+    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tot += part[w];
+  for (int w = 0; w < 32; ++w) tot += part[w];
   const float r = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    out[(size_t)t * H + i] = __float2bfloat16_rn(row[i] * r);
+  __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(out + (size_t)t * H);
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int i = threadIdx.x + rr * 1024;
+    if (i < n4) {
+      o2[2 * i] = __floats2bfloat162_rn(v[rr].x * r, v[rr].y * r);
+      o2[2 * i + 1] = __floats2bfloat162_rn(v[rr].z * r, v[rr].w * r);
+    }
+  }
+  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {
+    const float4 f = row[i];
+    o2[2 * i] = __floats2bfloat162_rn(f.x * r, f.y * r);
+    o2[2 * i + 1] = __floats2bfloat162_rn(f.z * r, f.w * r);
+  }
+}
+
+// Library weight layout, written once at init from the canonical layout.
+//  * Nibbles: each 32-bit word holds K indices 8w..8w+7.  Canonical order puts
+//    index 8w+j at bits 4j..4j+3 as two's complement; the library stores the
+//    even indices 8w+0,2,4,6 at bits 0-3, 4-7, 8-11, 12-15 and the odd ones at
+//    bits 16-19, 20-23, 24-27, 28-31, each as offset binary (value + 8), so a
+//    single AND/OR with 0x000F000F / 0x43004300 on the word shifted by 4i gives
+//    the bf16 pair (128 + q + 8) for indices (8w+2i, 8w+2i+1).
+//  * W1/W3 rows are interleaved in 128-row blocks: block b holds features
+//    64b..64b+63; its 32-row quadrant Q holds W1 rows of features 64b+16Q+0..15
+//    then W3 rows of the same 16 features.  Scales follow the same row order.
+__device__ __forceinline__ uint32_t repack_word(uint32_t w) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t nib = ((w >> (4 * j)) & 0xFu) ^ 0x8u;
+    const int pos = (j & 1) ? 4 + (j >> 1) : (j >> 1);
+    out |= nib << (4 * pos);
+  }
+  return out;
+}
+
+// W1 and W3 of n_exp experts ([n_exp][I][kb] bytes each) into the interleaved
+// [n_exp][2I][kb] array, nibbles repacked; kb = bytes per row (multiple of 4).
+__global__ void repack_w13_kernel(const uint8_t *__restrict__ w1, const uint8_t *__restrict__ w3,
+                                  uint8_t *__restrict__ dst, long long n_exp, int I, int kb) {
+  const long long words_per_row = kb / 4;
+  const long long total = n_exp * 2LL * I * words_per_row;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long wi = i % words_per_row;
+    long long r = i / words_per_row;                 // source row over [n_exp][2][I]
+    const int f = (int)(r % I);
+    r /= I;
+    const int which = (int)(r % 2);
+    const long long e = r / 2;
+    const uint8_t *src = (which ? w3 : w1) + ((size_t)e * I + f) * kb;
+    const uint32_t w = reinterpret_cast<const uint32_t *>(src)[wi];
+    uint8_t *drow = dst + ((size_t)e * 2 * I + w13_row_of(f, which)) * kb;
+    reinterpret_cast<uint32_t *>(drow)[wi] = repack_word(w);
+  }
+}
+
+// Scales of W1/W3 into the interleaved row order ([n_exp][2I][groups]).
+__global__ void repack_w13_scales_kernel(const float *__restrict__ s1, const float *__restrict__ s3,
+                                         float *__restrict__ dst, long long n_exp, int I,
+                                         int groups) {
+  const long long total = n_exp * 2LL * I * groups;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int g = (int)(i % groups);
+    long long r = i / groups;
+    const int f = (int)(r % I);
+    r /= I;
+    const int which = (int)(r % 2);
+    const long long e = r / 2;
+    const float v = (which ? s3 : s1)[((size_t)e * I + f) * groups + g];
+    dst[((size_t)e * 2 * I + w13_row_of(f, which)) * groups + g] = v;
+  }
+}
+
+// In-place nibble repack of a plain [rows][kb] array (W2).
+__global__ void repack_words_kernel(uint32_t *__restrict__ w, long long n_words) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_words;
+       i += (long long)gridDim.x * blockDim.x)
+    w[i] = repack_word(w[i]);
 }
 
 }  // namespace
+
+cudaError_t launch_repack_w13(const uint8_t *w1, const uint8_t *w3, uint8_t *dst, long long n_exp,
+                              int I, int kb, cudaStream_t s) {
+  repack_w13_kernel<<<152 * 8, 256, 0, s>>>(w1, w3, dst, n_exp, I, kb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_w13_scales(const float *s1, const float *s3, float *dst, long long n_exp,
+                                     int I, int groups, cudaStream_t s) {
+  repack_w13_scales_kernel<<<152 * 8, 256, 0, s>>>(s1, s3, dst, n_exp, I, groups);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_words(uint8_t *w, long long n_bytes, cudaStream_t s) {
+  repack_words_kernel<<<152 * 8, 256, 0, s>>>(reinterpret_cast<uint32_t *>(w), n_bytes / 4);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, cudaStream_t s) {
   const dim3 grid((E + 31) / 32, (H + 31) / 32), block(32, 8);
@@ -55,7 +166,7 @@ cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, 
 cudaError_t launch_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                                 cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(x, H, eps, reinterpret_cast<__nv_bfloat16 *>(out));
+  rmsnorm_bf16_kernel<<<T, 1024, 0, s>>>(x, H, eps, reinterpret_cast<__nv_bfloat16 *>(out));
   return cudaGetLastError();
 }
 

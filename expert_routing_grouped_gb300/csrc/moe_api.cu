@@ -16,7 +16,6 @@
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kTileM = 128;   // rows per tensor-core tile; the dispatch tile list uses it
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -71,18 +70,14 @@ void carve(moe_handle *h, Carver &c) {
   const size_t Imax = I > Is ? I : Is;
   h->wr_t = c.take<float>(E * H);
   h->bias = c.take<float>(E);
-  h->ex.w1q = c.take<uint8_t>(E * I * H / 2);
-  h->ex.w3q = c.take<uint8_t>(E * I * H / 2);
+  h->ex.w13q = c.take<uint8_t>(E * 2 * I * H / 2);
   h->ex.w2q = c.take<uint8_t>(E * H * I / 2);
-  h->ex.w1s = c.take<float>(E * I * H / 64);
-  h->ex.w3s = c.take<float>(E * I * H / 64);
+  h->ex.w13s = c.take<float>(E * 2 * I * H / 64);
   h->ex.w2s = c.take<float>(E * H * I / 64);
   if (S) {
-    h->sh.w1q = c.take<uint8_t>(Is * H / 2);
-    h->sh.w3q = c.take<uint8_t>(Is * H / 2);
+    h->sh.w13q = c.take<uint8_t>(2 * Is * H / 2);
     h->sh.w2q = c.take<uint8_t>(H * Is / 2);
-    h->sh.w1s = c.take<float>(Is * H / 64);
-    h->sh.w3s = c.take<float>(Is * H / 64);
+    h->sh.w13s = c.take<float>(2 * Is * H / 64);
     h->sh.w2s = c.take<float>(H * Is / 64);
   }
   moe::Workspace &w = h->ws;
@@ -98,57 +93,97 @@ void carve(moe_handle *h, Carver &c) {
   w.inv = c.take<int32_t>(A);
   w.active = c.take<int32_t>(E + 1);
   w.n_active = c.take<int32_t>(1);
-  w.tiles = c.take<int32_t>(A / kTileM + E + maxT / kTileM + 2);
+  w.tiles = c.take<int32_t>(A / moe::kTileTokens + E + maxT / moe::kTileTokens + 2);
   w.n_tiles = c.take<int32_t>(2);
   w.status = c.take<int32_t>(1);
   w.h = c.take<float>(rows * Imax);
   w.hb = c.take<__nv_bfloat16>(rows * Imax);
   w.y = c.take<float>(rows * H);
+  w.xp = c.take<__nv_bfloat16>(rows * H);
+  w.wperm = c.take<float>(rows);
   w.x_stage = c.take<char>(maxT * H * h->x_elem);
   w.out_stage = c.take<float>(maxT * H);
 }
 
+// Copies one expert set (E routed experts, or the shared one) from the
+// canonical layout into the library layout, staging through a bounded device
+// buffer so host and device sources are handled alike.
+int copy_expert_set(const moe::ExpertWeights &dst, const uint8_t *w1q, const float *w1s,
+                    const uint8_t *w3q, const float *w3s, const uint8_t *w2q, const float *w2s,
+                    size_t n_exp, size_t H, size_t I, char *stage, size_t stage_bytes) {
+  const size_t qrow = H / 2, srow = H / 64;                 // W1/W3 row bytes / groups
+  const size_t per_exp = 2 * I * qrow + 2 * I * srow * 4;   // staged bytes per expert (W1+W3)
+  size_t chunk = stage_bytes / per_exp;
+  if (chunk < 1) return MOE_ERR_NOMEM;
+  if (chunk > n_exp) chunk = n_exp;
+  for (size_t e0 = 0; e0 < n_exp; e0 += chunk) {
+    const size_t ne = (e0 + chunk <= n_exp) ? chunk : n_exp - e0;
+    uint8_t *t1 = reinterpret_cast<uint8_t *>(stage);
+    uint8_t *t3 = t1 + ne * I * qrow;
+    float *ts1 = reinterpret_cast<float *>(t3 + ne * I * qrow);
+    float *ts3 = ts1 + ne * I * srow;
+    if (cudaMemcpy(t1, w1q + e0 * I * qrow, ne * I * qrow, cudaMemcpyDefault) != cudaSuccess ||
+        cudaMemcpy(t3, w3q + e0 * I * qrow, ne * I * qrow, cudaMemcpyDefault) != cudaSuccess ||
+        cudaMemcpy(ts1, w1s + e0 * I * srow, ne * I * srow * 4, cudaMemcpyDefault) != cudaSuccess ||
+        cudaMemcpy(ts3, w3s + e0 * I * srow, ne * I * srow * 4, cudaMemcpyDefault) != cudaSuccess)
+      return MOE_ERR_DEVICE;
+    if (moe::launch_repack_w13(t1, t3, const_cast<uint8_t *>(dst.w13q) + e0 * 2 * I * qrow,
+                               (long long)ne, (int)I, (int)qrow, 0) != cudaSuccess ||
+        moe::launch_repack_w13_scales(ts1, ts3, const_cast<float *>(dst.w13s) + e0 * 2 * I * srow,
+                                      (long long)ne, (int)I, (int)srow, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return MOE_ERR_DEVICE;
+  }
+  // W2 [n_exp][H][I/2]: plain copy, then repack the nibbles in place.
+  if (cudaMemcpy(const_cast<uint8_t *>(dst.w2q), w2q, n_exp * H * I / 2, cudaMemcpyDefault) !=
+          cudaSuccess ||
+      cudaMemcpy(const_cast<float *>(dst.w2s), w2s, n_exp * H * (I / 64) * 4, cudaMemcpyDefault) !=
+          cudaSuccess ||
+      moe::launch_repack_words(const_cast<uint8_t *>(dst.w2q), (long long)(n_exp * H * I / 2), 0) !=
+          cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
 int copy_weights(moe_handle *h, const moe_weights *W) {
   const size_t E = h->E, H = h->H, I = h->I, Is = h->Is;
-  struct Job {
-    void *dst;
-    const void *src;
-    size_t bytes;
-  } jobs[] = {
-      {(void *)h->ex.w1q, W->w1_q, E * I * H / 2},  {(void *)h->ex.w3q, W->w3_q, E * I * H / 2},
-      {(void *)h->ex.w2q, W->w2_q, E * H * I / 2},  {(void *)h->ex.w1s, W->w1_s, E * I * H / 16},
-      {(void *)h->ex.w3s, W->w3_s, E * I * H / 16}, {(void *)h->ex.w2s, W->w2_s, E * H * I / 16},
-  };
-  for (const Job &j : jobs)
-    if (cudaMemcpy(j.dst, j.src, j.bytes, cudaMemcpyDefault) != cudaSuccess) return MOE_ERR_DEVICE;
-  if (h->S) {
-    Job sj[] = {
-        {(void *)h->sh.w1q, W->sw1_q, Is * H / 2}, {(void *)h->sh.w3q, W->sw3_q, Is * H / 2},
-        {(void *)h->sh.w2q, W->sw2_q, H * Is / 2}, {(void *)h->sh.w1s, W->sw1_s, Is * H / 16},
-        {(void *)h->sh.w3s, W->sw3_s, Is * H / 16}, {(void *)h->sh.w2s, W->sw2_s, H * Is / 16},
-    };
-    for (const Job &j : sj)
-      if (cudaMemcpy(j.dst, j.src, j.bytes, cudaMemcpyDefault) != cudaSuccess)
-        return MOE_ERR_DEVICE;
-  }
-  if (W->router_bias) {
-    if (cudaMemcpy(h->bias, W->router_bias, E * 4, cudaMemcpyDefault) != cudaSuccess)
-      return MOE_ERR_DEVICE;
-  } else if (cudaMemset(h->bias, 0, E * 4) != cudaSuccess) {
-    return MOE_ERR_DEVICE;
-  }
-  // Router: canonical [H][E] -> [E][H] through a temporary buffer.
-  float *tmp = nullptr;
-  if (fault_alloc(2) || cudaMalloc(&tmp, E * H * 4) != cudaSuccess) {
+  // One staging buffer: at least one expert's W1+W3, at most 512 MB.
+  const size_t Imax = I > Is ? I : Is;
+  const size_t per_exp = 2 * Imax * (H / 2) + 2 * Imax * (H / 64) * 4;
+  size_t stage_bytes = (size_t)512 << 20;
+  if (stage_bytes < per_exp) stage_bytes = per_exp;
+  if (stage_bytes > per_exp * E) stage_bytes = per_exp * (E > 1 ? E : 1);
+  char *stage = nullptr;
+  if (fault_alloc(2) || cudaMalloc(&stage, stage_bytes) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_NOMEM;
   }
-  int rc = MOE_OK;
-  if (cudaMemcpy(tmp, W->router_w, E * H * 4, cudaMemcpyDefault) != cudaSuccess ||
-      moe::launch_transpose_router(tmp, h->wr_t, (int)H, (int)E, 0) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess)
-    rc = MOE_ERR_DEVICE;
-  cudaFree(tmp);
+  int rc = copy_expert_set(h->ex, W->w1_q, W->w1_s, W->w3_q, W->w3_s, W->w2_q, W->w2_s, E, H, I,
+                           stage, stage_bytes);
+  if (rc == MOE_OK && h->S)
+    rc = copy_expert_set(h->sh, W->sw1_q, W->sw1_s, W->sw3_q, W->sw3_s, W->sw2_q, W->sw2_s, 1, H,
+                         Is, stage, stage_bytes);
+  if (rc == MOE_OK) {
+    if (W->router_bias) {
+      if (cudaMemcpy(h->bias, W->router_bias, E * 4, cudaMemcpyDefault) != cudaSuccess)
+        rc = MOE_ERR_DEVICE;
+    } else if (cudaMemset(h->bias, 0, E * 4) != cudaSuccess) {
+      rc = MOE_ERR_DEVICE;
+    }
+  }
+  // Router: canonical [H][E] -> [E][H] through the staging buffer.
+  if (rc == MOE_OK) {
+    float *tmp = reinterpret_cast<float *>(stage);
+    if (E * H * 4 > stage_bytes) {
+      rc = MOE_ERR_NOMEM;
+    } else if (cudaMemcpy(tmp, W->router_w, E * H * 4, cudaMemcpyDefault) != cudaSuccess ||
+               moe::launch_transpose_router(tmp, h->wr_t, (int)H, (int)E, 0) != cudaSuccess ||
+               cudaDeviceSynchronize() != cudaSuccess) {
+      rc = MOE_ERR_DEVICE;
+    }
+  }
+  cudaFree(stage);
   return rc;
 }
 
@@ -175,7 +210,7 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
   if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
   h->launches += 2;
   mark(h, "router", st);
-  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, kTileM, st);
+  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
   h->launches += 1;
   mark(h, "dispatch", st);
   if (err == cudaSuccess) {
@@ -271,7 +306,7 @@ __attribute__((visibility("default"))) int moe_route(moe_handle *h, const void *
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
   if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
-  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, kTileM, st);
+  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
   h->last_T = T;
   h->last_regime = 0;
   h->last_stream = st;
@@ -306,7 +341,7 @@ __attribute__((visibility("default"))) int moe_forward_host(moe_handle *h, const
 __attribute__((visibility("default"))) int moe_rmsnorm_bf16(const float *x, int T, int H,
                                                             float eps, uint16_t *out,
                                                             moe_stream_t stream) {
-  if (T < 0 || H <= 0 || !(eps >= 0.f)) return MOE_ERR_ARG;
+  if (T < 0 || H <= 0 || H % 8 || !(eps >= 0.f)) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !out) return MOE_ERR_ARG;
   return moe::launch_rmsnorm_bf16(x, T, H, eps, out, reinterpret_cast<cudaStream_t>(stream)) ==

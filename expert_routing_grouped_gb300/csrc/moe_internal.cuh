@@ -14,6 +14,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
+constexpr int kTileTokens = 256;      // tokens per tensor-core tile (the MMA's N)
 
 // Device status word codes (sticky until the next forward overwrites them).
 enum Status : int32_t {
@@ -23,10 +24,13 @@ enum Status : int32_t {
   kStatusBadTile = 3,         // a tile outside its expert's range
 };
 
-// Per-expert weight views into the library's device copy (canonical layout).
+// Per-expert weight views into the library's device copy.  W13 is the
+// interleaved [n_experts][2I][H/2] array (see misc.cu), W2 is [n_experts][H][I/2];
+// both with repacked offset-binary nibbles.  Scales are f32, gs64, in the same
+// row order: w13s [n_experts][2I][H/64], w2s [n_experts][H][I/64].
 struct ExpertWeights {
-  const uint8_t *w1q, *w3q, *w2q;   // [n_experts][rows][K/2]
-  const float *w1s, *w3s, *w2s;     // [n_experts][rows][K/64]
+  const uint8_t *w13q, *w2q;
+  const float *w13s, *w2s;
 };
 
 struct Workspace {
@@ -48,6 +52,8 @@ struct Workspace {
   float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
   __nv_bfloat16 *hb;  // [max_tokens*k + S*max_tokens][I_max] bf16 (tensor-core path)
   float *y;           // [max_tokens*k + S*max_tokens][H] f32 (tensor-core path)
+  __nv_bfloat16 *xp;  // [max_tokens*k + S*max_tokens][H] bf16 activations in grouped order
+  float *wperm;       // [max_tokens*k + S*max_tokens] routing weight per grouped row (shared 1)
   // host-call staging
   void *x_stage;      // [max_tokens][H] (x dtype)
   float *out_stage;   // [max_tokens][H]
@@ -100,5 +106,15 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
 cudaError_t launch_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                                 cudaStream_t s);
 cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, cudaStream_t s);
+cudaError_t launch_repack_w13(const uint8_t *w1, const uint8_t *w3, uint8_t *dst, long long n_exp,
+                              int I, int kb, cudaStream_t s);
+cudaError_t launch_repack_w13_scales(const float *s1, const float *s3, float *dst, long long n_exp,
+                                     int I, int groups, cudaStream_t s);
+cudaError_t launch_repack_words(uint8_t *w, long long n_bytes, cudaStream_t s);
+
+// Row of W1 (is_w3 = 0) or W3 (1) feature f in the interleaved W13 layout.
+__host__ __device__ __forceinline__ size_t w13_row_of(int f, int is_w3) {
+  return (size_t)(f >> 6) * 128 + (size_t)((f & 63) >> 4) * 32 + (f & 15) + (is_w3 ? 16 : 0);
+}
 
 }  // namespace moe

@@ -139,8 +139,15 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     key[i] = -INFINITY;
     val[i] = 0.f;
     if (e < E) {
+      // Issue all split loads before summing (in split order).
+      float part[kRouterSplitMax];
+#pragma unroll
+      for (int s = 0; s < kRouterSplitMax; ++s)
+        part[s] = (s < splits) ? z_part[((size_t)s * zstride + t) * E + e] : 0.f;
       float zz = 0.f;
-      for (int s = 0; s < splits; ++s) zz += z_part[((size_t)s * zstride + t) * E + e];
+#pragma unroll
+      for (int s = 0; s < kRouterSplitMax; ++s)
+        if (s < splits) zz += part[s];
       const float b = bias ? bias[e] : 0.f;
       if (mode == 0) {
         key[i] = zz + b;

@@ -159,7 +159,8 @@ int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
  * Pre-norm between stacked layers: out_bf16[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)),
  * computed in f32 with no learned gain (the pages normalise with RMSNorm before
  * the MoE layer: tutorial cf-1.com §2.1 step 1; the norm stays f32: teardown
- * "System map").  x [T][H] f32 device, out [T][H] bf16 bits device.
+ * "System map").  x [T][H] f32 device, out [T][H] bf16 bits device, both
+ * 16-byte aligned; H a multiple of 8.
  */
 int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                      moe_stream_t stream);

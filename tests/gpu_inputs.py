@@ -7,40 +7,7 @@ import oracle
 import synth
 from inputs import margin_x, oracle_weights_for
 
-_Q = (("w1_q", synth.T_W1Q), ("w3_q", synth.T_W3Q), ("w2_q", synth.T_W2Q))
-_S = (("w1_s", synth.T_W1S), ("w3_s", synth.T_W3S), ("w2_s", synth.T_W2S))
-
-
-def device_weights(wl, layer, dev):
-    """Canonical weights of one layer as device tensors (generated in HBM)."""
-    import torch
-    H, I, E = wl.H, wl.I, wl.E
-    t = {}
-    for name, tid in _Q:
-        per = I * H // 2
-        t[name] = torch.empty(E * per, dtype=torch.uint8, device=dev)
-        synth.dev_fill_int4(wl.seed, layer, tid, 0, per, E, t[name].data_ptr())
-    for name, tid in _S:
-        per = I * H // 64
-        t[name] = torch.empty(E * per, dtype=torch.float32, device=dev)
-        synth.dev_fill_scales(wl.seed, layer, tid, 0, per, E, t[name].data_ptr())
-    if wl.n_shared:
-        Is = wl.I_shared
-        for name, tid in _Q:
-            t["s" + name] = torch.empty(Is * H // 2, dtype=torch.uint8, device=dev)
-            synth.dev_fill_int4(wl.seed, layer, tid, synth.SHARED_EXPERT, Is * H // 2, 1,
-                                t["s" + name].data_ptr())
-        for name, tid in _S:
-            t["s" + name] = torch.empty(Is * H // 64, dtype=torch.float32, device=dev)
-            synth.dev_fill_scales(wl.seed, layer, tid, synth.SHARED_EXPERT, Is * H // 64, 1,
-                                  t["s" + name].data_ptr())
-    Wr = synth.router_w(wl, layer)
-    bias = synth.router_bias(wl, layer)
-    t["router_w"] = torch.from_numpy(Wr).to(dev)
-    if bias is not None:
-        t["router_bias"] = torch.from_numpy(bias).to(dev)
-    torch.cuda.synchronize()
-    return t, Wr, bias
+from synth.device import device_weights
 
 
 def make_layer(wl, layer, max_tokens, dev):

@@ -216,3 +216,82 @@ def test_init_fault_injection_leaks_nothing(dev):
     h = moe.MoELayer(moe.layout_for(wl, 64), t)
     assert h.device_bytes() > 0
     h.close()
+
+
+# ------------------------------------------------------------ tensor cores --
+
+TC_TOL = 5e-3          # relative L2 on the bf16 tensor-core path
+TC_MAXABS = 2e-2       # times rms(ref)
+
+
+def check_tc(got, ref_out):
+    rms = float(np.sqrt(np.mean(ref_out ** 2)))
+    assert rel_l2(got, ref_out) <= TC_TOL
+    assert np.max(np.abs(got - ref_out)) <= TC_MAXABS * rms
+
+
+def run_tc(wl, T, dev, rows=None):
+    """Full T on the GPU through the tensor-core path; oracle on `rows`."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    h, Wr, bias = get_layer(wl, T, dev)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_TC)
+    x, _ = margin_x(wl, T, Wr, bias)
+    ref = oracle_layer(wl, 0, x, Wr, bias, rows=rows)
+    xd = to_device_x(wl, x, dev)
+    out = torch.full((T, wl.H), float("nan"), device=dev)
+    h.forward(xd, T, out)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    assert h.debug_view().regime == moe.REGIME_TC
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k), ref["idx"])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM), ref["perm"])
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    return got, ref, h, xd
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("olmoe", 64), ("glm_decode", 4)])
+def test_tc_path_parity_small(dev, name, T):
+    """The tensor-core path on small batches (ragged tiles: N = 16..64)."""
+    wl = synth.BY_NAME[name]
+    got, ref, h, _ = run_tc(wl, T, dev)
+    check_tc(got, ref["out"])
+
+
+def _sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(np.concatenate([[0, T - 1], rng.choice(np.arange(1, T - 1), n - 2, replace=False)]))
+
+
+@pytest.mark.parametrize("name,T,n", [("mixtral", 512, 12), ("glm_prefill", 4096, 16)])
+def test_tc_path_parity_full_size(dev, name, T, n):
+    """Full-size prefill batches; the oracle checks a seeded sample of tokens
+    (per-token outputs are independent once the routing is fixed, and the
+    routing of all T tokens is checked bit-exact)."""
+    wl = synth.BY_NAME[name]
+    rows = _sample_rows(T, n, T)
+    got, ref, h, xd = run_tc(wl, T, dev, rows=rows)
+    check_tc(got[rows], ref["out"])
+    # bitwise repeatable
+    import torch
+    out2 = torch.empty(T, wl.H, device=dev)
+    h.forward(xd, T, out2)
+    torch.cuda.synchronize()
+    assert np.array_equal(out2.cpu().numpy(), got)
+
+
+def test_tc_and_gemv_agree(dev):
+    """Both expert paths on the same batch agree to the TC tolerance."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["olmoe"]
+    got_tc, ref, h, xd = run_tc(wl, 64, dev)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_GEMV)
+    out = torch.empty(64, wl.H, device=dev)
+    h.forward(xd, 64, out)
+    torch.cuda.synchronize()
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+    g = out.cpu().numpy()
+    assert rel_l2(g, ref["out"]) <= GEMV_TOL
+    assert rel_l2(got_tc, g) <= TC_TOL
