@@ -7,20 +7,30 @@
 // received tokens are read (Colibri C + cuBLASLt tutorial, cf-1.com, §3.3
 // Step 4: skip empty experts).
 //
-//   gemv_w13:  h[p][n] = silu(W1[n] . x_t) * (W3[n] . x_t) for every grouped
-//              position p of every active expert (and the shared expert),
-//              silu(g) = g / (1 + e^-g).
-//   gemv_w2:   out[t][o] = sum_j w[t][j] * (W2_{idx[t][j]}[o] . h[inv(t,j)])
-//              + W2_shared[o] . h_shared[t], summed in slot order then the
-//              shared expert -- the combine of tutorial §3.3 Step 5, fused,
-//              one owner per output element, no atomics.
+//   W13:  h[p][n] = silu(W1[n] . x_t) * (W3[n] . x_t) for every grouped
+//         position p of every active expert (and of the shared expert),
+//         silu(g) = g / (1 + e^-g).
+//   W2:   y[p][o] = w_p * (W2[o] . h[p]); the combine kernel then sums each
+//         token's rows in slot order, then the shared expert (tutorial §3.3
+//         Step 5), one owner per output element, no atomics.
 //
-// Weights are read with 128-bit non-allocating loads; a lane's 16 bytes are 32
-// consecutive weights, all inside one 64-wide scale group.
+// One kernel serves both matrices.  An item is 32 consecutive weight rows of
+// one active expert (W13: 16 features' W1 and W3 rows, interleaved; W2: 32
+// output rows); each of the 8 warps streams 4 of those rows over the full K
+// with 128-bit non-allocating loads (a lane's 16 bytes = 32 weights inside one
+// 64-wide scale group).  The expert's activation rows sit in shared memory as
+// f32 (staged when the expert changes) and are reused across the 4 rows.
+// Dequant and FMAs use packed f32x2 arithmetic.  CTAs take contiguous item
+// ranges, so one activation stage serves many items.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
+
+constexpr int kRowsPerItem = 32;
+constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = kRowsPerItem / kWarps;   // 4
+constexpr int kActSmemBytes = 96 * 1024;
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
@@ -30,151 +40,193 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return r;
 }
 
-// Exact int4 -> f32 for the 8 weights of one word of the library layout
-// (K indices 8w+0,2,4,6 at bits 0-15, 8w+1,3,5,7 at bits 16-31, offset binary).
-// A nibble at bits 4p..4p+3 (p <= 4) is OR-ed into the mantissa of 2^(23-4p),
-// whose unit in the last place is then exactly 1, and the float minus
-// (2^(23-4p) + 8) is the signed value.  Nibbles above bit 19 are shifted down
-// by 12 first.  q[j] is the weight of K index 8w+j.
-__device__ __forceinline__ void dequant8(uint32_t w, float q[8]) {
+// Exact int4 -> f32 pairs for the 8 weights of one word of the library layout
+// (K indices 8w+0,2,4,6 at bits 0-15, 8w+1,3,5,7 at bits 16-31, offset
+// binary).  A nibble at bits 4p..4p+3 (p <= 4) is OR-ed into the mantissa of
+// 2^(23-4p), whose unit in the last place is then exactly 1; subtracting
+// 2^(23-4p) + 8 leaves the signed value.  Nibbles above bit 19 are shifted
+// down by 12 first.  q[i] = (weight 8w+2i, weight 8w+2i+1).
+__device__ __forceinline__ void dequant8(uint32_t w, float2 q[4]) {
   const uint32_t v = w >> 12;
-  q[0] = __uint_as_float((w & 0x0000000Fu) | 0x4B000000u) - 8388616.0f;  // 2^23 + 8
-  q[2] = __uint_as_float((w & 0x000000F0u) | 0x49000000u) - 524296.0f;   // 2^19 + 8
-  q[4] = __uint_as_float((w & 0x00000F00u) | 0x47000000u) - 32776.0f;    // 2^15 + 8
-  q[6] = __uint_as_float((w & 0x0000F000u) | 0x45000000u) - 2056.0f;     // 2^11 + 8
-  q[1] = __uint_as_float((w & 0x000F0000u) | 0x43000000u) - 136.0f;      // 2^7 + 8
-  q[3] = __uint_as_float((v & 0x00000F00u) | 0x47000000u) - 32776.0f;
-  q[5] = __uint_as_float((v & 0x0000F000u) | 0x45000000u) - 2056.0f;
-  q[7] = __uint_as_float((v & 0x000F0000u) | 0x43000000u) - 136.0f;
+  q[0] = __fadd2_rn(make_float2(__uint_as_float((w & 0x0000000Fu) | 0x4B000000u),
+                                __uint_as_float((w & 0x000F0000u) | 0x43000000u)),
+                    make_float2(-8388616.0f, -136.0f));
+  q[1] = __fadd2_rn(make_float2(__uint_as_float((w & 0x000000F0u) | 0x49000000u),
+                                __uint_as_float((v & 0x00000F00u) | 0x47000000u)),
+                    make_float2(-524296.0f, -32776.0f));
+  q[2] = __fadd2_rn(make_float2(__uint_as_float((w & 0x00000F00u) | 0x47000000u),
+                                __uint_as_float((v & 0x0000F000u) | 0x45000000u)),
+                    make_float2(-32776.0f, -2056.0f));
+  q[3] = __fadd2_rn(make_float2(__uint_as_float((w & 0x0000F000u) | 0x45000000u),
+                                __uint_as_float((v & 0x000F0000u) | 0x43000000u)),
+                    make_float2(-2056.0f, -136.0f));
 }
 
-// 32 activations starting at element k0 of row `row`, as f32.
-__device__ __forceinline__ void load_x32(const void *x, int x_is_bf16, size_t row_off, int k0,
-                                         float xv[32]) {
-  if (x_is_bf16) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(
-        reinterpret_cast<const __nv_bfloat16 *>(x) + row_off + k0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 u = __ldg(p + i);
-      const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xv[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
-        xv[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
-      }
-    }
-  } else {
-    const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) +
-                                                       row_off + k0);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 f = __ldg(p + i);
-      xv[4 * i] = f.x;
-      xv[4 * i + 1] = f.y;
-      xv[4 * i + 2] = f.z;
-      xv[4 * i + 3] = f.w;
-    }
-  }
-}
-
-__device__ __forceinline__ float dot32(const uint4 wq, const float xv[32]) {
-  const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float q[8];
-    dequant8(ws[i], q);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc = fmaf(q[j], xv[8 * i + j], acc);
-  }
-  return acc;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// ---------------------------------------------------------------------------
-// W1/W3 + SwiGLU.  Block = 8 warps; an item is (active expert, 8 row pairs),
-// one row pair (W1 row n, W3 row n) per warp, full K per warp.  Tokens of the
-// expert are taken kGemvTokens at a time.
-constexpr int W13_WARPS = 8;
-
-__global__ void __launch_bounds__(256) gemv_w13_kernel(
-    const void *__restrict__ x, int x_is_bf16, int T, int H, int k, int E, int I, int Is,
-    int h_stride, ExpertWeights ex, ExpertWeights sh, const int32_t *__restrict__ active,
-    const int32_t *__restrict__ n_active_p, const int32_t *__restrict__ offsets,
-    const int32_t *__restrict__ perm, float *__restrict__ hbuf) {
+// mode 0: W13 + SwiGLU -> out = h;  mode 1: W2 times routing weight -> out = y.
+template <int NT>
+__global__ void __launch_bounds__(256) gemv_kernel(
+    int mode, const void *__restrict__ act, int act_is_bf16, int act_stride, int T, int k, int E,
+    int K_r, int K_s, int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
+    const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
+    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    const float *__restrict__ wts, float *__restrict__ out, int out_stride) {
+  extern __shared__ float act_s[];   // [NT][K] activations of the current expert pass
   const int n_active = *n_active_p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slabs_r = I / W13_WARPS, slabs_s = Is / W13_WARPS;
-  // Routed experts first, then (if present, as the last active entry) the shared one.
   const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
   const int n_routed = n_active - has_shared;
-  const int items = n_routed * slabs_r + has_shared * slabs_s;
+  const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
+  const int items = n_routed * items_r + has_shared * items_s;
   const int A = T * k;
-  const int chunks = H / 32;      // 16-byte chunks per row
+  const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+  const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+  int staged_e = -1, staged_b = -1;
 
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    int e, n;
-    const uint8_t *q13;
-    const float *s13;
-    int p0, cnt;
-    if (item < n_routed * slabs_r) {
-      e = active[item / slabs_r];
-      n = (item % slabs_r) * W13_WARPS + warp;
-      q13 = ex.w13q + (size_t)e * 2 * I * (H / 2);
-      s13 = ex.w13s + (size_t)e * 2 * I * (H / 64);
+  // Rows of this warp inside an item: W13 -> W1 of features 2w, 2w+1 and W3 of
+  // the same (rows 2w, 2w+1, 16+2w, 17+2w of the 32-row group); W2 -> 4w..4w+3.
+  int rr[kRowsPerWarp];
+  if (mode == 0) {
+    rr[0] = 2 * warp;
+    rr[1] = 2 * warp + 1;
+    rr[2] = 16 + 2 * warp;
+    rr[3] = 17 + 2 * warp;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) rr[i] = kRowsPerWarp * warp + i;
+  }
+
+  for (int item = i0; item < i1; ++item) {
+    int e, g, p0, cnt, K;
+    const uint8_t *wq;
+    const float *ws;
+    if (item < n_routed * items_r) {
+      K = K_r;
+      e = active[item / items_r];
+      g = item % items_r;
+      wq = wq_r + (size_t)e * rows_r * (K / 2);
+      ws = ws_r + (size_t)e * rows_r * (K / 64);
       p0 = offsets[e];
       cnt = offsets[e + 1] - p0;
     } else {
+      K = K_s;
       e = E;
-      n = (item - n_routed * slabs_r) * W13_WARPS + warp;
-      q13 = sh.w13q;
-      s13 = sh.w13s;
+      g = item - n_routed * items_r;
+      wq = wq_s;
+      ws = ws_s;
       p0 = A;
       cnt = T;
     }
-    const size_t row1 = w13_row_of(n, 0), row3 = w13_row_of(n, 1);
-    const uint8_t *r1 = q13 + row1 * (H / 2);
-    const uint8_t *r3 = q13 + row3 * (H / 2);
-    const float *rs1 = s13 + row1 * (H / 64);
-    const float *rs3 = s13 + row3 * (H / 64);
-    for (int b0 = 0; b0 < cnt; b0 += kGemvTokens) {
-      const int nb = min(kGemvTokens, cnt - b0);
-      size_t xoff[kGemvTokens];
-#pragma unroll
-      for (int i = 0; i < kGemvTokens; ++i) {
-        const int p = p0 + b0 + min(i, nb - 1);
-        const int t = (e < E) ? perm[p] / k : (p - A);
-        xoff[i] = (size_t)t * H;
-      }
-      float g[kGemvTokens] = {}, u[kGemvTokens] = {};
-      for (int c = lane; c < chunks; c += 32) {
-        const uint4 w1 = ld_stream(r1 + (size_t)c * 16);
-        const uint4 w3 = ld_stream(r3 + (size_t)c * 16);
-        const float sc1 = __ldg(rs1 + (c >> 1)), sc3 = __ldg(rs3 + (c >> 1));
-#pragma unroll
-        for (int i = 0; i < kGemvTokens; ++i) {
-          if (i < nb) {
-            float xv[32];
-            load_x32(x, x_is_bf16, xoff[i], c * 32, xv);
-            g[i] = fmaf(sc1, dot32(w1, xv), g[i]);
-            u[i] = fmaf(sc3, dot32(w3, xv), u[i]);
+    const int chunks = K / 32;   // 16-byte chunks per row
+    for (int b0 = 0; b0 < cnt; b0 += NT) {
+      const int nb = min(NT, cnt - b0);
+      if (e != staged_e || b0 != staged_b) {
+        __syncthreads();   // previous readers are done
+        for (int i = threadIdx.x; i < NT * (K / 4); i += blockDim.x) {
+          const int tkn = i / (K / 4), c4 = i - tkn * (K / 4);
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (tkn < nb) {
+            const int p = p0 + b0 + tkn;
+            // W13 reads the token's x row; W2 reads the grouped position's h row.
+            const int src = (mode == 0) ? ((e < E) ? perm[p] / k : p - A) : p;
+            if (act_is_bf16) {
+              const uint2 u = __ldg(reinterpret_cast<const uint2 *>(
+                                        reinterpret_cast<const __nv_bfloat16 *>(act) +
+                                        (size_t)src * act_stride) +
+                                    c4);
+              v = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                              __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+            } else {
+              v = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(act) +
+                                                         (size_t)src * act_stride) +
+                        c4);
+            }
           }
+          reinterpret_cast<float4 *>(act_s + (size_t)tkn * K)[c4] = v;
+        }
+        __syncthreads();
+        staged_e = e;
+        staged_b = b0;
+      }
+      const uint8_t *wrow[kRowsPerWarp];
+      const float *srow[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const size_t row = (size_t)g * kRowsPerItem + rr[i];
+        wrow[i] = wq + row * (K / 2);
+        srow[i] = ws + row * (K / 64);
+      }
+      float acc[kRowsPerWarp][NT];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[i][t] = 0.f;
+#pragma unroll 2
+      for (int c = lane; c < chunks; c += 32) {
+        uint4 wv[kRowsPerWarp];
+        float sc[kRowsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          wv[i] = ld_stream(wrow[i] + (size_t)c * 16);
+          sc[i] = __ldg(srow[i] + (c >> 1));
+        }
+        // activations of this chunk (32 K) for each token, as f32 pairs
+        float2 xa[NT][16];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float4 *xp = reinterpret_cast<const float4 *>(act_s + (size_t)t * K + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = xp[j];
+            xa[t][2 * j] = make_float2(f.x, f.y);
+            xa[t][2 * j + 1] = make_float2(f.z, f.w);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          float2 part[NT];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) part[t] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            float2 q[4];
+            dequant8(words[wi], q);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int t = 0; t < NT; ++t) part[t] = __ffma2_rn(q[j], xa[t][4 * wi + j], part[t]);
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[i][t] = fmaf(sc[i], part[t].x + part[t].y, acc[i][t]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < kGemvTokens; ++i) {
-        if (i < nb) {
-          const float gg = warp_sum(g[i]);
-          const float uu = warp_sum(u[i]);
-          if (lane == 0) {
-            const float silu = gg / (1.0f + expf(-gg));
-            hbuf[(size_t)(p0 + b0 + i) * h_stride + n] = silu * uu;
+      for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[i][t] += __shfl_xor_sync(0xffffffffu, acc[i][t], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t < nb) {
+            const int p = p0 + b0 + t;
+            if (mode == 0) {
+              // 32-row group g = 128-row block g/4, quadrant g%4: features
+              // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
+              const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float gg = acc[j][t], uu = acc[2 + j][t];
+                out[(size_t)p * out_stride + f0 + j] = gg / (1.0f + expf(-gg)) * uu;
+              }
+            } else {
+              const float wt = (e < E) ? wts[perm[p]] : 1.0f;
+#pragma unroll
+              for (int i = 0; i < kRowsPerWarp; ++i)
+                out[(size_t)p * out_stride + g * kRowsPerItem + rr[i]] = wt * acc[i][t];
+            }
           }
         }
       }
@@ -182,75 +234,63 @@ __global__ void __launch_bounds__(256) gemv_w13_kernel(
   }
 }
 
-// ---------------------------------------------------------------------------
-// W2 + combine.  Block = 8 warps, one output row o per warp, all tokens.
-__global__ void __launch_bounds__(256) gemv_w2_combine_kernel(
-    int T, int H, int k, int E, int I, int Is, int n_shared, int h_stride, ExpertWeights ex,
-    ExpertWeights sh, const int32_t *__restrict__ idx, const float *__restrict__ wts,
-    const int32_t *__restrict__ inv, const float *__restrict__ hbuf, float *__restrict__ out,
-    int accumulate) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int A = T * k;
-  for (int o = blockIdx.x * 8 + warp; o < H; o += gridDim.x * 8) {
-    for (int t = 0; t < T; ++t) {
-      float acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int e = idx[t * k + j];
-        const int p = inv[t * k + j];
-        const uint8_t *r2 = ex.w2q + ((size_t)e * H + o) * (I / 2);
-        const float *rs2 = ex.w2s + ((size_t)e * H + o) * (I / 64);
-        const float *hp = hbuf + (size_t)p * h_stride;
-        float part = 0.f;
-        for (int c = lane; c < I / 32; c += 32) {
-          const uint4 wq = ld_stream(r2 + (size_t)c * 16);
-          float hv[32];
-          load_x32(hp, 0, 0, c * 32, hv);
-          part = fmaf(__ldg(rs2 + (c >> 1)), dot32(wq, hv), part);
-        }
-        acc = fmaf(wts[t * k + j], warp_sum(part), acc);
-      }
-      if (n_shared) {
-        const uint8_t *r2 = sh.w2q + (size_t)o * (Is / 2);
-        const float *rs2 = sh.w2s + (size_t)o * (Is / 64);
-        const float *hp = hbuf + (size_t)(A + t) * h_stride;
-        float part = 0.f;
-        for (int c = lane; c < Is / 32; c += 32) {
-          const uint4 wq = ld_stream(r2 + (size_t)c * 16);
-          float hv[32];
-          load_x32(hp, 0, 0, c * 32, hv);
-          part = fmaf(__ldg(rs2 + (c >> 1)), dot32(wq, hv), part);
-        }
-        acc += warp_sum(part);
-      }
-      if (lane == 0) {
-        float *dst = out + (size_t)t * H + o;
-        *dst = accumulate ? *dst + acc : acc;
-      }
-    }
+template <int NT>
+cudaError_t launch_nt(int mode, const moe_handle *h, const void *act, int act_bf16, int act_stride,
+                      int T, int K, int K_s, int rows_r, int rows_s, const uint8_t *wq_r, const float *ws_r,
+                      const uint8_t *wq_s, const float *ws_s, float *out, int out_stride,
+                      cudaStream_t st) {
+  const size_t smem = (size_t)NT * (K > K_s ? K : K_s) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(
+        gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr = true;
   }
+  // Exactly the resident CTAs: items are split into contiguous per-CTA ranges,
+  // so a CTA that waited for a slot would add a second wave.
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<NT>, kWarps * 32, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int blocks = h->num_sms * per_sm;
+  gemv_kernel<NT><<<blocks, kWarps * 32, smem, st>>>(
+      mode, act, act_bf16, act_stride, T, h->k, h->E, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s, ws_s,
+      h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.w, out, out_stride);
+  return cudaGetLastError();
+}
+
+// Tokens per pass: up to 4, as many as fit 96 KB of f32 activations.
+cudaError_t launch_gemv(int mode, const moe_handle *h, const void *act, int act_bf16,
+                        int act_stride, int T, int K, int K_s, int rows_r, int rows_s, const uint8_t *wq_r,
+                        const float *ws_r, const uint8_t *wq_s, const float *ws_s, float *out,
+                        int out_stride, cudaStream_t st) {
+  const int fit = kActSmemBytes / ((K > K_s ? K : K_s) * 4);
+  if (fit >= 4 && T >= 3)
+    return launch_nt<4>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
+                        ws_s, out, out_stride, st);
+  if (fit >= 2 && T >= 2)
+    return launch_nt<2>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
+                        ws_s, out, out_stride, st);
+  return launch_nt<1>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
+                      ws_s, out, out_stride, st);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t st) {
-  const int blocks = h->num_sms * 4;
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  gemv_w13_kernel<<<blocks, 256, 0, st>>>(x, h->L.x_dtype == 1, T, h->H, h->k, h->E, h->I,
-                                          h->S ? h->Is : W13_WARPS, h_stride, h->ex, h->sh,
-                                          h->ws.active, h->ws.n_active, h->ws.offsets,
-                                          h->ws.perm, h->ws.h);
-  return cudaGetLastError();
+  return launch_gemv(0, h, x, h->L.x_dtype == 1, h->H, T, h->H, h->H, 2 * h->I,
+                     h->S ? 2 * h->Is : 0,
+                     h->ex.w13q, h->ex.w13s, h->sh.w13q, h->sh.w13s, h->ws.h, h_stride, st);
 }
 
-cudaError_t launch_gemv_w2_combine(const moe_handle *h, int T, float *out, bool accumulate,
-                                   cudaStream_t st) {
+cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  int blocks = (h->H + 7) / 8;
-  if (blocks > h->num_sms * 4) blocks = h->num_sms * 4;
-  gemv_w2_combine_kernel<<<blocks, 256, 0, st>>>(T, h->H, h->k, h->E, h->I, h->Is, h->S,
-                                                 h_stride, h->ex, h->sh, h->ws.idx, h->ws.w,
-                                                 h->ws.inv, h->ws.h, out, accumulate ? 1 : 0);
-  return cudaGetLastError();
+  return launch_gemv(1, h, h->ws.h, 0, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,
+                     h->S ? h->H : 0, h->ex.w2q,
+                     h->ex.w2s, h->sh.w2q, h->sh.w2s, h->ws.y, h->H, st);
 }
 
 }  // namespace moe

@@ -630,6 +630,13 @@ constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
 
 bool tc_path_available() { return get_encode() != nullptr; }
 
+cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
+                           cudaStream_t st) {
+  combine_kernel<<<h->num_sms * 8, 256, 0, st>>>(T, h->H, h->k, h->S, h->ws.inv, h->ws.y, out,
+                                                 accumulate ? 1 : 0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
                            cudaStream_t st) {
   const moe::Workspace &w = h->ws;
@@ -711,9 +718,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
     cudaEventRecord(hm->ev[hm->n_ev++], st);
   }
   hm->launches += 1;
-  combine_kernel<<<h->num_sms * 8, 256, 0, st>>>(T, H, k, S, w.inv, w.y, out, accumulate ? 1 : 0);
+  err = launch_combine(h, T, out, accumulate, st);
   hm->launches += 1;
-  err = cudaGetLastError();
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "combine";
     cudaEventRecord(hm->ev[hm->n_ev++], st);

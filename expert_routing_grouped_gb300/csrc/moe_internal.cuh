@@ -96,10 +96,11 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
 cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t s);
 // gemv.cu
 cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t s);
-cudaError_t launch_gemv_w2_combine(const moe_handle *h, int T, float *out, bool accumulate,
-                                   cudaStream_t s);
+cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t s);
 // ggemm_tc.cu
 bool tc_path_available();
+cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
+                           cudaStream_t s);
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,
                            bool accumulate, cudaStream_t s);
 // misc.cu

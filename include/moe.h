@@ -191,7 +191,7 @@ int moe_debug_view(moe_handle *h, moe_debug *d);
 int moe_debug_read(moe_handle *h, int field, void *host_dst, size_t bytes);
 
 /* Stage times of the last forward with MOE_OPT_PROFILE on (synchronises).
- * Small-T path: router, dispatch, w13, w2+combine.  Tensor-core path: router,
+ * Small-T path: router, dispatch, w13, w2, combine.  Tensor-core path: router,
  * dispatch, gather, w13, w2, combine.  Writes up to `max` values in ms and the
  * stage count to *n; names[i] (optional) receives static strings. */
 int moe_stage_times(moe_handle *h, float *ms, const char **names, int max, int *n);

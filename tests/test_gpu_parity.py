@@ -44,12 +44,12 @@ def get_layer(wl, max_tokens, dev, layer=0):
     return _layers[key]
 
 
-def run_and_compare(wl, T, dev, regime=None, layer=0):
+def run_and_compare(wl, T, dev, regime=1, layer=0):
+    """Forward through the given expert path (default: the small-T GEMV path)."""
     import torch
     import expert_routing_grouped_gb300 as moe
     h, Wr, bias = get_layer(wl, max(T, 4), dev, layer)
-    if regime is not None:
-        h.set_option(moe.MOE_OPT_REGIME, regime)
+    h.set_option(moe.MOE_OPT_REGIME, regime)
     x, _ = margin_x(wl, T, Wr, bias)
     ref = oracle_layer(wl, layer, x, Wr, bias)
     xd = to_device_x(wl, x, dev)
@@ -99,7 +99,6 @@ def test_gemv_path_parity_olmoe_64(dev):
     import expert_routing_grouped_gb300 as moe
     wl = synth.BY_NAME["olmoe"]
     got, ref, h, _ = run_and_compare(wl, 64, dev, regime=moe.REGIME_GEMV)
-    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
     assert rel_l2(got, ref["out"]) <= GEMV_TOL
 
 
