@@ -21,7 +21,8 @@ MOE_DBG_IDX, MOE_DBG_W, MOE_DBG_COUNTS, MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_I
 
 EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual", "moe_forward_host",
            "moe_rmsnorm_bf16", "moe_set_option", "moe_debug_view", "moe_debug_read",
-           "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror")
+           "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror",
+           "moe_route_noalloc")
 
 
 class MoeLayout(ctypes.Structure):
@@ -67,6 +68,7 @@ def _load():
         "moe_device_bytes": (ctypes.c_size_t, [P]),
         "moe_free": (None, [P]),
         "moe_strerror": (ctypes.c_char_p, [i]),
+        "moe_route_noalloc": (i, [P, i, i, i, i, i, i, f, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -194,3 +196,11 @@ def layout_for(wl, max_tokens):
                      n_shared=wl.n_shared, shared_intermediate=wl.I_shared,
                      router_mode=wl.router_mode, routed_scaling_factor=wl.rsf,
                      x_dtype=wl.x_dtype, max_tokens=max_tokens)
+
+
+def route_noalloc(x, T, hidden, num_experts, top_k, x_dtype, router_mode, rsf, router_w_eh,
+                  router_bias, idx, w, stream=None):
+    """moe_route_noalloc: routing with no device allocation (see include/moe.h)."""
+    return _check(lib.moe_route_noalloc(_ptr(x), T, hidden, num_experts, top_k, x_dtype,
+                                        router_mode, rsf, _ptr(router_w_eh), _ptr(router_bias),
+                                        _ptr(idx), _ptr(w), _stream(stream)), "moe_route_noalloc")

@@ -10,6 +10,8 @@
 // Logits are plain f32 FMA (no TF32) so the selection matches an exact
 // reference whenever the top keys are separated by more than f32 rounding.
 // Every reduction runs in a fixed order, so results are bitwise reproducible.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -259,3 +261,102 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free routing (moe_route_noalloc).  The pages have no counterpart;
+// this serves callers that cannot call cudaMalloc (see include/moe.h).  It
+// launches the same router kernels as above, but their logit scratch lives in
+// the file-scope array below instead of a handle's workspace.
+
+namespace moe {
+namespace {
+
+constexpr size_t kRouteScratchFloats = size_t(1) << 20;   // 4 MiB per device
+static __device__ __align__(256) float g_route_scratch[kRouteScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float *g_scratch_ptr[kMaxDevices] = {};
+int g_scratch_sms[kMaxDevices] = {};
+
+// Device address of the scratch array for the current device (looked up once
+// per device with that device current).  Returns cudaSuccess or the error.
+cudaError_t scratch_for_current_device(float **ptr, int *num_sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (err != cudaSuccess) return err;
+    int sms = 0;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    g_scratch_ptr[dev] = static_cast<float *>(p);
+    g_scratch_sms[dev] = sms;
+  }
+  *ptr = g_scratch_ptr[dev];
+  *num_sms = g_scratch_sms[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
+    const void *x, int T, int hidden, int num_experts, int top_k, int x_dtype, int router_mode,
+    float routed_scaling_factor, const float *router_w_eh, const float *router_bias,
+    int32_t *idx, float *w, moe_stream_t stream) {
+  using namespace moe;
+  if (num_experts < 1 || num_experts > kMaxExperts || top_k < 1 || top_k > num_experts ||
+      top_k > kMaxTopK || (router_mode != 0 && router_mode != 1) ||
+      !(routed_scaling_factor > 0.f))
+    return MOE_ERR_ROUTING;
+  if (T < 0 || hidden < 512 || hidden % 512 || (x_dtype != 0 && x_dtype != 1))
+    return MOE_ERR_ARG;
+  if (router_mode == 1 && !router_bias) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w_eh || !idx || !w) return MOE_ERR_ARG;
+  const int E = num_experts, H = hidden;
+  // Scratch needed: split partials [splits][4][E] for T <= 4, logits [T][E] above.
+  if (T > 4 && (size_t)T * E > kRouteScratchFloats) return MOE_ERR_NOMEM;
+  float *z = nullptr;
+  int sms = 0;
+  if (scratch_for_current_device(&z, &sms) != cudaSuccess) return MOE_ERR_DEVICE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int xb = x_dtype == 1;
+  int splits = 1;
+  if (T <= 4) {
+    splits = router_splits(T, E, H, sms);
+    if ((size_t)splits * kGemvTokens * E > kRouteScratchFloats) return MOE_ERR_NOMEM;
+    const int hps = H / splits;
+    const size_t smem = (size_t)4 * hps * sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(router_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return MOE_ERR_DEVICE;
+    router_gemv_kernel<4><<<dim3((E + 7) / 8, splits), 256, smem, st>>>(x, xb, T, H, E,
+                                                                        router_w_eh, hps, z,
+                                                                        kGemvTokens);
+  } else {
+    router_gemm_kernel<<<dim3((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT), 256, 0, st>>>(
+        x, xb, T, H, E, router_w_eh, z);
+  }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_DEVICE;
+  const int zstride = (T <= 4) ? kGemvTokens : T;
+  const int epl = (E + 31) / 32;
+  const dim3 g2((T + 7) / 8);
+#define MOE_TOPK_NA(N)                                                                      \
+  router_topk_kernel<N><<<g2, 256, 0, st>>>(z, splits, zstride, T, E, top_k, router_mode,  \
+                                            router_bias, routed_scaling_factor, idx, w)
+  if (epl <= 1) MOE_TOPK_NA(1);
+  else if (epl <= 2) MOE_TOPK_NA(2);
+  else if (epl <= 4) MOE_TOPK_NA(4);
+  else if (epl <= 8) MOE_TOPK_NA(8);
+  else if (epl <= 16) MOE_TOPK_NA(16);
+  else MOE_TOPK_NA(32);
+#undef MOE_TOPK_NA
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
+}

@@ -178,6 +178,42 @@ int moe_set_option(moe_handle *h, int option, int value);
 /* Fills *d with device pointers describing the last forward call. */
 int moe_debug_view(moe_handle *h, moe_debug *d);
 
+/*
+ * Allocation-free routing.  The pages have no counterpart to this call; it
+ * exists for callers that cannot call cudaMalloc: code running inside a
+ * stream-capture region, where allocation is not allowed; hot loops that must
+ * not pay for the device-wide synchronisation cudaMalloc/cudaFree may cause;
+ * and processes whose GPU memory is entirely owned by another allocator (a
+ * framework's caching allocator, a fixed arena).  Such a caller cannot create
+ * a moe_handle, because moe_init allocates.
+ *
+ * Runs steps 1-2 of the layer (router logits in f32, then softmax or
+ * sigmoid + noaux_tc top-k with renormalised weights times rsf) with the same
+ * kernels as moe_forward, and allocates nothing: the logit scratch is a fixed
+ * 4 MiB array in the library's device image, which every GPU that loads the
+ * library keeps until the process exits.
+ *   x            [T][hidden] device, f32 (x_dtype 0) or bf16 (x_dtype 1)
+ *   router_w_eh  [num_experts][hidden] f32 device: row e is expert e's router
+ *                vector (the layout of a linear layer's weight; the transpose
+ *                of moe_weights.router_w)
+ *   router_bias  [num_experts] f32 device, or NULL (softmax mode only)
+ *   idx, w       [T][top_k] device outputs, as moe_debug.idx / moe_debug.w
+ * Limits: hidden a multiple of 512; num_experts <= 1024; top_k <= 32; for
+ * T > 4, T * num_experts <= 1048576 (larger calls return MOE_ERR_NOMEM and
+ * launch nothing).  T == 0 does nothing.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one scratch array, which
+ * keeps the last call's contents; nothing in it needs clearing, because every
+ * value a call reads was written earlier in the same call.  Calls that
+ * overlap on the GPU (different streams, or concurrent host threads) race on
+ * the scratch and must be serialised by the caller.
+ * Returns MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_ARG or MOE_ERR_DEVICE.
+ */
+int moe_route_noalloc(const void *x, int T, int hidden, int num_experts, int top_k, int x_dtype,
+                      int router_mode, float routed_scaling_factor, const float *router_w_eh,
+                      const float *router_bias, int32_t *idx, float *w, moe_stream_t stream);
+
 /* Fields of moe_debug_read. */
 #define MOE_DBG_IDX 0      /* int32 [T][k]  */
 #define MOE_DBG_W 1        /* f32   [T][k]  */
