@@ -15,6 +15,9 @@ a "decode" object carries the decode step.  Metric: MoE-layer tokens/s.
 Multi-GPU (torchrun): replicas only -- each rank runs its own replica, no data
 is exchanged; value = tokens of all ranks / max time over ranks.
 
+prefill_small is a reduced GLM-shaped layer (32 experts, T = 2048, ~2.5 GB on
+the device) used for detailed kernel profiles; it is not a headline workload.
+
 --impl reference times the f64 oracle (plain C, one host core) on a bounded
 sample of the same workload: the slow reference arm.
 """
@@ -131,12 +134,12 @@ def make_layer(wl, layer, max_tokens, dev):
 
 # -------------------------------------------------------------- prefill --
 
-def bench_prefill(dev, steps, warmup, stream):
+def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
-    wl = synth.BY_NAME["glm_prefill"]
-    T = 4096
+    wl = synth.BY_NAME[name]
+    T = wl.tokens[0]
     layer, Wr, bias = make_layer(wl, 0, T, dev)
     x = synth.x_rows(wl, T)
     xd = torch.from_numpy(x).to(dev)
@@ -324,7 +327,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="both", choices=["both", "prefill", "decode"])
+    ap.add_argument("--workload", default="both",
+                    choices=["both", "prefill", "decode", "prefill_small"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -367,11 +371,12 @@ def main():
     stream = torch.cuda.Stream()
     pk, src = peaks()
 
-    do_prefill = args.workload in ("both", "prefill")
+    do_prefill = args.workload in ("both", "prefill", "prefill_small")
     do_decode = args.workload in ("both", "decode")
     pre = dec = None
     if do_prefill:
-        pre = bench_prefill(dev, args.steps, args.warmup, stream)
+        pre = bench_prefill(dev, args.steps, args.warmup, stream,
+                            "glm_prefill_small" if args.workload == "prefill_small" else "glm_prefill")
         if pre["regime"] != 2 and args.workload == "both":
             pre = None          # tensor-core path unavailable: decode becomes the headline
     if do_decode:

@@ -19,7 +19,8 @@
 // output rows); each of the 8 warps streams 4 of those rows over the full K
 // with 128-bit non-allocating loads (a lane's 16 bytes = 32 weights inside one
 // 64-wide scale group).  The expert's activation rows sit in shared memory as
-// f32 (staged when the expert changes) and are reused across the 4 rows.
+// f32 (staged when the expert changes, XOR-swizzled against bank conflicts)
+// and are reused across the 4 rows.
 // Dequant and FMAs use packed f32x2 arithmetic.  CTAs take contiguous item
 // ranges, so one activation stage serves many items.
 #include "moe_internal.cuh"
@@ -142,7 +143,10 @@ __global__ void __launch_bounds__(256) gemv_kernel(
                         c4);
             }
           }
-          reinterpret_cast<float4 *>(act_s + (size_t)tkn * K)[c4] = v;
+          // float4 j of 32-float chunk c is stored at slot j ^ (c & 7) of the
+          // chunk: lanes reading the same j of chunks c..c+7 hit 8 bank groups.
+          const int cc = c4 >> 3, jj = c4 & 7;
+          reinterpret_cast<float4 *>(act_s + (size_t)tkn * K)[cc * 8 + (jj ^ (cc & 7))] = v;
         }
         __syncthreads();
         staged_e = e;
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           const float4 *xp = reinterpret_cast<const float4 *>(act_s + (size_t)t * K + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 f = xp[j];
+            const float4 f = xp[j ^ (c & 7)];
             xa[t][2 * j] = make_float2(f.x, f.y);
             xa[t][2 * j + 1] = make_float2(f.z, f.w);
           }

@@ -594,6 +594,167 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
   }
 }
 
+// ------------------------------------------------- router on tensor cores --
+//
+// z[t][e] = sum_h x[t][h] * Wr[e][h] for bf16 x, with Wr held as three bf16
+// planes hi + mid + lo (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi -
+// mid): 24 significant bits, the f32 value up to its last bit).  All three
+// planes accumulate into one f32 TMEM accumulator, so the logits carry f32
+// rounding, not bf16 (the router stays f32: colibrì engine teardown,
+// "System map").  Tile: 128 experts x 64 tokens, one tile per CTA.
+constexpr int RT_N = 64;         // tokens per tile
+constexpr int RT_S = 3;          // stages
+constexpr uint32_t RT_STAGE_TX = 3 * BM * 128 + RT_N * 128;
+
+struct __align__(1024) SmemRT {
+  uint8_t a[RT_S][3][BM * 128];  // 3 stages x 3 planes x 16 KB
+  uint8_t b[RT_S][RT_N * 128];   // 3 stages x 8 KB
+  uint64_t full[RT_S], empty[RT_S], acc_full;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct RtParams {
+  CUtensorMap map_a;       // bf16 planes [3E][H]
+  CUtensorMap map_x;       // bf16 x [T][H]
+  int E, T, H;
+  float *z;                // [T][E]
+  int32_t *status;
+};
+
+__device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *sm,
+                                        int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*reinterpret_cast<volatile int *>(&sm->abort)) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        atomicExch(reinterpret_cast<int *>(&sm->abort), 1);
+        atomicExch(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant__ RtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemRT *sm = reinterpret_cast<SmemRT *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * BM, t0 = blockIdx.y * RT_N;
+  const int nk = p.H / BK;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RT_S; ++i) {
+      mbar_init(&sm->full[i], 1);
+      mbar_init(&sm->empty[i], 1);
+    }
+    mbar_init(&sm->acc_full, 1);
+    sm->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 64;" ::"r"(
+                     smem_u32(&sm->tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int last_par[RT_S] = {-1, -1, -1};
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % RT_S;
+        const uint32_t ph = (kb / RT_S) & 1;
+        if (!rt_wait(&sm->empty[s], ph ^ 1, sm, p.status)) break;
+        mbar_expect_tx(&sm->full[s], RT_STAGE_TX);
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+          tma_load_2d(sm->a[s][pl], &p.map_a, kb * BK, pl * p.E + e0, &sm->full[s]);
+        tma_load_2d(sm->b[s], &p.map_x, kb * BK, t0, &sm->full[s]);
+        last_par[s] = ph;
+      }
+      const unsigned long long tw = globaltimer();
+      for (int s = 0; s < RT_S; ++s)
+        while (last_par[s] >= 0 && !mbar_try_wait(&sm->full[s], last_par[s]) &&
+               globaltimer() - tw < kWaitNs) {
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, RT_N);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % RT_S;
+        if (!(ok = rt_wait(&sm->full[s], (kb / RT_S) & 1, sm, p.status))) break;
+        tc_fence_after();
+        const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+          const uint64_t da = sw128_desc(smem_u32(sm->a[s][pl]));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                     (kb | pl | kk) ? 1u : 0u);
+        }
+        mma_commit(&sm->empty[s]);
+      }
+      if (ok) {
+        mma_commit(&sm->acc_full);
+        const unsigned long long tw = globaltimer();
+        while (!mbar_try_wait(&sm->acc_full, 0) && globaltimer() - tw < kWaitNs) {
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    const int q = warp - 4;
+    const int e = e0 + q * 32 + lane;
+    if (rt_wait(&sm->acc_full, 0, sm, p.status)) {
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < RT_N; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        if (e < p.E) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int t = t0 + c0 + j;
+            if (t < p.T) p.z[(size_t)t * p.E + e] = v[j];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;" ::"r"(tmem) : "memory");
+  }
+}
+
+// hi/mid/lo bf16 planes of the transposed router weights: planes [3][E][H].
+__global__ void split_planes_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ planes,
+                                    long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    planes[i] = hi;
+    planes[n + i] = mid;
+    planes[2 * n + i] = lo;
+  }
+}
+
 // ---------------------------------------------------------- host side --
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -629,6 +790,36 @@ constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
 }  // namespace
 
 bool tc_path_available() { return get_encode() != nullptr; }
+
+cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
+                                cudaStream_t st) {
+  split_planes_kernel<<<152 * 4, 256, 0, st>>>(wr_t, planes, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t st) {
+  const int E = h->E, H = h->H;
+  static bool attr = false;
+  const size_t smem = sizeof(SmemRT) + 1024;
+  if (!attr) {
+    cudaError_t err =
+        cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  RtParams p{};
+  if (!make_map(&p.map_a, h->wr_planes, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, (uint64_t)3 * E, H,
+                BK, BM) ||
+      !make_map(&p.map_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, (uint64_t)T, H, BK, RT_N))
+    return cudaErrorInvalidValue;
+  p.E = E;
+  p.T = T;
+  p.H = H;
+  p.z = z;
+  p.status = h->ws.status;
+  router_tc_kernel<<<dim3((E + BM - 1) / BM, (T + RT_N - 1) / RT_N), 256, smem, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
                            cudaStream_t st) {

@@ -69,6 +69,7 @@ void carve(moe_handle *h, Carver &c) {
   const size_t maxT = h->L.max_tokens, A = maxT * k, rows = A + S * maxT;
   const size_t Imax = I > Is ? I : Is;
   h->wr_t = c.take<float>(E * H);
+  h->wr_planes = c.take<__nv_bfloat16>(3 * E * H);
   h->bias = c.take<float>(E);
   h->ex.w13q = c.take<uint8_t>(E * 2 * I * H / 2);
   h->ex.w2q = c.take<uint8_t>(E * H * I / 2);
@@ -179,6 +180,8 @@ int copy_weights(moe_handle *h, const moe_weights *W) {
       rc = MOE_ERR_NOMEM;
     } else if (cudaMemcpy(tmp, W->router_w, E * H * 4, cudaMemcpyDefault) != cudaSuccess ||
                moe::launch_transpose_router(tmp, h->wr_t, (int)H, (int)E, 0) != cudaSuccess ||
+               moe::launch_split_planes(h->wr_t, h->wr_planes, (long long)(E * H), 0) !=
+                   cudaSuccess ||
                cudaDeviceSynchronize() != cudaSuccess) {
       rc = MOE_ERR_DEVICE;
     }

@@ -67,6 +67,7 @@ struct moe_handle {
   size_t x_elem;                 // 4 (f32) or 2 (bf16)
   // weights (device, library-owned)
   float *wr_t;                   // [E][H] f32 router weights, transposed
+  __nv_bfloat16 *wr_planes;      // [3][E][H] bf16 hi/mid/lo planes of wr_t (tensor-core router)
   float *bias;                   // [E] or nullptr
   moe::ExpertWeights ex;         // routed experts
   moe::ExpertWeights sh;         // shared expert (single)
@@ -101,6 +102,9 @@ cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t s);
 bool tc_path_available();
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
                            cudaStream_t s);
+cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
+                                cudaStream_t s);
+cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t s);
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,
                            bool accumulate, cudaStream_t s);
 // misc.cu

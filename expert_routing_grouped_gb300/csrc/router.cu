@@ -7,8 +7,10 @@
 // §2.1 step 2) or sigmoid with a noaux_tc selection bias, n_group = 1, scaled
 // by routed_scaling_factor (teardown "Three key engineering decisions" (1)).
 //
-// Logits are plain f32 FMA (no TF32) so the selection matches an exact
-// reference whenever the top keys are separated by more than f32 rounding.
+// Logits carry f32 rounding (plain f32 FMA here; for large T with bf16
+// activations, tensor cores over three bf16 planes of the f32 weights, see
+// ggemm_tc.cu) so the selection matches an exact reference whenever the top
+// keys are separated by more than f32 rounding.  No TF32.
 // Every reduction runs in a fixed order, so results are bitwise reproducible.
 #include <mutex>
 
@@ -237,6 +239,10 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
     }
     router_gemv_kernel<4><<<grid, 256, smem, st>>>(x, xb, T, H, E, h->wr_t, hps, h->ws.z_part,
                                                    kGemvTokens);
+  } else if (xb && tc_path_available()) {
+    // bf16 activations: tensor cores on the three bf16 planes of the f32 weights.
+    cudaError_t err = launch_router_tc(h, x, T, h->ws.z_part, st);
+    if (err != cudaSuccess) return err;
   } else {
     const dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT);
     router_gemm_kernel<<<grid, 256, 0, st>>>(x, xb, T, H, E, h->wr_t, h->ws.z_part);

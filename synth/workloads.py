@@ -67,5 +67,12 @@ GLM_PREFILL = Workload("glm_prefill", H=6144, E=256, k=8, I=2048, n_shared=1, I_
                        seed=5, bias="zipf", zipf_s=1.2,
                        notes="GLM-5.2-style prefill layer, Zipf(1.2) expert loads")
 
-ALL = (TINY, OLMOE, MIXTRAL, GLM_DECODE, GLM_PREFILL)
+# A reduced GLM-shaped prefill layer (32 experts, uniform-ish routing) that
+# holds ~2.5 GB on the device: the case the detailed kernel profiles capture.
+GLM_PREFILL_SMALL = Workload("glm_prefill_small", H=6144, E=32, k=8, I=2048, n_shared=1,
+                             I_shared=2048, router_mode=ROUTER_SIGMOID, rsf=2.5, x_dtype=X_BF16,
+                             tokens=(2048,), seed=6, bias="normal", bias_sigma=0.1,
+                             notes="GLM-shaped layer with 32 experts, for kernel profiles")
+
+ALL = (TINY, OLMOE, MIXTRAL, GLM_DECODE, GLM_PREFILL, GLM_PREFILL_SMALL)
 BY_NAME = {w.name: w for w in ALL}
