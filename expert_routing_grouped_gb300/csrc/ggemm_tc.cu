@@ -599,10 +599,13 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
 // z[t][e] = sum_h x[t][h] * Wr[e][h] for bf16 x, with Wr held as three bf16
 // planes hi + mid + lo (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi -
 // mid): 24 significant bits, the f32 value up to its last bit).  All three
-// planes accumulate into one f32 TMEM accumulator, so the logits carry f32
-// rounding, not bf16 (the router stays f32: colibrì engine teardown,
-// "System map").  Tile: 128 experts x 64 tokens, one tile per CTA.
+// planes accumulate in f32 TMEM, so the logits carry f32 rounding, not bf16
+// (the router stays f32: colibrì engine teardown, "System map").  The K range
+// is split over 8 accumulators, summed in IEEE f32 in the epilogue: the tensor
+// core's accumulation then never runs more than 1/8 of K in one chain.
+// Tile: 128 experts x 64 tokens, one tile per CTA.
 constexpr int RT_N = 64;         // tokens per tile
+constexpr int RT_ACC = 8;        // accumulators (TMEM columns RT_ACC * RT_N)
 constexpr int RT_S = 3;          // stages
 constexpr uint32_t RT_STAGE_TX = 3 * BM * 128 + RT_N * 128;
 
@@ -656,7 +659,7 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 64;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                      smem_u32(&sm->tmem_base))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -695,13 +698,16 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         if (!(ok = rt_wait(&sm->full[s], (kb / RT_S) & 1, sm, p.status))) break;
         tc_fence_after();
         const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
+        const int acc = kb * RT_ACC / nk;                       // accumulator of this k-block
+        const bool first = (kb == 0) || ((kb - 1) * RT_ACC / nk != acc);
+        const uint32_t d = tmem + acc * RT_N;
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl) {
           const uint64_t da = sw128_desc(smem_u32(sm->a[s][pl]));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                     (kb | pl | kk) ? 1u : 0u);
+            mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                     (!first || pl || kk) ? 1u : 0u);
         }
         mma_commit(&sm->empty[s]);
       }
@@ -717,10 +723,18 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
     const int e = e0 + q * 32 + lane;
     if (rt_wait(&sm->acc_full, 0, sm, p.status)) {
       tc_fence_after();
+      const int n_acc = nk < RT_ACC ? nk : RT_ACC;   // accumulators that received k-blocks
 #pragma unroll
       for (int c0 = 0; c0 < RT_N; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        for (int a = 1; a < RT_ACC; ++a) {
+          if (a >= n_acc) break;
+          float u[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + a * RT_N + c0, u);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += u[j];
+        }
         if (e < p.E) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -735,7 +749,7 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;" ::"r"(tmem) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
 }
 
