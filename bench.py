@@ -15,8 +15,9 @@ a "decode" object carries the decode step.  Metric: MoE-layer tokens/s.
 Multi-GPU (torchrun): replicas only -- each rank runs its own replica, no data
 is exchanged; value = tokens of all ranks / max time over ranks.
 
-prefill_small is a reduced GLM-shaped layer (32 experts, T = 2048, ~2.5 GB on
-the device) used for detailed kernel profiles; it is not a headline workload.
+prefill_small / decode_small use a reduced GLM-shaped layer (32 experts, ~2.5 GB
+on the device; T = 2048 / T = 1) for detailed kernel profiles; they are not
+headline workloads.
 
 --impl reference times the f64 oracle (plain C, one host core) on a bounded
 sample of the same workload: the slow reference arm.
@@ -191,70 +192,86 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
 
 # --------------------------------------------------------------- decode --
 
-def bench_decode(dev, steps, warmup, stream, T=1):
+def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None):
+    """The decode stack: per layer an RMS pre-norm and moe_forward_residual.
+    The timed steps replay one CUDA graph of the whole stack (the library's
+    launches are stream-ordered and capturable); a separate eager pass with
+    tracing on gives the per-stage breakdown."""
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
-    wl = synth.BY_NAME["glm_decode"]
-    layers = [make_layer(wl, l, 4, dev)[0] for l in range(wl.layers)]
+    wl = synth.BY_NAME[name]
+    n_layers = layers or wl.layers
+    built = [make_layer(wl, l if wl.layers > 1 else 0, 4, dev)[0] for l in range(n_layers)]
     x = synth.x_rows(wl, T)
     x32 = torch.from_numpy(synth.bf16_to_f32(x)).to(dev)
     resid = torch.empty(T, wl.H, device=dev)
     u = torch.empty(T, wl.H, dtype=torch.int16, device=dev)
 
-    def step():
+    def step(st):
         resid.copy_(x32)
-        for lay in layers:
-            moe.rmsnorm_bf16(resid, T, wl.H, 1e-6, u, stream)
-            lay.forward_residual(u, T, resid, stream)
+        for lay in built:
+            moe.rmsnorm_bf16(resid, T, wl.H, 1e-6, u, st)
+            lay.forward_residual(u, T, resid, st)
 
-    for lay in layers:
+    # eager pass with tracing: stage breakdown and activated-expert counts
+    for lay in built:
         lay.set_option(moe.MOE_OPT_PROFILE, 1)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            step()
+            step(stream)
     torch.cuda.synchronize()
     n_active = []
-    for lay in layers:
+    for lay in built:
         idx = lay.debug_read(moe.MOE_DBG_IDX)
         n_active.append(distinct_active(idx, wl.n_shared))
-    launches0 = sum(l.debug_view().launches for l in layers)
     stage = {}
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(stream)
+            torch.cuda.synchronize()
+            for lay in built:
+                for nm, ms in lay.stage_times():
+                    stage.setdefault(nm, []).append(ms)
+    for lay in built:
+        lay.set_option(moe.MOE_OPT_PROFILE, 0)
+    # capture the stack once, replay it for the timed steps
+    launches0 = sum(l.debug_view().launches for l in built)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    per_replay = sum(l.debug_view().launches for l in built) - launches0 + n_layers
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    with torch.cuda.stream(stream):
-        with ClockSampler(dev.index or 0) as clk:
-            for i in range(steps):
-                evs[i][0].record(stream)
-                step()
-                evs[i][1].record(stream)
-                torch.cuda.synchronize()
-                for lay in layers:
-                    for name, ms in lay.stage_times():
-                        stage.setdefault(name, []).append(ms)
-            torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    with ClockSampler(dev.index or 0) as clk:
+        for i in range(steps):
+            evs[i][0].record(cur)
+            g.replay()
+            evs[i][1].record(cur)
+        torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    launches = sum(l.debug_view().launches for l in layers) - launches0 + steps * wl.layers
-    # e2e: pinned host x -> device, the stack, result -> host, per step
+    # e2e: pinned host x -> device, the stack, result -> host, every step
     xh = torch.from_numpy(synth.bf16_to_f32(x)).pin_memory()
     oh = torch.empty(T, wl.H).pin_memory()
-    for lay in layers:
-        lay.set_option(moe.MOE_OPT_PROFILE, 0)
     e2e = []
-    with torch.cuda.stream(stream):
-        for i in range(max(3, steps // 2) + 2):
-            t1 = time.perf_counter()
-            x32.copy_(xh, non_blocking=True)
-            step()
-            oh.copy_(resid, non_blocking=True)
-            stream.synchronize()
-            if i >= 2:
-                e2e.append(time.perf_counter() - t1)
-    res = dict(wl=wl, T=T, step_ms=step_ms,
+    for i in range(max(3, steps // 2) + 2):
+        t1 = time.perf_counter()
+        x32.copy_(xh, non_blocking=True)
+        g.replay()
+        oh.copy_(resid, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 2:
+            e2e.append(time.perf_counter() - t1)
+    res = dict(wl=wl, T=T, step_ms=step_ms, layers=n_layers,
                stage={k: statistics.mean(v) for k, v in stage.items()},
-               launches=launches, n_active=n_active, clocks=clk.summary(),
+               launches=per_replay * steps, n_active=n_active, clocks=clk.summary(),
                e2e_s=statistics.median(e2e), h2d=T * wl.H * 4, d2h=T * wl.H * 4)
-    for lay in layers:
+    del g
+    for lay in built:
         lay.close()
     torch.cuda.empty_cache()
     return res
@@ -328,7 +345,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="both",
-                    choices=["both", "prefill", "decode", "prefill_small"])
+                    choices=["both", "prefill", "decode", "prefill_small", "decode_small"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -372,7 +389,7 @@ def main():
     pk, src = peaks()
 
     do_prefill = args.workload in ("both", "prefill", "prefill_small")
-    do_decode = args.workload in ("both", "decode")
+    do_decode = args.workload in ("both", "decode", "decode_small")
     pre = dec = None
     if do_prefill:
         pre = bench_prefill(dev, args.steps, args.warmup, stream,
@@ -380,7 +397,11 @@ def main():
         if pre["regime"] != 2 and args.workload == "both":
             pre = None          # tensor-core path unavailable: decode becomes the headline
     if do_decode:
-        dec = bench_decode(dev, args.steps, args.warmup, stream)
+        if args.workload == "decode_small":
+            dec = bench_decode(dev, args.steps, args.warmup, stream, name="glm_prefill_small",
+                               layers=1)
+        else:
+            dec = bench_decode(dev, args.steps, args.warmup, stream)
 
     def reduce_max(v):
         if world == 1:
@@ -398,7 +419,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if head is pre else "f32", "data": "synthetic",
             "config": {"workload": head["wl"].name, "T": head["T"],
-                       "layers_per_step": 1 if head is pre else head["wl"].layers,
+                       "layers_per_step": 1 if head is pre else head["layers"],
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (weights %.1f GB per step)"
                              % ((layer_bytes(head["wl"], head["wl"].E + 1, head["T"]) if head is pre
@@ -417,9 +438,10 @@ def main():
     if dec is not None and head is not dec:
         dms = statistics.mean(dec["step_ms"])
         byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
-        line["decode"] = {"workload": "glm_decode x%d layers" % dec["wl"].layers, "T": dec["T"],
+        line["decode"] = {"workload": "%s x%d layers, CUDA-graph replay" % (dec["wl"].name, dec["layers"]),
+                          "T": dec["T"],
                           "tokens_per_s": dec["T"] / (dms * 1e-3), "ms_per_step": dms,
-                          "us_per_layer": 1e3 * dms / dec["wl"].layers,
+                          "us_per_layer": 1e3 * dms / dec["layers"],
                           "hbm_gbs": byts / (dms * 1e-3) / 1e9,
                           "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
                           "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
@@ -429,10 +451,10 @@ def main():
         byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
         line["hbm_gbs"] = byts / (dms * 1e-3) / 1e9
         line["hbm_frac"] = line["hbm_gbs"] / pk["hbm_gbs"]
-        line["us_per_layer"] = 1e3 * dms / dec["wl"].layers
+        line["us_per_layer"] = 1e3 * dms / dec["layers"]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(head["wl"], head["T"], 8 if head is pre else 1,
-                                            1 if head is pre else head["wl"].layers)
+                                            1 if head is pre else head["layers"])
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

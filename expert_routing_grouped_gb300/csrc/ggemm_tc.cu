@@ -52,6 +52,7 @@ struct __align__(1024) SmemTC {
   uint8_t raw[NR][BM * 128];     // 2 x 16 KB
   uint8_t a[NA][BM * 128];       // 3 x 16 KB
   uint8_t b[NA][BN * 128];       // 3 x 32 KB
+  float sc[NR][BM * (RK / 64)];  // 2 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
   uint64_t a_full[NA], b_full[NA], ab_empty[NA];
   uint64_t acc_full[2], acc_empty[2];
@@ -62,6 +63,8 @@ struct __align__(1024) SmemTC {
 struct TcParams {
   CUtensorMap map_w;       // raw weights of the routed experts [E * rows][K/2] u8
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
+  CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
+  CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
   CUtensorMap map_b;       // bf16 token operand [R][K]
   const float *scale;      // routed scales [E * rows][K/64]
   const float *scale_s;    // shared scales [rows_s][K/64]
@@ -304,16 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < NR; ++i) {
       mbar_init(&sm->raw_full[i], 1);
-      mbar_init(&sm->raw_empty[i], kDeqThreads);
+      mbar_init(&sm->raw_empty[i], kDeqThreads / 32);
     }
     for (int i = 0; i < NA; ++i) {
-      mbar_init(&sm->a_full[i], kDeqThreads / 2);
+      mbar_init(&sm->a_full[i], kDeqThreads / 64);
       mbar_init(&sm->b_full[i], 1);
       mbar_init(&sm->ab_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm->acc_full[i], 1);
-      mbar_init(&sm->acc_empty[i], 128);
+      mbar_init(&sm->acc_empty[i], 4);
     }
     sm->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -339,12 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
         const CUtensorMap *mw = tl.shared ? &p.map_ws : &p.map_w;
+        const CUtensorMap *ms = tl.shared ? &p.map_scs : &p.map_sc;
         for (int r = 0; ok && r < tl.K / RK; ++r) {
           const int s = rk % NR;
           const uint32_t ph = (rk / NR) & 1;
           if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
-          mbar_expect_tx(&sm->raw_full[s], BM * 128);
+          mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
           tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
+          tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
           last_raw_par[s] = ph;
           ++rk;
           for (int j = 0; j < RK / BK; ++j) {
@@ -454,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm->acc_empty[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->acc_empty[buf]);
       ++it;
     }
   } else if (warp >= kDeqWarp0) {
@@ -467,12 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       Tile tl;
       if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
-      const float *srow = (tl.shared ? p.scale_s : p.scale) + (size_t)tl.wrow0 * (tl.K / 64) +
-                          (size_t)r * (tl.K / 64);
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
-        const float2 sc = *reinterpret_cast<const float2 *>(srow + rr * (RK / 64) + half * 2);
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
+        const float2 sc = *reinterpret_cast<const float2 *>(&sm->sc[s][r * (RK / 64) + half * 2]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
@@ -496,10 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
             *reinterpret_cast<uint4 *>(arow + ((wv ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
           fence_proxy_async();
-          mbar_arrive(&sm->a_full[s2]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->a_full[s2]);
         }
         if (!ok) break;
-        mbar_arrive(&sm->raw_empty[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->raw_empty[s]);
         ++rk;
         kb += RK / BK;
       }
@@ -785,9 +791,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2D map over a row-major [rows][cols] array, box [box_rows][box_cols], 128B swizzle.
+// 2D map over a row-major [rows][cols] array, box [box_rows][box_cols], 128B
+// swizzle (or none).
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, uint64_t cols,
-              uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows,
+              bool swizzle = true) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -795,7 +803,8 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t e
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -871,11 +880,16 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   TcParams p{};
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   // ---- W13
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
   ok = ok && make_map(&p.map_b, w.xp, BF, 2, H, (uint64_t)maxR, H, BK, BN);
+  ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
+                      RK / 64, BM, false);
+  ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
+                      (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
   p.scale = h->ex.w13s;
   p.scale_s = S ? h->sh.w13s : h->ex.w13s;
@@ -908,6 +922,10 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
   ok = ok && make_map(&p.map_b, w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK, BN);
+  ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
+                      false);
+  ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
+                      RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
   p.scale = h->ex.w2s;
   p.scale_s = S ? h->sh.w2s : h->ex.w2s;
