@@ -16,8 +16,10 @@
 //               y[grouped row][o] in f32.
 //
 // Per CTA (one per SM, 16 warps):
-//   warp 0      TMA producer: raw int4 weight tiles (128 rows x 256 K) and
-//               bf16 token tiles (256 rows x 64 K), both 128-byte swizzled.
+//   warp 0      TMA producer of raw int4 weight tiles (128 rows x 256 K, 128-byte
+//               swizzled) and their gs64 scales, 4 stages deep;
+//   warp 2      TMA producer of bf16 token tiles (256 rows x 64 K, 128-byte
+//               swizzled); the two producers run independently.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
 //               f32 accumulate) M=128, N=16..256, K=16 by one thread, commits
 //               to mbarriers; two 256-column accumulators in TMEM so the
@@ -41,7 +43,7 @@ constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
 constexpr int BK = 64;           // K per bf16 stage (128 bytes of a row)
 constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
 constexpr int NA = 3;            // bf16 A/B stages
-constexpr int NR = 2;            // raw stages
+constexpr int NR = 4;            // raw stages
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
@@ -49,10 +51,10 @@ constexpr int kDeqThreads = 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 
 struct __align__(1024) SmemTC {
-  uint8_t raw[NR][BM * 128];     // 2 x 16 KB
+  uint8_t raw[NR][BM * 128];     // 4 x 16 KB
   uint8_t a[NA][BM * 128];       // 3 x 16 KB
   uint8_t b[NA][BN * 128];       // 3 x 32 KB
-  float sc[NR][BM * (RK / 64)];  // 2 x 2 KB: the raw stage's gs64 scales, [row][4]
+  float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
   uint64_t a_full[NA], b_full[NA], ab_empty[NA];
   uint64_t acc_full[2], acc_empty[2];
@@ -333,17 +335,18 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------------------ raw weight producer
     if (lane == 0) {
-      uint32_t rk = 0, kb = 0;
-      int last_raw_par[NR] = {-1, -1}, last_b_par[NA] = {-1, -1, -1};
+      uint32_t rk = 0;
+      int last_raw_par[NR];
+      for (int i = 0; i < NR; ++i) last_raw_par[i] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
         const CUtensorMap *mw = tl.shared ? &p.map_ws : &p.map_w;
         const CUtensorMap *ms = tl.shared ? &p.map_scs : &p.map_sc;
-        for (int r = 0; ok && r < tl.K / RK; ++r) {
+        for (int r = 0; r < tl.K / RK; ++r) {
           const int s = rk % NR;
           const uint32_t ph = (rk / NR) & 1;
           if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
@@ -352,15 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
           last_raw_par[s] = ph;
           ++rk;
-          for (int j = 0; j < RK / BK; ++j) {
-            const int s2 = kb % NA;
-            const uint32_t ph2 = (kb / NA) & 1;
-            if (!(ok = wait_bar(&sm->ab_empty[s2], ph2 ^ 1, sm, p.status))) break;
-            mbar_expect_tx(&sm->b_full[s2], BN * 128);
-            tma_load_2d(sm->b[s2], &p.map_b, (r * (RK / BK) + j) * BK, tl.p0, &sm->b_full[s2]);
-            last_b_par[s2] = ph2;
-            ++kb;
-          }
         }
       }
       // Drain: every copy this thread issued has landed before the CTA exits.
@@ -369,6 +363,28 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         while (last_raw_par[s] >= 0 && !mbar_try_wait(&sm->raw_full[s], last_raw_par[s]) &&
                globaltimer() - t0 < kWaitNs) {
         }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------ token tile producer
+    if (lane == 0) {
+      uint32_t kb = 0;
+      int last_b_par[NA];
+      for (int i = 0; i < NA; ++i) last_b_par[i] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        Tile tl;
+        if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+        for (int k = 0; k < tl.K / BK; ++k) {
+          const int s2 = kb % NA;
+          const uint32_t ph2 = (kb / NA) & 1;
+          if (!(ok = wait_bar(&sm->ab_empty[s2], ph2 ^ 1, sm, p.status))) break;
+          mbar_expect_tx(&sm->b_full[s2], BN * 128);
+          tma_load_2d(sm->b[s2], &p.map_b, k * BK, tl.p0, &sm->b_full[s2]);
+          last_b_par[s2] = ph2;
+          ++kb;
+        }
+      }
+      const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NA; ++s)
         while (last_b_par[s] >= 0 && !mbar_try_wait(&sm->b_full[s], last_b_par[s]) &&
                globaltimer() - t0 < kWaitNs) {
