@@ -14,8 +14,8 @@
 //
 // Also produced here, for the expert kernels: the ascending list of experts
 // that received tokens (the shared expert, id E, appended last), and the
-// tensor-core tile list: one entry (expert, first row) per tile_m rows of
-// every non-empty group, shared expert last.
+// tensor-core token blocks: one entry per tile_m tokens of every non-empty
+// group (the shared expert's included), costliest first.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -130,19 +130,33 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
     if (n_shared) active[na++] = E;
     *n_active = na;
   }
-  // Tensor-core tiles: (expert << 16 | m-tile index) packed in one int32.
-  const int nt = (tid < E) ? (c + tile_m - 1) / tile_m : 0;
-  const int tpos = block_exclusive_scan(nt, warp_sums, &total);
-  for (int i = 0; i < nt; ++i) tiles[tpos + i] = (tid << 16) | i;
-  if (tid == 0) {
-    int ntot = total;
-    if (n_shared) {
-      const int ns = (T + tile_m - 1) / tile_m;
-      for (int i = 0; i < ns; ++i) tiles[ntot + i] = (E << 16) | i;
-      ntot += ns;
+  // Tensor-core token blocks, (expert << 16 | block index) in one int32,
+  // ordered by cost so that a round-robin deal of tiles over the CTAs gives
+  // each a similar mix: every full block (routed experts in expert order, then
+  // the shared expert's), then the partial last blocks by size class
+  // (> 128 tokens, > 64, > 32, the rest).
+  const int nfull = (tid < E) ? c / tile_m : 0;
+  const int rem = (tid < E) ? c - nfull * tile_m : 0;
+  const int base_pos = block_exclusive_scan(nfull, warp_sums, &total);
+  for (int i = 0; i < nfull; ++i) tiles[base_pos + i] = (tid << 16) | i;
+  int ntot = total;
+  const int s_full = n_shared ? T / tile_m : 0, s_rem = n_shared ? T - s_full * tile_m : 0;
+  if (tid == 0)
+    for (int i = 0; i < s_full; ++i) tiles[ntot + i] = (E << 16) | i;
+  ntot += s_full;
+  for (int cls = 0; cls < 4; ++cls) {
+    const int lo = cls == 0 ? 128 : cls == 1 ? 64 : cls == 2 ? 32 : 0;
+    const int hi = cls == 0 ? tile_m : cls == 1 ? 128 : cls == 2 ? 64 : 32;
+    const int f = (rem > lo && rem <= hi) ? 1 : 0;
+    const int pos = block_exclusive_scan(f, warp_sums, &total);
+    if (f) tiles[ntot + pos] = (tid << 16) | nfull;
+    ntot += total;
+    if (s_rem > lo && s_rem <= hi) {
+      if (tid == 0) tiles[ntot] = (E << 16) | s_full;
+      ntot += 1;
     }
-    n_tiles[0] = ntot;
   }
+  if (tid == 0) n_tiles[0] = ntot;
 }
 
 }  // namespace

@@ -67,7 +67,7 @@ struct TcParams {
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
   CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
-  CUtensorMap map_b;       // bf16 token operand [R][K]
+  CUtensorMap map_b[4];    // bf16 token operand [R][K], boxes of 32/64/128/256 rows
   const float *scale;      // routed scales [E * rows][K/64]
   const float *scale_s;    // shared scales [rows_s][K/64]
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
@@ -374,12 +374,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+        // Smallest box that covers the tile's tokens: a 13-token tile of a
+        // cold expert moves 32 rows, not 256.
+        const int bi = tl.nvalid <= 32 ? 0 : tl.nvalid <= 64 ? 1 : tl.nvalid <= 128 ? 2 : 3;
+        const uint32_t bbytes = (32u << bi) * 128u;
         for (int k = 0; k < tl.K / BK; ++k) {
           const int s2 = kb % NA;
           const uint32_t ph2 = (kb / NA) & 1;
           if (!(ok = wait_bar(&sm->ab_empty[s2], ph2 ^ 1, sm, p.status))) break;
-          mbar_expect_tx(&sm->b_full[s2], BN * 128);
-          tma_load_2d(sm->b[s2], &p.map_b, k * BK, tl.p0, &sm->b_full[s2]);
+          mbar_expect_tx(&sm->b_full[s2], bbytes);
+          tma_load_2d(sm->b[s2], &p.map_b[bi], k * BK, tl.p0, &sm->b_full[s2]);
           last_b_par[s2] = ph2;
           ++kb;
         }
@@ -901,7 +905,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
-  ok = ok && make_map(&p.map_b, w.xp, BF, 2, H, (uint64_t)maxR, H, BK, BN);
+  for (int i = 0; i < 4; ++i)
+    ok = ok && make_map(&p.map_b[i], w.xp, BF, 2, H, (uint64_t)maxR, H, BK, 32u << i);
   ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
                       RK / 64, BM, false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
@@ -937,7 +942,9 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
-  ok = ok && make_map(&p.map_b, w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK, BN);
+  for (int i = 0; i < 4; ++i)
+    ok = ok && make_map(&p.map_b[i], w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK,
+                        32u << i);
   ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
                       false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
