@@ -56,11 +56,19 @@ struct __align__(1024) SmemTC {
   uint8_t b[NA][BN * 128];       // 3 x 32 KB
   float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
-  uint64_t a_full[NA], b_full[NA], ab_empty[NA];
+  uint64_t a_full[NA], a_empty[NA];
+  uint64_t b_full[NA], b_empty[NA];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
+
+// Token slots hold 32 KB: 256 rows of one 64-K block, or several K blocks of
+// a smaller box (8 blocks of 32 rows, ...), so small tiles keep as many K
+// blocks in flight as large ones keep bytes.
+__device__ __forceinline__ int box_index(int nvalid) {
+  return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 128 ? 2 : 3;
+}
 
 struct TcParams {
   CUtensorMap map_w;       // raw weights of the routed experts [E * rows][K/2] u8
@@ -313,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     }
     for (int i = 0; i < NA; ++i) {
       mbar_init(&sm->a_full[i], kDeqThreads / 64);
+      mbar_init(&sm->a_empty[i], 1);
       mbar_init(&sm->b_full[i], 1);
-      mbar_init(&sm->ab_empty[i], 1);
+      mbar_init(&sm->b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm->acc_full[i], 1);
@@ -367,25 +376,27 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   } else if (warp == 2) {
     // ------------------------------------------------------ token tile producer
     if (lane == 0) {
-      uint32_t kb = 0;
+      uint32_t sb = 0;                    // token slots filled so far
       int last_b_par[NA];
       for (int i = 0; i < NA; ++i) last_b_par[i] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
-        // Smallest box that covers the tile's tokens: a 13-token tile of a
-        // cold expert moves 32 rows, not 256.
-        const int bi = tl.nvalid <= 32 ? 0 : tl.nvalid <= 64 ? 1 : tl.nvalid <= 128 ? 2 : 3;
-        const uint32_t bbytes = (32u << bi) * 128u;
-        for (int k = 0; k < tl.K / BK; ++k) {
-          const int s2 = kb % NA;
-          const uint32_t ph2 = (kb / NA) & 1;
-          if (!(ok = wait_bar(&sm->ab_empty[s2], ph2 ^ 1, sm, p.status))) break;
-          mbar_expect_tx(&sm->b_full[s2], bbytes);
-          tma_load_2d(sm->b[s2], &p.map_b[bi], k * BK, tl.p0, &sm->b_full[s2]);
+        // Smallest box covering the tile's tokens; one slot carries 256 / rows
+        // K blocks of it (K / 64 is a multiple of 8).
+        const int bi = box_index(tl.nvalid);
+        const int rows = 32 << bi, kps = BN / rows;
+        for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
+          const int s2 = sb % NA;
+          const uint32_t ph2 = (sb / NA) & 1;
+          if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
+          mbar_expect_tx(&sm->b_full[s2], BN * 128);
+          for (int j = 0; j < kps; ++j)
+            tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, tl.p0,
+                        &sm->b_full[s2]);
           last_b_par[s2] = ph2;
-          ++kb;
+          ++sb;
         }
       }
       const unsigned long long t0 = globaltimer();
@@ -397,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kb = 0, it = 0;
+      uint32_t ka = 0, sb = 0, it = 0;
       int last_acc = -1;
       uint32_t last_acc_par = 0;
       bool ok = true;
@@ -410,20 +421,28 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         const int n_mma = (tl.nvalid + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
         const uint32_t d = tmem + buf * BN;
+        const int rows = 32 << box_index(tl.nvalid), kps = BN / rows;
         for (int k = 0; k < tl.K / BK; ++k) {
-          const int s = kb % NA;
-          const uint32_t ph = (kb / NA) & 1;
-          if (!(ok = wait_bar(&sm->a_full[s], ph, sm, p.status))) break;
-          if (!(ok = wait_bar(&sm->b_full[s], ph, sm, p.status))) break;
+          const int j = k % kps;              // K block inside the token slot
+          const int s2 = sb % NA;
+          if (j == 0) {
+            if (!(ok = wait_bar(&sm->b_full[s2], (sb / NA) & 1, sm, p.status))) break;
+          }
+          const int s = ka % NA;
+          if (!(ok = wait_bar(&sm->a_full[s], (ka / NA) & 1, sm, p.status))) break;
           tc_fence_after();
           const uint64_t da = sw128_desc(smem_u32(sm->a[s]));
-          const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
+          const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + j * rows * 128));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
                      (k | kk) ? 1u : 0u);
-          mma_commit(&sm->ab_empty[s]);
-          ++kb;
+          mma_commit(&sm->a_empty[s]);
+          ++ka;
+          if (j == kps - 1) {
+            mma_commit(&sm->b_empty[s2]);
+            ++sb;
+          }
         }
         if (!ok) break;
         mma_commit(&sm->acc_full[buf]);
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
           const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
           const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
-          if (!(ok = wait_bar(&sm->ab_empty[s2], ((kbj / NA) & 1) ^ 1, sm, p.status))) break;
+          if (!(ok = wait_bar(&sm->a_empty[s2], ((kbj / NA) & 1) ^ 1, sm, p.status))) break;
           uint8_t *arow = sm->a[s2] + r * 128;
           const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
