@@ -26,7 +26,8 @@
 //               epilogue of one tile overlaps the main loop of the next.
 //   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
 //   warps 8-15  dequant: raw int4 -> bf16(q * s) into the UMMA operand layout
-//               (K-major, 128-byte swizzle), one row-half per thread.
+//               (K-major, 128-byte swizzle); all 8 warps on each 64-K block in
+//               order, half a row per thread.
 // Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
 // the device status word, flags the CTA to stop, and the kernel drains its
 // outstanding copies and MMAs (bounded), frees TMEM and returns.
@@ -42,8 +43,9 @@ constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
 constexpr int BK = 64;           // K per bf16 stage (128 bytes of a row)
 constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
-constexpr int NA = 3;            // bf16 A/B stages
-constexpr int NR = 4;            // raw stages
+constexpr int NA = 4;            // bf16 A stages (dequantised weights)
+constexpr int NB = 3;            // token slots
+constexpr int NR = 3;            // raw stages
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
@@ -51,13 +53,13 @@ constexpr int kDeqThreads = 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 
 struct __align__(1024) SmemTC {
-  uint8_t raw[NR][BM * 128];     // 4 x 16 KB
-  uint8_t a[NA][BM * 128];       // 3 x 16 KB
-  uint8_t b[NA][BN * 128];       // 3 x 32 KB
-  float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
+  uint8_t raw[NR][BM * 128];     // 3 x 16 KB
+  uint8_t a[NA][BM * 128];       // 4 x 16 KB
+  uint8_t b[NB][BN * 128];       // 3 x 32 KB
+  float sc[NR][BM * (RK / 64)];  // 3 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
   uint64_t a_full[NA], a_empty[NA];
-  uint64_t b_full[NA], b_empty[NA];
+  uint64_t b_full[NB], b_empty[NB];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
@@ -320,8 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       mbar_init(&sm->raw_empty[i], kDeqThreads / 32);
     }
     for (int i = 0; i < NA; ++i) {
-      mbar_init(&sm->a_full[i], kDeqThreads / 64);
+      mbar_init(&sm->a_full[i], kDeqThreads / 32);
       mbar_init(&sm->a_empty[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
       mbar_init(&sm->b_full[i], 1);
       mbar_init(&sm->b_empty[i], 1);
     }
@@ -377,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     // ------------------------------------------------------ token tile producer
     if (lane == 0) {
       uint32_t sb = 0;                    // token slots filled so far
-      int last_b_par[NA];
-      for (int i = 0; i < NA; ++i) last_b_par[i] = -1;
+      int last_b_par[NB];
+      for (int i = 0; i < NB; ++i) last_b_par[i] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -388,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         const int bi = box_index(tl.nvalid);
         const int rows = 32 << bi, kps = BN / rows;
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
-          const int s2 = sb % NA;
-          const uint32_t ph2 = (sb / NA) & 1;
+          const int s2 = sb % NB;
+          const uint32_t ph2 = (sb / NB) & 1;
           if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
           mbar_expect_tx(&sm->b_full[s2], BN * 128);
           for (int j = 0; j < kps; ++j)
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         }
       }
       const unsigned long long t0 = globaltimer();
-      for (int s = 0; s < NA; ++s)
+      for (int s = 0; s < NB; ++s)
         while (last_b_par[s] >= 0 && !mbar_try_wait(&sm->b_full[s], last_b_par[s]) &&
                globaltimer() - t0 < kWaitNs) {
         }
@@ -424,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         const int rows = 32 << box_index(tl.nvalid), kps = BN / rows;
         for (int k = 0; k < tl.K / BK; ++k) {
           const int j = k % kps;              // K block inside the token slot
-          const int s2 = sb % NA;
+          const int s2 = sb % NB;
           if (j == 0) {
-            if (!(ok = wait_bar(&sm->b_full[s2], (sb / NA) & 1, sm, p.status))) break;
+            if (!(ok = wait_bar(&sm->b_full[s2], (sb / NB) & 1, sm, p.status))) break;
           }
           const int s = ka % NA;
           if (!(ok = wait_bar(&sm->a_full[s], (ka / NA) & 1, sm, p.status))) break;
@@ -504,9 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     }
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------ dequant
-    const int dt = threadIdx.x - kDeqWarp0 * 32;   // 0..255
-    const int half = dt >> 7;                       // K half of a raw stage
-    const int r = dt & 127;                         // tile row
+    // All 256 threads work on each A block in K order: thread -> (row, half
+    // row), with the 8 lanes of a shared-memory phase on 8 consecutive rows of
+    // the same half so the swizzled 16-byte reads and writes hit 8 different
+    // bank groups.
+    const int dt = threadIdx.x - kDeqWarp0 * 32;    // 0..255
+    const int hh = (dt >> 3) & 1;                    // half of the 64-K row
+    const int r = (dt & 7) + 8 * (dt >> 4);          // tile row 0..127
     uint32_t rk = 0, kb = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
@@ -515,28 +523,27 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
-        const float2 sc = *reinterpret_cast<const float2 *>(&sm->sc[s][r * (RK / 64) + half * 2]);
+        const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = half * 2 + jj;                 // A block within the raw stage
+        for (int j = 0; j < RK / BK; ++j) {           // A block j of the raw stage
           const uint32_t kbj = kb + j;
           const int s2 = kbj % NA;
-          // Raw 16-byte chunks 2j, 2j+1 of this row (128-byte swizzle: chunk c at c ^ (r & 7)).
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (r & 7)) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (r & 7)) << 4));
-          const float sv = jj ? sc.y : sc.x;
+          // raw 16-byte chunk 2j + hh of this row (128-byte swizzle: chunk c at c ^ (r & 7))
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + hh) ^ (r & 7)) << 4));
+          const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
           const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
           const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
           const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
           if (!(ok = wait_bar(&sm->a_empty[s2], ((kbj / NA) & 1) ^ 1, sm, p.status))) break;
           uint8_t *arow = sm->a[s2] + r * 128;
-          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
-          for (int wv = 0; wv < 8; ++wv) {   // word wv -> output chunk wv (8 bf16)
+          for (int wv = 0; wv < 4; ++wv) {   // word -> output chunk 4 hh + wv (8 bf16)
             uint32_t o[4];
             dequant_word(words[wv], shi2, slo2, o);
-            *reinterpret_cast<uint4 *>(arow + ((wv ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            const int oc = 4 * hh + wv;
+            *reinterpret_cast<uint4 *>(arow + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
           fence_proxy_async();
           __syncwarp();
