@@ -21,7 +21,8 @@
 //   warp 2      TMA producer of bf16 token tiles (256 rows x 64 K, 128-byte
 //               swizzled); the two producers run independently.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
-//               f32 accumulate) M=128, N=16..256, K=16 by one thread, commits
+//               f32 accumulate) M=128, N=16..256, K=16 by one elected lane
+//               (the warp runs the loop, so operands stay uniform), commits
 //               to mbarriers; two 256-column accumulators in TMEM so the
 //               epilogue of one tile overlaps the main loop of the next.
 //   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
@@ -161,6 +162,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// One lane of a converged warp (elect.sync); the role loops run warp-wide so
+// descriptors, coordinates and barrier addresses stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------ raw weight producer
-    if (lane == 0) {
+    {
       uint32_t rk = 0;
       int last_raw_par[NR];
       for (int i = 0; i < NR; ++i) last_raw_par[i] = -1;
@@ -363,14 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           const int s = rk % NR;
           const uint32_t ph = (rk / NR) & 1;
           if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
-          mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
-          tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
-          tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
+          if (elect_one()) {
+            mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
+            tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
+            tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
+          }
+          __syncwarp();
           last_raw_par[s] = ph;
           ++rk;
         }
       }
-      // Drain: every copy this thread issued has landed before the CTA exits.
+      // Drain: every copy this warp issued has landed before the CTA exits.
       const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NR; ++s)
         while (last_raw_par[s] >= 0 && !mbar_try_wait(&sm->raw_full[s], last_raw_par[s]) &&
@@ -379,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     }
   } else if (warp == 2) {
     // ------------------------------------------------------ token tile producer
-    if (lane == 0) {
+    {
       uint32_t sb = 0;                    // token slots filled so far
       int last_b_par[NB];
       for (int i = 0; i < NB; ++i) last_b_par[i] = -1;
@@ -395,10 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
           if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
-          mbar_expect_tx(&sm->b_full[s2], BN * 128);
-          for (int j = 0; j < kps; ++j)
-            tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, tl.p0,
-                        &sm->b_full[s2]);
+          if (elect_one()) {
+            mbar_expect_tx(&sm->b_full[s2], BN * 128);
+            for (int j = 0; j < kps; ++j)
+              tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, tl.p0,
+                          &sm->b_full[s2]);
+          }
+          __syncwarp();
           last_b_par[s2] = ph2;
           ++sb;
         }
@@ -411,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       uint32_t ka = 0, sb = 0, it = 0;
       int last_acc = -1;
       uint32_t last_acc_par = 0;
@@ -437,19 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           tc_fence_after();
           const uint64_t da = sw128_desc(smem_u32(sm->a[s]));
           const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + j * rows * 128));
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                     (k | kk) ? 1u : 0u);
-          mma_commit(&sm->a_empty[s]);
-          ++ka;
-          if (j == kps - 1) {
-            mma_commit(&sm->b_empty[s2]);
-            ++sb;
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                       (k | kk) ? 1u : 0u);
+            mma_commit(&sm->a_empty[s]);
+            if (j == kps - 1) mma_commit(&sm->b_empty[s2]);
           }
+          __syncwarp();
+          ++ka;
+          if (j == kps - 1) ++sb;
         }
         if (!ok) break;
-        mma_commit(&sm->acc_full[buf]);
+        if (elect_one()) mma_commit(&sm->acc_full[buf]);
+        __syncwarp();
         last_acc = buf;
         last_acc_par = (it >> 1) & 1;
         ++it;
@@ -722,37 +741,38 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) {
-      int last_par[RT_S] = {-1, -1, -1};
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % RT_S;
-        const uint32_t ph = (kb / RT_S) & 1;
-        if (!rt_wait(&sm->empty[s], ph ^ 1, sm, p.status)) break;
+    int last_par[RT_S] = {-1, -1, -1};
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % RT_S;
+      const uint32_t ph = (kb / RT_S) & 1;
+      if (!rt_wait(&sm->empty[s], ph ^ 1, sm, p.status)) break;
+      if (elect_one()) {
         mbar_expect_tx(&sm->full[s], RT_STAGE_TX);
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl)
           tma_load_2d(sm->a[s][pl], &p.map_a, kb * BK, pl * p.E + e0, &sm->full[s]);
         tma_load_2d(sm->b[s], &p.map_x, kb * BK, t0, &sm->full[s]);
-        last_par[s] = ph;
       }
-      const unsigned long long tw = globaltimer();
-      for (int s = 0; s < RT_S; ++s)
-        while (last_par[s] >= 0 && !mbar_try_wait(&sm->full[s], last_par[s]) &&
-               globaltimer() - tw < kWaitNs) {
-        }
+      __syncwarp();
+      last_par[s] = ph;
     }
+    const unsigned long long tw = globaltimer();
+    for (int s = 0; s < RT_S; ++s)
+      while (last_par[s] >= 0 && !mbar_try_wait(&sm->full[s], last_par[s]) &&
+             globaltimer() - tw < kWaitNs) {
+      }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, RT_N);
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % RT_S;
-        if (!(ok = rt_wait(&sm->full[s], (kb / RT_S) & 1, sm, p.status))) break;
-        tc_fence_after();
-        const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
-        const int acc = kb * RT_ACC / nk;                       // accumulator of this k-block
-        const bool first = (kb == 0) || ((kb - 1) * RT_ACC / nk != acc);
-        const uint32_t d = tmem + acc * RT_N;
+    const uint32_t idesc = idesc_bf16(BM, RT_N);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % RT_S;
+      if (!(ok = rt_wait(&sm->full[s], (kb / RT_S) & 1, sm, p.status))) break;
+      tc_fence_after();
+      const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
+      const int acc = kb * RT_ACC / nk;                       // accumulator of this k-block
+      const bool first = (kb == 0) || ((kb - 1) * RT_ACC / nk != acc);
+      const uint32_t d = tmem + acc * RT_N;
+      if (elect_one()) {
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl) {
           const uint64_t da = sw128_desc(smem_u32(sm->a[s][pl]));
@@ -763,11 +783,13 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         }
         mma_commit(&sm->empty[s]);
       }
-      if (ok) {
-        mma_commit(&sm->acc_full);
-        const unsigned long long tw = globaltimer();
-        while (!mbar_try_wait(&sm->acc_full, 0) && globaltimer() - tw < kWaitNs) {
-        }
+      __syncwarp();
+    }
+    if (ok) {
+      if (elect_one()) mma_commit(&sm->acc_full);
+      __syncwarp();
+      const unsigned long long tw = globaltimer();
+      while (!mbar_try_wait(&sm->acc_full, 0) && globaltimer() - tw < kWaitNs) {
       }
     }
   } else if (warp >= 4) {
