@@ -137,10 +137,10 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 
 // Bounded wait: false if the CTA is stopping or the wait timed out (then the
-// status word and the CTA's abort flag are set).
-__device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
-                                      int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// status word and the CTA's abort flag are set).  The first test is inlined;
+// only a wait that has to poll calls the out-of-line loop.
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, SmemTC *sm,
+                                           int32_t *status) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -153,6 +153,11 @@ __device__ __noinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
+                                         int32_t *status) {
+  return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, sm, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -362,8 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     // ------------------------------------------------------ raw weight producer
     {
       uint32_t rk = 0;
-      int last_raw_par[NR];
-      for (int i = 0; i < NR; ++i) last_raw_par[i] = -1;
+      uint32_t armed = 0, par = 0;        // per stage: a copy was issued / its parity
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -380,14 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
             tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
           }
           __syncwarp();
-          last_raw_par[s] = ph;
+          armed |= 1u << s;
+          par = (par & ~(1u << s)) | (ph << s);
           ++rk;
         }
       }
       // Drain: every copy this warp issued has landed before the CTA exits.
       const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NR; ++s)
-        while (last_raw_par[s] >= 0 && !mbar_try_wait(&sm->raw_full[s], last_raw_par[s]) &&
+        while (((armed >> s) & 1) && !mbar_try_wait(&sm->raw_full[s], (par >> s) & 1) &&
                globaltimer() - t0 < kWaitNs) {
         }
     }
@@ -395,8 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     // ------------------------------------------------------ token tile producer
     {
       uint32_t sb = 0;                    // token slots filled so far
-      int last_b_par[NB];
-      for (int i = 0; i < NB; ++i) last_b_par[i] = -1;
+      uint32_t armed = 0, par = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -416,13 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
                           &sm->b_full[s2]);
           }
           __syncwarp();
-          last_b_par[s2] = ph2;
+          armed |= 1u << s2;
+          par = (par & ~(1u << s2)) | (ph2 << s2);
           ++sb;
         }
       }
       const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NB; ++s)
-        while (last_b_par[s] >= 0 && !mbar_try_wait(&sm->b_full[s], last_b_par[s]) &&
+        while (((armed >> s) & 1) && !mbar_try_wait(&sm->b_full[s], (par >> s) & 1) &&
                globaltimer() - t0 < kWaitNs) {
         }
     }
@@ -696,9 +701,8 @@ struct RtParams {
   int32_t *status;
 };
 
-__device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *sm,
-                                        int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool rt_wait_slow(uint64_t *bar, uint32_t parity, SmemRT *sm,
+                                          int32_t *status) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -711,6 +715,11 @@ __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *
       }
     }
   }
+}
+
+__device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *sm,
+                                        int32_t *status) {
+  return mbar_try_wait(bar, parity) || rt_wait_slow(bar, parity, sm, status);
 }
 
 __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant__ RtParams p) {
@@ -741,7 +750,7 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
-    int last_par[RT_S] = {-1, -1, -1};
+    uint32_t armed = 0, par = 0;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % RT_S;
       const uint32_t ph = (kb / RT_S) & 1;
@@ -754,11 +763,12 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         tma_load_2d(sm->b[s], &p.map_x, kb * BK, t0, &sm->full[s]);
       }
       __syncwarp();
-      last_par[s] = ph;
+      armed |= 1u << s;
+      par = (par & ~(1u << s)) | (ph << s);
     }
     const unsigned long long tw = globaltimer();
     for (int s = 0; s < RT_S; ++s)
-      while (last_par[s] >= 0 && !mbar_try_wait(&sm->full[s], last_par[s]) &&
+      while (((armed >> s) & 1) && !mbar_try_wait(&sm->full[s], (par >> s) & 1) &&
              globaltimer() - tw < kWaitNs) {
       }
   } else if (warp == 1) {
