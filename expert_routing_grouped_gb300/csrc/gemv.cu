@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
   const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
   const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
   int staged_e = -1, staged_b = -1;
+  const int sw = lane & 7;             // swizzle of every chunk this lane reads
 
   // Rows of this warp inside an item: W13 -> W1 of features 2w, 2w+1 and W3 of
   // the same (rows 2w, 2w+1, 16+2w, 17+2w of the 32-row group); W2 -> 4w..4w+3.
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           const float4 *xp = reinterpret_cast<const float4 *>(act_s + (size_t)t * K + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 f = xp[j ^ (c & 7)];
+            const float4 f = xp[j ^ sw];   // c & 7 == lane & 7
             xa[t][2 * j] = make_float2(f.x, f.y);
             xa[t][2 * j + 1] = make_float2(f.z, f.w);
           }

@@ -97,6 +97,7 @@ void carve(moe_handle *h, Carver &c) {
   w.tiles = c.take<int32_t>(A / moe::kTileTokens + E + maxT / moe::kTileTokens + 2);
   w.n_tiles = c.take<int32_t>(2);
   w.status = c.take<int32_t>(1);
+  w.ticket = c.take<int32_t>(1);
   w.h = c.take<float>(rows * Imax);
   w.hb = c.take<__nv_bfloat16>(rows * Imax);
   w.y = c.take<float>(rows * H);
@@ -208,14 +209,22 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
                 cudaStream_t st) {
   int regime = choose_regime(h, T);
   h->n_ev = 0;
-  cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
+  cudaError_t err = cudaSuccess;
   mark(h, nullptr, st);
-  if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
-  h->launches += 2;
-  mark(h, "router", st);
-  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
-  h->launches += 1;
-  mark(h, "dispatch", st);
+  if (T <= moe::kGemvTokens) {
+    // One launch routes and groups (and clears the status word).
+    err = moe::launch_route_small(h, x, T, st);
+    h->launches += 1;
+    mark(h, "route", st);
+  } else {
+    err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
+    if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
+    h->launches += 2;
+    mark(h, "router", st);
+    if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
+    h->launches += 1;
+    mark(h, "dispatch", st);
+  }
   if (err == cudaSuccess) {
     if (regime == 1) {
       err = moe::launch_gemv_w13(h, x, T, st);
@@ -288,7 +297,9 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   Carver c{static_cast<char *>(h->pool)};
   carve(h, c);
   rc = copy_weights(h, weights);
-  if (rc == MOE_OK && cudaMemset(h->ws.status, 0, 4) != cudaSuccess) rc = MOE_ERR_DEVICE;
+  if (rc == MOE_OK && (cudaMemset(h->ws.status, 0, 4) != cudaSuccess ||
+                       cudaMemset(h->ws.ticket, 0, 4) != cudaSuccess))
+    rc = MOE_ERR_DEVICE;
   if (rc != MOE_OK) {
     cudaFree(h->pool);
     delete h;

@@ -48,6 +48,7 @@ struct Workspace {
   int32_t *tiles;     // [max_tiles] packed (expert, m-tile) for the tensor-core path
   int32_t *n_tiles;   // [2] tile count for W13 and W2 kernels
   int32_t *status;    // [1]
+  int32_t *ticket;    // [1] last-CTA-done counter of the fused small-T routing (self-resetting)
   // expert activations
   float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
   __nv_bfloat16 *hb;  // [max_tokens*k + S*max_tokens][I_max] bf16 (tensor-core path)
@@ -93,6 +94,8 @@ namespace moe {
 
 // router.cu
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t s);
+// T <= 4: router, top-k and dispatch in one launch (also clears the status word)
+cudaError_t launch_route_small(const moe_handle *h, const void *x, int T, cudaStream_t s);
 // dispatch.cu
 cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t s);
 // gemv.cu

@@ -122,20 +122,20 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Top-k per token: one warp per token, expert e lives in lane e % 32, slot e / 32.
+// Top-k of one token by one warp; expert e lives in lane e % 32, slot e / 32.
 // Keys: softmax mode, l = z + b; sigmoid mode, s = sigmoid(z), key = s + b.
 // k rounds of a warp argmax (larger key first, lower id on ties) give the
 // slots in descending key order.  Weights are renormalised over the selection
 // and times rsf: softmax w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); sigmoid
-// w_j = s_j / sum_i s_i.
+// w_j = s_j / sum_i s_i.  Split partial logits are summed in split order;
+// `coherent` reads them through L2 (written by other CTAs of the same kernel).
 template <int EPL>
-__global__ void __launch_bounds__(256) router_topk_kernel(
-    const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k,
-    int mode, const float *__restrict__ bias, float rsf, int32_t *__restrict__ idx_out,
-    float *__restrict__ w_out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
+__device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int splits,
+                                           int zstride, int t, int E, int k, int mode,
+                                           const float *__restrict__ bias, float rsf,
+                                           int32_t *__restrict__ idx_out,
+                                           float *__restrict__ w_out, bool coherent) {
+  const int lane = threadIdx.x & 31;
   float key[EPL], val[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -146,8 +146,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
       // Issue all split loads before summing (in split order).
       float part[kRouterSplitMax];
 #pragma unroll
-      for (int s = 0; s < kRouterSplitMax; ++s)
-        part[s] = (s < splits) ? z_part[((size_t)s * zstride + t) * E + e] : 0.f;
+      for (int s = 0; s < kRouterSplitMax; ++s) {
+        const float *src = z_part + ((size_t)s * zstride + t) * E + e;
+        part[s] = (s < splits) ? (coherent ? __ldcg(src) : *src) : 0.f;
+      }
       float zz = 0.f;
 #pragma unroll
       for (int s = 0; s < kRouterSplitMax; ++s)
@@ -213,6 +215,162 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   }
 }
 
+template <int EPL>
+__global__ void __launch_bounds__(256) router_topk_kernel(
+    const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k, int mode,
+    const float *__restrict__ bias, float rsf, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_token<EPL>(z_part, splits, zstride, t, E, k, mode, bias, rsf, idx_out, w_out, false);
+}
+
+// ---------------------------------------------------------------------------
+// T <= 4 in one launch: the split-K router GEMV of router_gemv_kernel, then the
+// last CTA to finish (an atomic ticket, reset by that CTA for the next call;
+// nothing waits) reads every partial through L2, takes the top-k of each token
+// and groups the T*k <= 128 assignments by expert with the same stable
+// counting sort as dispatch.cu.  Also clears the status word first.
+template <int EPL>
+__global__ void __launch_bounds__(256) route_small_kernel(
+    const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, int mode,
+    const float *__restrict__ wr_t, const float *__restrict__ bias, float rsf, int h_per_split,
+    float *__restrict__ z_part, int32_t *__restrict__ ticket, int n_shared,
+    int32_t *__restrict__ idx, float *__restrict__ w, int32_t *__restrict__ counts,
+    int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+    int32_t *__restrict__ active, int32_t *__restrict__ n_active, int32_t *__restrict__ tiles,
+    int32_t *__restrict__ n_tiles, int32_t *__restrict__ status) {
+  extern __shared__ float xs[];   // [4][h_per_split]
+  __shared__ int last;
+  const int split = blockIdx.y;
+  const int h0 = split * h_per_split;
+  for (int i = threadIdx.x; i < 4 * h_per_split; i += blockDim.x) {
+    const int t = i / h_per_split, hh = i - t * h_per_split;
+    xs[i] = (t < T) ? load_x(x, x_is_bf16, (size_t)t * H + h0 + hh) : 0.f;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e < E) {
+    const float *wrow = wr_t + (size_t)e * H + h0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int hh = lane * 4; hh < h_per_split; hh += 128) {
+      const float4 wv = __ldg(reinterpret_cast<const float4 *>(wrow + hh));
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float4 xv = *reinterpret_cast<const float4 *>(xs + t * h_per_split + hh);
+        acc[t] = fmaf(xv.x, wv.x, acc[t]);
+        acc[t] = fmaf(xv.y, wv.y, acc[t]);
+        acc[t] = fmaf(xv.z, wv.z, acc[t]);
+        acc[t] = fmaf(xv.w, wv.w, acc[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (t < T) z_part[((size_t)split * kGemvTokens + t) * E + e] = acc[t];
+    }
+  }
+  // Last-CTA-done: publish the partials, take a ticket.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int n = gridDim.x * gridDim.y;
+    last = (atomicAdd(ticket, 1) == n - 1);
+    if (last) *ticket = 0;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *status = kStatusOk;
+  // Top-k: warp t handles token t.
+  if (warp < T)
+    topk_token<EPL>(z_part, gridDim.y, kGemvTokens, warp, E, k, mode, bias, rsf, idx, w, true);
+  __syncthreads();
+  // Stable counting sort of the A = T*k assignments (A <= 128, E <= 1024).
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int base[kMaxExperts];
+  __shared__ int wsum[8];
+  const int A = T * k;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int a = threadIdx.x; a < A; a += blockDim.x) {
+    const int ea = __ldcg(idx + a);
+    if (ea >= 0 && ea < E) atomicAdd(&cnt[ea], 1);
+    else atomicExch(status, kStatusBadExpert);
+  }
+  __syncthreads();
+  // Exclusive scan of cnt over E: each thread owns a contiguous run of experts.
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per;
+  int run = 0;
+  for (int i = 0; i < per; ++i)
+    if (e0 + i < E) run += cnt[e0 + i];
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int i = 0; i < warp; ++i) wbase += wsum[i];
+  int pos = wbase + incl - run;
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee < E) {
+      counts[ee] = cnt[ee];
+      offsets[ee] = pos;
+      base[ee] = pos;
+      pos += cnt[ee];
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) offsets[E] = pos;
+  __syncthreads();
+  // Scatter in ascending assignment order (warp 0, 32 assignments at a time).
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < A; c0 += 32) {
+      const int a = c0 + lane;
+      int ea = (a < A) ? __ldcg(idx + a) : E;
+      if (ea < 0 || ea >= E) ea = E;
+      const unsigned peers = __match_any_sync(0xffffffffu, ea);
+      const int rank = __popc(peers & lt);
+      if (ea < E) {
+        const int p = base[ea] + rank;
+        perm[p] = a;
+        inv[a] = p;
+      }
+      __syncwarp();
+      if (ea < E && (peers & lt) == 0) base[ea] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  // Active experts (ascending, shared expert last) and one token block each.
+  if (threadIdx.x == 0) {
+    int na = 0;
+    for (int ee = 0; ee < E; ++ee)
+      if (cnt[ee] > 0) {
+        active[na] = ee;
+        tiles[na] = ee << 16;
+        ++na;
+      }
+    int nt = na;
+    if (n_shared) {
+      active[na++] = E;
+      tiles[nt++] = E << 16;
+    }
+    *n_active = na;
+    n_tiles[0] = nt;
+  }
+}
+
 int router_splits(int T, int E, int H, int num_sms) {
   if (T > 4) return 1;
   const int blocks_e = (E + 7) / 8;
@@ -223,6 +381,37 @@ int router_splits(int T, int E, int H, int num_sms) {
 }
 
 }  // namespace
+
+cudaError_t launch_route_small(const moe_handle *h, const void *x, int T, cudaStream_t st) {
+  const int E = h->E, H = h->H, k = h->k;
+  const int splits = router_splits(T, E, H, h->num_sms);
+  const int hps = H / splits;
+  const size_t smem = (size_t)4 * hps * sizeof(float);
+  const int epl = (E + 31) / 32;
+  const dim3 grid((E + 7) / 8, splits);
+  const moe::Workspace &w = h->ws;
+#define MOE_RS(N)                                                                               \
+  do {                                                                                          \
+    if (smem > 48 * 1024) {                                                                     \
+      cudaError_t err = cudaFuncSetAttribute(route_small_kernel<N>,                             \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,       \
+                                             (int)smem);                                        \
+      if (err != cudaSuccess) return err;                                                       \
+    }                                                                                           \
+    route_small_kernel<N><<<grid, 256, smem, st>>>(                                             \
+        x, h->L.x_dtype == 1, T, H, E, k, h->L.router_mode, h->wr_t, h->bias,                   \
+        h->L.routed_scaling_factor, hps, w.z_part, w.ticket, h->S, w.idx, w.w, w.counts,        \
+        w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status);          \
+  } while (0)
+  if (epl <= 1) MOE_RS(1);
+  else if (epl <= 2) MOE_RS(2);
+  else if (epl <= 4) MOE_RS(4);
+  else if (epl <= 8) MOE_RS(8);
+  else if (epl <= 16) MOE_RS(16);
+  else MOE_RS(32);
+#undef MOE_RS
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t st) {
   const int E = h->E, H = h->H, k = h->k;

@@ -227,8 +227,9 @@ int moe_route_noalloc(const void *x, int T, int hidden, int num_experts, int top
 int moe_debug_read(moe_handle *h, int field, void *host_dst, size_t bytes);
 
 /* Stage times of the last forward with MOE_OPT_PROFILE on (synchronises).
- * Small-T path: router, dispatch, w13, w2, combine.  Tensor-core path: router,
- * dispatch, gather, w13, w2, combine.  Writes up to `max` values in ms and the
+ * T <= 4: route (router, top-k and dispatch in one kernel), then w13, w2,
+ * combine (small-T path) or gather, w13, w2, combine (tensor-core path).
+ * T > 4: router, dispatch, then the same expert stages.  Writes up to `max` values in ms and the
  * stage count to *n; names[i] (optional) receives static strings. */
 int moe_stage_times(moe_handle *h, float *ms, const char **names, int max, int *n);
 
