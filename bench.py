@@ -50,23 +50,84 @@ def peaks():
 # --------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi sampling during the timed region."""
+    """SM clock and clock-event reasons sampled during the timed region.
 
+    Polls NVML (libnvidia-ml, read-only queries) from a thread every ~2 ms, so
+    that a timed region of a few milliseconds still gets samples; falls back to
+    `nvidia-smi -lms` when NVML cannot be loaded.  The device is found by the
+    UUID the CUDA runtime reports, so CUDA_VISIBLE_DEVICES remapping is safe."""
+
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, dev):
+        self.dev = dev
+        self.samples = []          # (sm_mhz, reason_mask)
+        self.max_mhz = None
         self.proc = None
         self.lines = []
+        self.stop = threading.Event()
+        self.nvml = None
+        self.source = "none"
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = self.dev.index or 0
+            ids = [v for v in vis.split(",") if v.strip()]
+            if ids and all(v.strip().isdigit() for v in ids):
+                idx = int(ids[idx])
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                return None, None
+        return lib, h
+
+    def _poll(self, lib, h):
+        import ctypes
+        clk = ctypes.c_uint()
+        mask = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:   # NVML_CLOCK_SM
+                m = mask.value if get_reasons(h, ctypes.byref(mask)) == 0 else 0
+                self.samples.append((float(clk.value), m))
+            time.sleep(0.002)
 
     def __enter__(self):
         try:
+            import ctypes
+            lib, h = self._nvml_handle()
+            if lib is not None:
+                mx = ctypes.c_uint()
+                if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                    self.max_mhz = float(mx.value)
+                self.source = "nvml"
+                self.t = threading.Thread(target=self._poll, args=(lib, h), daemon=True)
+                self.t.start()
+                return self
+        except OSError:
+            pass
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", "-i", str(self.dev.index or 0), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -78,6 +139,9 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.source == "nvml":
+            self.t.join(timeout=1)
         if self.proc:
             self.proc.terminate()
             try:
@@ -86,7 +150,12 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons = [], self.max_mhz, set()
+        for mhz, m in self.samples:
+            sm.append(mhz)
+            for bit, n in self.REASONS.items():
+                if m & bit:
+                    reasons.add(n)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -101,7 +170,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 # ------------------------------------------------------------- helpers --
@@ -157,7 +226,7 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     torch.cuda.synchronize()
-    with ClockSampler(dev.index or 0) as clk:
+    with ClockSampler(dev) as clk:
         t0 = time.perf_counter()
         for i in range(steps):
             evs[i][0].record(stream)
@@ -247,7 +316,7 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     cur = torch.cuda.current_stream()
-    with ClockSampler(dev.index or 0) as clk:
+    with ClockSampler(dev) as clk:
         for i in range(steps):
             evs[i][0].record(cur)
             g.replay()

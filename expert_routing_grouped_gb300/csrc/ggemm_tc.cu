@@ -18,17 +18,23 @@
 // Per CTA (one per SM, 16 warps):
 //   warp 0      TMA producer of raw int4 weight tiles (128 rows x 256 K, 128-byte
 //               swizzled) and their gs64 scales, 4 stages deep;
-//   warp 2      TMA producer of bf16 token tiles (256 rows x 64 K, 128-byte
-//               swizzled); the two producers run independently.
+//   warp 2      TMA producer of bf16 token tiles (up to 128 rows x 64 K, 128-byte
+//               swizzled, several K blocks per 32 KB slot for small tiles); the
+//               two producers run independently.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
-//               f32 accumulate) M=128, N=16..256, K=16 by one elected lane
+//               f32 accumulate) M=128, N=16..128, K=16 by one elected lane
 //               (the warp runs the loop, so operands stay uniform), commits
-//               to mbarriers; two 256-column accumulators in TMEM so the
-//               epilogue of one tile overlaps the main loop of the next.
+//               to mbarriers.  A is read from TMEM, B from shared memory.
 //   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
-//   warps 8-15  dequant: raw int4 -> bf16(q * s) into the UMMA operand layout
-//               (K-major, 128-byte swizzle); all 8 warps on each 64-K block in
-//               order, half a row per thread.
+//   warps 8-15  dequant: raw int4 -> bf16(q * s), written straight into TMEM
+//               as the MMA's A operand with tcgen05.st (a warp owns one lane
+//               quadrant and half of each 64-K block: one row, 32 K per thread).
+// TMEM (512 columns): two 128-column accumulators, so the epilogue of one tile
+// overlaps the main loop of the next, and two 128-column A groups (4 K blocks
+// of 64 each), so the dequant of one raw stage overlaps the MMAs of the last.
+// Keeping A out of shared memory leaves shared-memory bandwidth to the token
+// operand: per 64-K block the MMA reads N x 128 bytes of tokens that TMA wrote,
+// and nothing else but the 4.5 KB raw stage passes through it.
 // Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
 // the device status word, flags the CTA to stop, and the kernel drains its
 // outstanding copies and MMAs (bounded), frees TMEM and returns.
@@ -42,35 +48,39 @@ namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
-constexpr int BK = 64;           // K per bf16 stage (128 bytes of a row)
-constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
-constexpr int NA = 4;            // bf16 A stages (dequantised weights)
-constexpr int NB = 3;            // token slots
-constexpr int NR = 3;            // raw stages
+constexpr int BK = 64;           // K per bf16 block (128 bytes of a row)
+constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row) = one A group
+constexpr int KPG = RK / BK;     // K blocks per A group (4)
+constexpr int NG = 2;            // A groups in TMEM
+constexpr int NB = 4;            // token slots
+constexpr int NR = 4;            // raw stages
+constexpr int kSlotRows = 256;   // rows of 128 bytes per token slot (32 KB)
+constexpr uint32_t kACol0 = 2 * BN;          // first TMEM column of the A groups
+constexpr uint32_t kGroupCols = KPG * BK / 2;  // 128 columns: 2 bf16 per column
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
-constexpr int kDeqThreads = 256;
+constexpr int kDeqWarps = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
+static_assert(kACol0 + NG * kGroupCols <= 512, "TMEM columns");
 
 struct __align__(1024) SmemTC {
-  uint8_t raw[NR][BM * 128];     // 3 x 16 KB
-  uint8_t a[NA][BM * 128];       // 4 x 16 KB
-  uint8_t b[NB][BN * 128];       // 3 x 32 KB
-  float sc[NR][BM * (RK / 64)];  // 3 x 2 KB: the raw stage's gs64 scales, [row][4]
+  uint8_t raw[NR][BM * 128];     // 4 x 16 KB
+  uint8_t b[NB][kSlotRows * 128];  // 4 x 32 KB
+  float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
-  uint64_t a_full[NA], a_empty[NA];
+  uint64_t a_full[NG], a_empty[NG];
   uint64_t b_full[NB], b_empty[NB];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
 
-// Token slots hold 32 KB: 256 rows of one 64-K block, or several K blocks of
-// a smaller box (8 blocks of 32 rows, ...), so small tiles keep as many K
+// Token slots hold 32 KB: two 64-K blocks of a 128-row box, or more K blocks
+// of a smaller box (8 blocks of 32 rows, ...), so small tiles keep as many K
 // blocks in flight as large ones keep bytes.
 __device__ __forceinline__ int box_index(int nvalid) {
-  return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 128 ? 2 : 3;
+  return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : 2;
 }
 
 struct TcParams {
@@ -78,9 +88,7 @@ struct TcParams {
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
   CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
-  CUtensorMap map_b[4];    // bf16 token operand [R][K], boxes of 32/64/128/256 rows
-  const float *scale;      // routed scales [E * rows][K/64]
-  const float *scale_s;    // shared scales [rows_s][K/64]
+  CUtensorMap map_b[3];    // bf16 token operand [R][K], boxes of 32/64/128 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
   int K;                   // reduction length (H for W13, I for W2)
   int K_s;                 // the shared expert's reduction length (H, or Is for W2)
@@ -179,9 +187,6 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -218,6 +223,34 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T: A in tensor memory, 128 lanes = 128 rows,
+// two bf16 per 32-bit column in K order.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Thread i of the warp writes 16 consecutive 32-bit columns of TMEM lane
+// (quadrant base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -335,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < NR; ++i) {
       mbar_init(&sm->raw_full[i], 1);
-      mbar_init(&sm->raw_empty[i], kDeqThreads / 32);
+      mbar_init(&sm->raw_empty[i], kDeqWarps);
     }
-    for (int i = 0; i < NA; ++i) {
-      mbar_init(&sm->a_full[i], kDeqThreads / 32);
+    for (int i = 0; i < NG; ++i) {
+      mbar_init(&sm->a_full[i], kDeqWarps);
       mbar_init(&sm->a_empty[i], 1);
     }
     for (int i = 0; i < NB; ++i) {
@@ -408,13 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         // Smallest box covering the tile's tokens; one slot carries 256 / rows
         // K blocks of it (K / 64 is a multiple of 8).
         const int bi = box_index(tl.nvalid);
-        const int rows = 32 << bi, kps = BN / rows;
+        const int rows = 32 << bi, kps = kSlotRows / rows;
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
           if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
           if (elect_one()) {
-            mbar_expect_tx(&sm->b_full[s2], BN * 128);
+            mbar_expect_tx(&sm->b_full[s2], kSlotRows * 128);
             for (int j = 0; j < kps; ++j)
               tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, tl.p0,
                           &sm->b_full[s2]);
@@ -434,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     {
-      uint32_t ka = 0, sb = 0, it = 0;
+      uint32_t ag = 0, sb = 0, it = 0;
       int last_acc = -1;
       uint32_t last_acc_par = 0;
       bool ok = true;
@@ -447,29 +480,35 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         const int n_mma = (tl.nvalid + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
         const uint32_t d = tmem + buf * BN;
-        const int rows = 32 << box_index(tl.nvalid), kps = BN / rows;
-        for (int k = 0; k < tl.K / BK; ++k) {
-          const int j = k % kps;              // K block inside the token slot
-          const int s2 = sb % NB;
-          if (j == 0) {
-            if (!(ok = wait_bar(&sm->b_full[s2], (sb / NB) & 1, sm, p.status))) break;
-          }
-          const int s = ka % NA;
-          if (!(ok = wait_bar(&sm->a_full[s], (ka / NA) & 1, sm, p.status))) break;
+        const int rows = 32 << box_index(tl.nvalid), kps = kSlotRows / rows;
+        for (int g0 = 0; ok && g0 < tl.K / BK; g0 += KPG) {
+          const int ga = ag % NG;
+          if (!(ok = wait_bar(&sm->a_full[ga], (ag / NG) & 1, sm, p.status))) break;
           tc_fence_after();
-          const uint64_t da = sw128_desc(smem_u32(sm->a[s]));
-          const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + j * rows * 128));
-          if (elect_one()) {
+          const uint32_t acol = tmem + kACol0 + ga * kGroupCols;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                       (k | kk) ? 1u : 0u);
-            mma_commit(&sm->a_empty[s]);
-            if (j == kps - 1) mma_commit(&sm->b_empty[s2]);
+          for (int j = 0; j < KPG; ++j) {
+            const int k = g0 + j;
+            const int jj = k % kps;              // K block inside the token slot
+            const int s2 = sb % NB;
+            if (jj == 0) {
+              if (!(ok = wait_bar(&sm->b_full[s2], (sb / NB) & 1, sm, p.status))) break;
+            }
+            const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + jj * rows * 128));
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                mma_bf16_ta(d, acol + j * (BK / 2) + kk * 8, db + (uint64_t)(kk * 2), idesc,
+                            (k | kk) ? 1u : 0u);
+              if (jj == kps - 1) mma_commit(&sm->b_empty[s2]);
+            }
+            __syncwarp();
+            if (jj == kps - 1) ++sb;
           }
+          if (!ok) break;
+          if (elect_one()) mma_commit(&sm->a_empty[ga]);
           __syncwarp();
-          ++ka;
-          if (j == kps - 1) ++sb;
+          ++ag;
         }
         if (!ok) break;
         if (elect_one()) mma_commit(&sm->acc_full[buf]);
@@ -532,14 +571,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     }
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------ dequant
-    // All 256 threads work on each A block in K order: thread -> (row, half
-    // row), with the 8 lanes of a shared-memory phase on 8 consecutive rows of
-    // the same half so the swizzled 16-byte reads and writes hit 8 different
-    // bank groups.
-    const int dt = threadIdx.x - kDeqWarp0 * 32;    // 0..255
-    const int hh = (dt >> 3) & 1;                    // half of the 64-K row
-    const int r = (dt & 7) + 8 * (dt >> 4);          // tile row 0..127
-    uint32_t rk = 0, kb = 0;
+    // Warp w owns TMEM lane quadrant w % 4 (tile rows 32 (w % 4) .. +31, one
+    // per lane) and half (w - 8) / 4 of every 64-K block: per raw stage a
+    // thread turns 4 x 32 weights of its row into 4 x 16 bf16x2 columns of the
+    // stage's A group.  The 32 lanes read 32 consecutive rows of the swizzled
+    // raw tile, 8 distinct 16-byte bank groups per 8 lanes.
+    const int dw = warp - kDeqWarp0;
+    const int qd = dw & 3, hh = dw >> 2;
+    const int r = qd * 32 + lane;                    // tile row 0..127
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    uint32_t rk = 0, ag = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       Tile tl;
@@ -549,35 +590,34 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
         const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
+        uint4 c[KPG];
 #pragma unroll
-        for (int j = 0; j < RK / BK; ++j) {           // A block j of the raw stage
-          const uint32_t kbj = kb + j;
-          const int s2 = kbj % NA;
-          // raw 16-byte chunk 2j + hh of this row (128-byte swizzle: chunk c at c ^ (r & 7))
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + hh) ^ (r & 7)) << 4));
+        for (int j = 0; j < KPG; ++j)   // raw 16-byte chunk 2j + hh (128-byte swizzle)
+          c[j] = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + hh) ^ (r & 7)) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->raw_empty[s]);
+        const int ga = ag % NG;
+        if (!(ok = wait_bar(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p.status))) break;
+        tc_fence_after();
+        const uint32_t acol = tmem + lane_base + kACol0 + ga * kGroupCols + hh * 16;
+#pragma unroll
+        for (int j = 0; j < KPG; ++j) {
           const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
           const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
           const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
           const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
-          if (!(ok = wait_bar(&sm->a_empty[s2], ((kbj / NA) & 1) ^ 1, sm, p.status))) break;
-          uint8_t *arow = sm->a[s2] + r * 128;
-          const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
+          const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+          uint32_t o[16];
 #pragma unroll
-          for (int wv = 0; wv < 4; ++wv) {   // word -> output chunk 4 hh + wv (8 bf16)
-            uint32_t o[4];
-            dequant_word(words[wv], shi2, slo2, o);
-            const int oc = 4 * hh + wv;
-            *reinterpret_cast<uint4 *>(arow + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->a_full[s2]);
+          for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o + 4 * wv);
+          tmem_st16(acol + j * (BK / 2), o);
         }
-        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->raw_empty[s]);
+        if (lane == 0) mbar_arrive(&sm->a_full[ga]);
         ++rk;
-        kb += RK / BK;
+        ++ag;
       }
     }
   }
@@ -963,15 +1003,13 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     ok = ok && make_map(&p.map_b[i], w.xp, BF, 2, H, (uint64_t)maxR, H, BK, 32u << i);
   ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
                       RK / 64, BM, false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
                       (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
-  p.scale = h->ex.w13s;
-  p.scale_s = S ? h->sh.w13s : h->ex.w13s;
   p.mode = 0;
   p.K = H;
   p.K_s = H;
@@ -1000,7 +1038,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     ok = ok && make_map(&p.map_b[i], w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK,
                         32u << i);
   ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
@@ -1008,8 +1046,6 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
                       RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
-  p.scale = h->ex.w2s;
-  p.scale_s = S ? h->sh.w2s : h->ex.w2s;
   p.mode = 1;
   p.K = I;
   p.K_s = Is;

@@ -14,7 +14,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
-constexpr int kTileTokens = 256;      // tokens per tensor-core tile (the MMA's N)
+constexpr int kTileTokens = 128;      // tokens per tensor-core tile (the MMA's N)
 
 // Device status word codes (sticky until the next forward overwrites them).
 enum Status : int32_t {
