@@ -49,12 +49,19 @@ namespace {
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
 constexpr int BK = 64;           // K per bf16 block (128 bytes of a row)
-constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row) = one A group
-constexpr int KPG = RK / BK;     // K blocks per A group (4)
-constexpr int NG = 2;            // A groups in TMEM
+constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
+#ifndef MOE_TC_KPG
+#define MOE_TC_KPG 4
+#endif
+constexpr int KPG = MOE_TC_KPG;  // K blocks per A group (TMEM handoff unit)
+constexpr int GPS = RK / BK / KPG;  // A groups per raw stage
+constexpr int NG = 8 / KPG;      // A groups in TMEM (256 columns in all)
 constexpr int NB = 4;            // token slots
 constexpr int NR = 4;            // raw stages
 constexpr int kSlotRows = 256;   // rows of 128 bytes per token slot (32 KB)
+constexpr int NSL = 16;          // exact mode: per-group accumulator slices
+constexpr int kSliceCols = 16;   // exact mode: columns per slice (MMA N)
+constexpr int NSE = 8;           // exact mode: scale stages read by the epilogue
 constexpr uint32_t kACol0 = 2 * BN;          // first TMEM column of the A groups
 constexpr uint32_t kGroupCols = KPG * BK / 2;  // 128 columns: 2 bf16 per column
 constexpr int kThreads = 512;
@@ -63,15 +70,18 @@ constexpr int kDeqWarp0 = 8;
 constexpr int kDeqWarps = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 static_assert(kACol0 + NG * kGroupCols <= 512, "TMEM columns");
+static_assert(NSL * kSliceCols <= (int)kACol0, "TMEM columns (exact mode)");
 
 struct __align__(1024) SmemTC {
   uint8_t raw[NR][BM * 128];     // 4 x 16 KB
   uint8_t b[NB][kSlotRows * 128];  // 4 x 32 KB
   float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
+  float sce[NSE][BM * (RK / 64)];  // exact mode: the same scales, for the epilogue
   uint64_t raw_full[NR], raw_empty[NR];
+  uint64_t sce_full[NSE], sce_empty[NSE];
   uint64_t a_full[NG], a_empty[NG];
   uint64_t b_full[NB], b_empty[NB];
-  uint64_t acc_full[2], acc_empty[2];
+  uint64_t acc_full[NSL], acc_empty[NSL];
   uint32_t tmem_base;
   int abort;
 };
@@ -90,6 +100,7 @@ struct TcParams {
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
   CUtensorMap map_b[3];    // bf16 token operand [R][K], boxes of 32/64/128 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
+  int planes;              // operand rows per token (exact mode: 2 for hi/lo planes)
   int K;                   // reduction length (H for W13, I for W2)
   int K_s;                 // the shared expert's reduction length (H, or Is for W2)
   int rows;                // weight rows per routed expert (2I or H)
@@ -98,7 +109,7 @@ struct TcParams {
   const int32_t *blocks;   // token blocks (expert << 16 | block index)
   const int32_t *n_blocks;
   const int32_t *offsets;  // [E+1]
-  __nv_bfloat16 *hb;       // W13 output [R][h_stride]
+  __nv_bfloat16 *hb;       // W13 output [R][h_stride] (exact mode: [2R][h_stride], hi/lo)
   int h_stride;
   float *y;                // W2 output [R][H]
   int H;
@@ -279,6 +290,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ------------------------------------------------------------- dequant --
 
 // bf16x2 arithmetic on raw 32-bit registers.
@@ -315,6 +341,13 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_hi2, uint32_
     const uint32_t q = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
     out[i] = hfma2_bf16(q, s_hi2, hmul2_bf16(q, s_lo2));
   }
+}
+
+// 8 weights of one library-layout word -> 4 bf16x2 words of the exact codes q.
+__device__ __forceinline__ void dequant_word_q(uint32_t w, uint32_t out[4]) {
+  const uint32_t c136 = 0x43084308u;   // bf16x2 (136, 136)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_splat(__nv_bfloat16 v) {
@@ -355,7 +388,16 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
 }
 
 // --------------------------------------------------------------- kernel --
-
+//
+// EXACT = false (prefill): A = bf16(q * s) per weight, one accumulator per
+// tile (up to 128 tokens), bf16 h out of W13.
+// EXACT = true (decode, up to 8 tokens per expert): A = the exact int4 codes q,
+// each 64-K group accumulates into its own 16-column TMEM slice, and the
+// epilogue applies the group's f32 scale: out = sum_g s_g * (q_g . b_g), the
+// same sum as the f32 GEMV.  f32 operands enter as two bf16 planes (hi, lo:
+// two columns per token), so every product is exact and the accumulation is
+// f32; h goes out of W13 as such a plane pair.
+template <bool EXACT>
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   SmemTC *sm = reinterpret_cast<SmemTC *>(
@@ -364,11 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   const int n_blocks = *p.n_blocks;
   const int n_fb = p.rows / BM;
   const int n_tiles = n_blocks * n_fb;
+  constexpr int NACC = EXACT ? NSL : 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NR; ++i) {
       mbar_init(&sm->raw_full[i], 1);
       mbar_init(&sm->raw_empty[i], kDeqWarps);
+    }
+    for (int i = 0; i < NSE; ++i) {
+      mbar_init(&sm->sce_full[i], 1);
+      mbar_init(&sm->sce_empty[i], 4);
     }
     for (int i = 0; i < NG; ++i) {
       mbar_init(&sm->a_full[i], kDeqWarps);
@@ -378,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       mbar_init(&sm->b_full[i], 1);
       mbar_init(&sm->b_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NACC; ++i) {
       mbar_init(&sm->acc_full[i], 1);
       mbar_init(&sm->acc_empty[i], 4);
     }
@@ -401,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     {
       uint32_t rk = 0;
       uint32_t armed = 0, par = 0;        // per stage: a copy was issued / its parity
+      uint32_t armed3 = 0, par3 = 0;      // the same for the epilogue's scale stages
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -412,13 +460,26 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           const uint32_t ph = (rk / NR) & 1;
           if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
           if (elect_one()) {
-            mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
+            mbar_expect_tx(&sm->raw_full[s], BM * 128 + (EXACT ? 0 : BM * (RK / 64) * 4));
             tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
-            tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
+            if (!EXACT) tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
           }
           __syncwarp();
           armed |= 1u << s;
           par = (par & ~(1u << s)) | (ph << s);
+          if (EXACT) {
+            // The scales go to the epilogue, which applies them per group.
+            const int s3 = rk % NSE;
+            const uint32_t ph3 = (rk / NSE) & 1;
+            if (!(ok = wait_bar(&sm->sce_empty[s3], ph3 ^ 1, sm, p.status))) break;
+            if (elect_one()) {
+              mbar_expect_tx(&sm->sce_full[s3], BM * (RK / 64) * 4);
+              tma_load_2d(sm->sce[s3], ms, r * (RK / 64), tl.wrow0, &sm->sce_full[s3]);
+            }
+            __syncwarp();
+            armed3 |= 1u << s3;
+            par3 = (par3 & ~(1u << s3)) | (ph3 << s3);
+          }
           ++rk;
         }
       }
@@ -426,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NR; ++s)
         while (((armed >> s) & 1) && !mbar_try_wait(&sm->raw_full[s], (par >> s) & 1) &&
+               globaltimer() - t0 < kWaitNs) {
+        }
+      for (int s = 0; s < NSE; ++s)
+        while (((armed3 >> s) & 1) && !mbar_try_wait(&sm->sce_full[s], (par3 >> s) & 1) &&
                globaltimer() - t0 < kWaitNs) {
         }
     }
@@ -438,10 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
-        // Smallest box covering the tile's tokens; one slot carries 256 / rows
-        // K blocks of it (K / 64 is a multiple of 8).
-        const int bi = box_index(tl.nvalid);
+        // Smallest box covering the tile's operand rows (planes per token);
+        // one slot carries 256 / rows K blocks of it (K / 64 is a multiple of 8).
+        const int bi = box_index(p.planes * tl.nvalid);
         const int rows = 32 << bi, kps = kSlotRows / rows;
+        const int brow = p.planes * tl.p0;
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
@@ -449,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           if (elect_one()) {
             mbar_expect_tx(&sm->b_full[s2], kSlotRows * 128);
             for (int j = 0; j < kps; ++j)
-              tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, tl.p0,
+              tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, brow,
                           &sm->b_full[s2]);
           }
           __syncwarp();
@@ -467,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     {
-      uint32_t ag = 0, sb = 0, it = 0;
+      uint32_t ag = 0, sb = 0, it = 0, ks = 0;
       int last_acc = -1;
       uint32_t last_acc_par = 0;
       bool ok = true;
@@ -475,12 +541,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
         const int buf = it & 1;
-        if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
-        tc_fence_after();
-        const int n_mma = (tl.nvalid + 15) & ~15;
+        if (!EXACT) {
+          if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
+          tc_fence_after();
+        }
+        const int ncols = p.planes * tl.nvalid;
+        const int n_mma = (ncols + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
-        const uint32_t d = tmem + buf * BN;
-        const int rows = 32 << box_index(tl.nvalid), kps = kSlotRows / rows;
+        const int rows = 32 << box_index(ncols), kps = kSlotRows / rows;
         for (int g0 = 0; ok && g0 < tl.K / BK; g0 += KPG) {
           const int ga = ag % NG;
           if (!(ok = wait_bar(&sm->a_full[ga], (ag / NG) & 1, sm, p.status))) break;
@@ -494,16 +562,30 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
             if (jj == 0) {
               if (!(ok = wait_bar(&sm->b_full[s2], (sb / NB) & 1, sm, p.status))) break;
             }
+            uint32_t d = tmem + buf * BN;
+            int sl = 0;
+            if (EXACT) {
+              sl = ks % NSL;
+              if (!(ok = wait_bar(&sm->acc_empty[sl], ((ks / NSL) & 1) ^ 1, sm, p.status))) break;
+              tc_fence_after();
+              d = tmem + sl * kSliceCols;
+            }
             const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + jj * rows * 128));
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 mma_bf16_ta(d, acol + j * (BK / 2) + kk * 8, db + (uint64_t)(kk * 2), idesc,
-                            (k | kk) ? 1u : 0u);
+                            (EXACT ? kk : (k | kk)) ? 1u : 0u);
               if (jj == kps - 1) mma_commit(&sm->b_empty[s2]);
+              if (EXACT) mma_commit(&sm->acc_full[sl]);
             }
             __syncwarp();
             if (jj == kps - 1) ++sb;
+            if (EXACT) {
+              last_acc = sl;
+              last_acc_par = (ks / NSL) & 1;
+              ++ks;
+            }
           }
           if (!ok) break;
           if (elect_one()) mma_commit(&sm->a_empty[ga]);
@@ -511,10 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           ++ag;
         }
         if (!ok) break;
-        if (elect_one()) mma_commit(&sm->acc_full[buf]);
-        __syncwarp();
-        last_acc = buf;
-        last_acc_par = (it >> 1) & 1;
+        if (!EXACT) {
+          if (elect_one()) mma_commit(&sm->acc_full[buf]);
+          __syncwarp();
+          last_acc = buf;
+          last_acc_par = (it >> 1) & 1;
+        }
         ++it;
       }
       // Drain: the last commit covers every MMA issued before it.
@@ -529,28 +613,103 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     // ------------------------------------------------------ epilogue
     const int q = warp - kEpiWarp0;       // TMEM lane quadrant
     const int row = q * 32 + lane;        // weight row of the tile
-    uint32_t it = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t it = 0, ks = 0, rk = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       Tile tl;
       if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
-      const int buf = it & 1;
-      if (!wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status)) break;
-      tc_fence_after();
       const int fb = (tl.wrow0 - (tl.shared ? 0 : tl.e * p.rows)) / BM;
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
+      if (EXACT) {
+        // acc[c] = sum over groups of s_g(row) * D_g[row][c], c = plane-major
+        // column (token c / planes, plane c % planes).
+        float acc[kSliceCols];
+#pragma unroll
+        for (int c = 0; c < kSliceCols; ++c) acc[c] = 0.f;
+        for (int rr = 0; ok && rr < tl.K / RK; ++rr) {
+          const int s3 = rk % NSE;
+          if (!(ok = wait_bar(&sm->sce_full[s3], (rk / NSE) & 1, sm, p.status))) break;
+          const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sce[s3][row * (RK / 64)]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->sce_empty[s3]);
+          ++rk;
+#pragma unroll
+          for (int j = 0; j < RK / BK; ++j) {
+            const int sl = ks % NSL;
+            if (!(ok = wait_bar(&sm->acc_full[sl], (ks / NSL) & 1, sm, p.status))) break;
+            tc_fence_after();
+            float v[kSliceCols];
+            tmem_ld16(tmem + lane_base + sl * kSliceCols, v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm->acc_empty[sl]);
+            ++ks;
+            const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
+#pragma unroll
+            for (int c = 0; c < kSliceCols; ++c) acc[c] = fmaf(sv, v[c], acc[c]);
+          }
+        }
+        if (!ok) break;
+        if (p.mode == 0) {
+          // lanes 0-15: g of features fb*64 + 16q + lane; lanes 16-31: u of the same.
+          const int feat = fb * 64 + q * 16 + (lane & 15);
+          auto put = [&](int tk, float gsum) {
+            const float u = __shfl_xor_sync(0xffffffffu, gsum, 16);
+            if (lane < 16) {
+              const float hval = gsum / (1.0f + expf(-gsum)) * u;
+              const __nv_bfloat16 hi = __float2bfloat16_rn(hval);
+              const __nv_bfloat16 lo = __float2bfloat16_rn(hval - __bfloat162float(hi));
+              const size_t r2 = 2 * (size_t)(tl.p0 + tk);
+              p.hb[r2 * p.h_stride + feat] = hi;
+              p.hb[(r2 + 1) * p.h_stride + feat] = lo;
+            }
+          };
+          if (p.planes == 2) {
+#pragma unroll
+            for (int tk = 0; tk < kSliceCols / 2; ++tk)
+              if (tk < tl.nvalid) put(tk, acc[2 * tk] + acc[2 * tk + 1]);
+          } else {
+#pragma unroll
+            for (int tk = 0; tk < kSliceCols; ++tk)
+              if (tk < tl.nvalid) put(tk, acc[tk]);
+          }
+        } else {
+          const int o = fb * BM + row;
+#pragma unroll
+          for (int tk = 0; tk < kSliceCols / 2; ++tk) {
+            if (tk < tl.nvalid) {
+              const int pr = tl.p0 + tk;
+              p.y[(size_t)pr * p.H + o] = (acc[2 * tk] + acc[2 * tk + 1]) * p.wperm[pr];
+            }
+          }
+        }
+        continue;
+      }
+      const int buf = it & 1;
+      if (!(ok = wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + lane_base + buf * BN;
       for (int c0 = 0; c0 < tl.nvalid; c0 += 32) {
         float v[32];
         tmem_ld32(tbase + c0, v);
         if (p.mode == 0) {
-          // lanes 0-15: g of features fb*64 + 16q + lane; lanes 16-31: u of the same.
+          // Rows: lanes 0-15 hold g of features fb*64 + 16q + (lane & 15),
+          // lanes 16-31 u of the same.  One exchange per column pair: lanes
+          // 0-15 finish token j (their g, the partner's u), lanes 16-31 token
+          // j + 1 (the partner's g, their u).  h is rounded to bf16, so the
+          // fast exponential and division are well inside its resolution.
           const int feat = fb * 64 + q * 16 + (lane & 15);
+          const bool lo_half = lane < 16;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float u = __shfl_xor_sync(0xffffffffu, v[j], 16);
-            if (lane < 16 && c0 + j < tl.nvalid) {
-              const float g = v[j];
-              const float hval = g / (1.0f + expf(-g)) * u;
-              p.hb[(size_t)(tl.p0 + c0 + j) * p.h_stride + feat] = __float2bfloat16_rn(hval);
+          for (int j = 0; j < 32; j += 2) {
+            const float recv = __shfl_xor_sync(0xffffffffu, lo_half ? v[j + 1] : v[j], 16);
+            const float g = lo_half ? v[j] : recv;
+            const float u = lo_half ? recv : v[j + 1];
+            const int col = c0 + j + (lo_half ? 0 : 1);
+            if (col < tl.nvalid) {
+              const float e = __expf(fminf(-g, 80.0f));
+              const float hval = __fdividef(g, 1.0f + e) * u;
+              p.hb[(size_t)(tl.p0 + col) * p.h_stride + feat] = __float2bfloat16_rn(hval);
             }
           }
         } else {
@@ -588,36 +747,47 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
-        const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
+        float4 sc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!EXACT) sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
-        uint4 c[KPG];
+        uint4 c[RK / BK];
 #pragma unroll
-        for (int j = 0; j < KPG; ++j)   // raw 16-byte chunk 2j + hh (128-byte swizzle)
+        for (int j = 0; j < RK / BK; ++j)   // raw 16-byte chunk 2j + hh (128-byte swizzle)
           c[j] = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + hh) ^ (r & 7)) << 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[s]);
-        const int ga = ag % NG;
-        if (!(ok = wait_bar(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p.status))) break;
-        tc_fence_after();
-        const uint32_t acol = tmem + lane_base + kACol0 + ga * kGroupCols + hh * 16;
 #pragma unroll
-        for (int j = 0; j < KPG; ++j) {
-          const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
-          const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
-          const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
-          const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
-          const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-          uint32_t o[16];
+        for (int gi = 0; gi < GPS; ++gi) {
+          const int ga = ag % NG;
+          if (!(ok = wait_bar(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p.status))) break;
+          tc_fence_after();
+          const uint32_t acol = tmem + lane_base + kACol0 + ga * kGroupCols + hh * 16;
 #pragma unroll
-          for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o + 4 * wv);
-          tmem_st16(acol + j * (BK / 2), o);
+          for (int jj = 0; jj < KPG; ++jj) {
+            const int j = gi * KPG + jj;
+            const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+            uint32_t o[16];
+            if (EXACT) {
+#pragma unroll
+              for (int wv = 0; wv < 4; ++wv) dequant_word_q(words[wv], o + 4 * wv);
+            } else {
+              const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
+              const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
+              const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
+              const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
+#pragma unroll
+              for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o + 4 * wv);
+            }
+            tmem_st16(acol + jj * (BK / 2), o);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->a_full[ga]);
+          ++ag;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->a_full[ga]);
+        if (!ok) break;
         ++rk;
-        ++ag;
       }
     }
   }
@@ -667,6 +837,53 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
         const float4 f = __ldg(src + i);
         dst[2 * i] = __floats2bfloat162_rn(f.x, f.y);
         dst[2 * i + 1] = __floats2bfloat162_rn(f.z, f.w);
+      }
+    }
+  }
+}
+
+// Exact mode: grouped row pr of x as operand planes -- x itself when it is
+// bf16 (planes = 1), else rows 2pr, 2pr+1 = bf16 hi, bf16(x - hi).
+__global__ void __launch_bounds__(256) gather_exact_kernel(const void *__restrict__ x,
+                                                           int x_is_bf16, int T, int H, int k,
+                                                           int n_shared,
+                                                           const int32_t *__restrict__ perm,
+                                                           const float *__restrict__ w,
+                                                           __nv_bfloat16 *__restrict__ xe,
+                                                           float *__restrict__ wperm) {
+  const int A = T * k, R = A + n_shared * T;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int pr = warp; pr < R; pr += nwarps) {
+    int t;
+    float wt;
+    if (pr < A) {
+      const int a = perm[pr];
+      t = a / k;
+      wt = w[a];
+    } else {
+      t = pr - A;
+      wt = 1.0f;
+    }
+    if (lane == 0) wperm[pr] = wt;
+    if (x_is_bf16) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H);
+      uint4 *dst = reinterpret_cast<uint4 *>(xe + (size_t)pr * H);
+      for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+    } else {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          reinterpret_cast<const float *>(x) + (size_t)t * H);
+      __nv_bfloat162 *hi = reinterpret_cast<__nv_bfloat162 *>(xe + (size_t)(2 * pr) * H);
+      __nv_bfloat162 *lo = reinterpret_cast<__nv_bfloat162 *>(xe + (size_t)(2 * pr + 1) * H);
+      for (int i = lane; i < H / 4; i += 32) {
+        const float4 f = __ldg(src + i);
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(f.x, f.y);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(f.z, f.w);
+        hi[2 * i] = h0;
+        hi[2 * i + 1] = h1;
+        lo[2 * i] = __floats2bfloat162_rn(f.x - __low2float(h0), f.y - __high2float(h0));
+        lo[2 * i + 1] = __floats2bfloat162_rn(f.z - __low2float(h1), f.w - __high2float(h1));
       }
     }
   }
@@ -969,6 +1186,118 @@ cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumula
   return cudaGetLastError();
 }
 
+namespace {
+cudaError_t set_tc_attrs() {
+  static bool attr = false;   // per process; the attribute is per function
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(ggemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *out,
+                            bool accumulate, cudaStream_t st) {
+  const moe::Workspace &w = h->ws;
+  const int E = h->E, H = h->H, I = h->I, k = h->k, S = h->S;
+  const int Is = S ? h->Is : I;
+  const int A = T * k;
+  const int rows_x = kExactTokens * (k + S);
+  const int h_stride = I > Is ? I : Is;
+  const int xplanes = h->L.x_dtype == 1 ? 1 : 2;
+  if (T > kExactTokens) return cudaErrorInvalidValue;
+  cudaError_t err = set_tc_attrs();
+  if (err != cudaSuccess) return err;
+  moe_handle *hm = const_cast<moe_handle *>(h);
+  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm, w.w,
+                                                  w.xe, w.wperm);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  hm->launches += 1;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "gather";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  TcParams p{};
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  // ---- W13 over x planes
+  bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
+  ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
+                      (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
+  for (int i = 0; i < 3; ++i)
+    ok = ok && make_map(&p.map_b[i], w.xe, BF, 2, H, (uint64_t)2 * rows_x, H, BK, 32u << i);
+  ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
+                      RK / 64, BM, false);
+  ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
+                      (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
+  if (!ok) return cudaErrorInvalidValue;
+  p.mode = 0;
+  p.planes = xplanes;
+  p.K = H;
+  p.K_s = H;
+  p.rows = 2 * I;
+  p.rows_s = 2 * Is;
+  p.E = E;
+  p.A = A;
+  p.T = T;
+  p.blocks = w.tiles;
+  p.n_blocks = w.n_tiles;
+  p.offsets = w.offsets;
+  p.hb = w.he;
+  p.h_stride = h_stride;
+  p.y = w.y;
+  p.H = H;
+  p.wperm = w.wperm;
+  p.status = w.status;
+  ggemm_kernel<true><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  hm->launches += 1;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "w13";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  // ---- W2 over h planes
+  ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
+  ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
+                      BM);
+  for (int i = 0; i < 3; ++i)
+    ok = ok && make_map(&p.map_b[i], w.he, BF, 2, h_stride, (uint64_t)2 * rows_x, h_stride, BK,
+                        32u << i);
+  ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
+                      false);
+  ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
+                      RK / 64, BM, false);
+  if (!ok) return cudaErrorInvalidValue;
+  p.mode = 1;
+  p.planes = 2;
+  p.K = I;
+  p.K_s = Is;
+  p.rows = H;
+  p.rows_s = H;
+  ggemm_kernel<true><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  hm->launches += 1;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "w2";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  err = launch_combine(h, T, out, accumulate, st);
+  hm->launches += 1;
+  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
+    hm->stage_names[hm->n_ev - 1] = "combine";
+    cudaEventRecord(hm->ev[hm->n_ev++], st);
+  }
+  return err;
+}
+
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
                            cudaStream_t st) {
   const moe::Workspace &w = h->ws;
@@ -977,16 +1306,11 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   const int A = T * k, R = A + S * T;
   const int maxR = h->L.max_tokens * k + S * h->L.max_tokens;
   const int h_stride = I > Is ? I : Is;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  cudaError_t err = set_tc_attrs();
+  if (err != cudaSuccess) return err;
   gather_kernel<<<h->num_sms * 4, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm, w.w,
                                                 w.xp, w.wperm);
-  cudaError_t err = cudaGetLastError();
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   moe_handle *hm = const_cast<moe_handle *>(h);
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
@@ -1011,6 +1335,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
                       (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
   p.mode = 0;
+  p.planes = 1;
   p.K = H;
   p.K_s = H;
   p.rows = 2 * I;
@@ -1027,7 +1352,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.H = H;
   p.wperm = w.wperm;
   p.status = w.status;
-  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  ggemm_kernel<false><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w13";
@@ -1051,7 +1376,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.K_s = Is;
   p.rows = H;
   p.rows_s = H;
-  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  ggemm_kernel<false><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w2";

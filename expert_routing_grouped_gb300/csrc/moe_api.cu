@@ -103,6 +103,9 @@ void carve(moe_handle *h, Carver &c) {
   w.y = c.take<float>(rows * H);
   w.xp = c.take<__nv_bfloat16>(rows * H);
   w.wperm = c.take<float>(rows);
+  const size_t rows_x = (size_t)moe::kExactTokens * (h->k + S);
+  w.xe = c.take<__nv_bfloat16>(2 * rows_x * H);
+  w.he = c.take<__nv_bfloat16>(2 * rows_x * Imax);
   w.x_stage = c.take<char>(maxT * H * h->x_elem);
   w.out_stage = c.take<float>(maxT * H);
 }
@@ -194,6 +197,7 @@ int copy_weights(moe_handle *h, const moe_weights *W) {
 int choose_regime(const moe_handle *h, int T) {
   if (h->regime_opt == 1) return 1;
   if (h->regime_opt == 2) return 2;
+  if (h->regime_opt == 3) return T <= moe::kExactTokens ? 3 : 1;
   if (!moe::tc_path_available()) return 1;
   return T <= h->small_t_max ? 1 : 2;
 }
@@ -236,6 +240,8 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
       if (err == cudaSuccess) err = moe::launch_combine(h, T, out, accumulate, st);
       h->launches += 1;
       mark(h, "combine", st);
+    } else if (regime == 3) {
+      err = moe::launch_tc_exact(h, x, T, out, accumulate, st);
     } else {
       err = moe::launch_tc_path(h, x, T, out, accumulate, st);
     }
@@ -370,7 +376,7 @@ __attribute__((visibility("default"))) int moe_rmsnorm_bf16(const float *x, int 
 __attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int option, int value) {
   if (!h) return MOE_ERR_ARG;
   if (option == MOE_OPT_REGIME) {
-    if (value < 0 || value > 2) return MOE_ERR_ARG;
+    if (value < 0 || value > 3) return MOE_ERR_ARG;
     h->regime_opt = value;
     return MOE_OK;
   }

@@ -15,6 +15,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
 constexpr int kTileTokens = 128;      // tokens per tensor-core tile (the MMA's N)
+constexpr int kExactTokens = 8;       // largest batch of the exact (f32-accumulate) tensor-core mode
 
 // Device status word codes (sticky until the next forward overwrites them).
 enum Status : int32_t {
@@ -55,6 +56,9 @@ struct Workspace {
   float *y;           // [max_tokens*k + S*max_tokens][H] f32 (tensor-core path)
   __nv_bfloat16 *xp;  // [max_tokens*k + S*max_tokens][H] bf16 activations in grouped order
   float *wperm;       // [max_tokens*k + S*max_tokens] routing weight per grouped row (shared 1)
+  // exact tensor-core mode (T <= kExactTokens): operands as bf16 (hi, lo) plane pairs
+  __nv_bfloat16 *xe;  // [2 * kExactTokens*(k+S)][H] grouped x (one plane when x is bf16)
+  __nv_bfloat16 *he;  // [2 * kExactTokens*(k+S)][I_max] h planes
   // host-call staging
   void *x_stage;      // [max_tokens][H] (x dtype)
   float *out_stage;   // [max_tokens][H]
@@ -108,6 +112,8 @@ cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumula
 cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
                                 cudaStream_t s);
 cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t s);
+cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
+                            cudaStream_t st);
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,
                            bool accumulate, cudaStream_t s);
 // misc.cu

@@ -114,7 +114,7 @@ typedef struct moe_debug {
   const int32_t *perm;     /* [T*k] grouped position -> assignment t*k+j        */
   const int32_t *inv;      /* [T*k] assignment -> grouped position              */
   const int32_t *status;   /* one int32 device status word (0 = ok)             */
-  int32_t regime;          /* 1 small-T GEMV path, 2 tensor-core path           */
+  int32_t regime;          /* 1 GEMV path, 2 tensor-core path, 3 exact TC path  */
   int64_t launches;        /* kernels launched by this handle since moe_init    */
 } moe_debug;
 
@@ -165,8 +165,11 @@ int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
 int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                      moe_stream_t stream);
 
-/* Chooses the expert path: 0 automatic (T <= small_t_max -> GEMV path,
- * else tensor cores), 1 always GEMV, 2 always tensor cores. */
+/* Chooses the expert path: 0 automatic (T <= small_t_max -> the small-T
+ * path, else tensor cores), 1 always the SIMT GEMV path, 2 always the
+ * tensor-core path (bf16 weights, bf16 operands), 3 the exact tensor-core
+ * path (T <= 8 only: exact int4 codes, f32 operands as bf16 hi/lo pairs, f32
+ * group scales and accumulation; the small-T path's numerics on tensor cores). */
 #define MOE_OPT_REGIME 1
 /* Largest T that the automatic choice sends to the GEMV path (default 4). */
 #define MOE_OPT_SMALL_T_MAX 2

@@ -94,6 +94,26 @@ def test_gemv_path_parity(dev, name, T):
     assert rel_l2(got, ref["out"]) <= GEMV_TOL
 
 
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 8), ("olmoe", 1), ("olmoe", 3),
+                                    ("mixtral", 1), ("mixtral", 4), ("glm_decode", 1),
+                                    ("glm_decode", 4), ("glm_decode", 8)])
+def test_tc_exact_path_parity(dev, name, T):
+    """The exact tensor-core path (int4 codes, f32 operands as bf16 hi/lo
+    pairs, f32 group scales) holds the GEMV path's tolerance; tiny has f32 x
+    (two operand planes), the others bf16 x."""
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME[name]
+    got, ref, h, xd = run_and_compare(wl, T, dev, regime=moe.REGIME_TC_EXACT)
+    assert h.debug_view().regime == moe.REGIME_TC_EXACT
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+    import torch
+    out2 = torch.empty(T, wl.H, device=dev)
+    h.forward(xd, T, out2)
+    torch.cuda.synchronize()
+    assert np.array_equal(out2.cpu().numpy(), got)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+
+
 def test_gemv_path_parity_olmoe_64(dev):
     """OLMoE-shaped T=64 (Zipf routing) forced onto the GEMV path."""
     import expert_routing_grouped_gb300 as moe
