@@ -238,13 +238,21 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t 
 
 // D[tmem] (+)= A[tmem] . B[smem]^T: A in tensor memory, 128 lanes = 128 rows,
 // two bf16 per 32-bit column in K order.
-__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
-                                            uint32_t idesc, uint32_t accumulate) {
+// One 64-K block: four K=16 MMAs, A columns a0 + 8 kk, B descriptor db + 2 kk
+// (32 bytes further along the swizzled row); the first accumulates only if
+// `accumulate`, the other three always.
+__device__ __forceinline__ void mma_kblock_ta(uint32_t tmem_d, uint32_t a0, uint64_t db,
+                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(db), "r"(idesc), "r"(accumulate)
+      "setp.eq.b32 q, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}" ::"r"(tmem_d),
+      "r"(a0), "l"(db), "r"(idesc), "r"(accumulate), "r"(a0 + 8), "l"(db + 2), "r"(a0 + 16),
+      "l"(db + 4), "r"(a0 + 24), "l"(db + 6)
       : "memory");
 }
 
@@ -533,9 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     {
-      uint32_t ag = 0, sb = 0, it = 0, ks = 0;
+      // Ring positions advance incrementally (no divisions in the loop) and
+      // the token descriptor is the slot's base plus a constant per K block.
+      uint32_t it = 0;
+      uint32_t ga = 0, gpar = 0;          // A group and its phase
+      uint32_t bs = 0, bpar = 0;          // token slot and its phase
+      uint32_t sl = 0, slpar = 0;         // exact mode: accumulator slice and its phase
       int last_acc = -1;
       uint32_t last_acc_par = 0;
+      constexpr uint32_t kSlotDesc = (kSlotRows * 128) >> 4;   // descriptor units per slot
+      const uint64_t db0 = sw128_desc(smem_u32(sm->b[0]));
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -546,51 +561,56 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           tc_fence_after();
         }
         const int ncols = p.planes * tl.nvalid;
-        const int n_mma = (ncols + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(BM, n_mma);
-        const int rows = 32 << box_index(ncols), kps = kSlotRows / rows;
-        for (int g0 = 0; ok && g0 < tl.K / BK; g0 += KPG) {
-          const int ga = ag % NG;
-          if (!(ok = wait_bar(&sm->a_full[ga], (ag / NG) & 1, sm, p.status))) break;
+        const uint32_t idesc = idesc_bf16(BM, (ncols + 15) & ~15);
+        const int bi = box_index(ncols);
+        const int kps_m1 = (kSlotRows >> 5 >> bi) - 1;          // K blocks per slot - 1
+        const uint32_t jj_desc = (uint32_t)((32 << bi) * 128) >> 4;
+        const uint32_t dacc = tmem + buf * BN;
+        const int nkb = tl.K / BK;
+        int jj = 0;
+        uint32_t first = 1;
+        uint64_t db_slot = db0;
+        for (int k0 = 0; ok && k0 < nkb; k0 += KPG) {
+          if (!(ok = wait_bar(&sm->a_full[ga], gpar, sm, p.status))) break;
           tc_fence_after();
           const uint32_t acol = tmem + kACol0 + ga * kGroupCols;
 #pragma unroll
           for (int j = 0; j < KPG; ++j) {
-            const int k = g0 + j;
-            const int jj = k % kps;              // K block inside the token slot
-            const int s2 = sb % NB;
             if (jj == 0) {
-              if (!(ok = wait_bar(&sm->b_full[s2], (sb / NB) & 1, sm, p.status))) break;
+              if (!(ok = wait_bar(&sm->b_full[bs], bpar, sm, p.status))) break;
+              db_slot = db0 + (uint64_t)(bs * kSlotDesc);
             }
-            uint32_t d = tmem + buf * BN;
-            int sl = 0;
+            uint32_t d = dacc;
             if (EXACT) {
-              sl = ks % NSL;
-              if (!(ok = wait_bar(&sm->acc_empty[sl], ((ks / NSL) & 1) ^ 1, sm, p.status))) break;
+              if (!(ok = wait_bar(&sm->acc_empty[sl], slpar ^ 1, sm, p.status))) break;
               tc_fence_after();
               d = tmem + sl * kSliceCols;
             }
-            const uint64_t db = sw128_desc(smem_u32(sm->b[s2] + jj * rows * 128));
+            const bool slot_done = (jj == kps_m1);
             if (elect_one()) {
-#pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                mma_bf16_ta(d, acol + j * (BK / 2) + kk * 8, db + (uint64_t)(kk * 2), idesc,
-                            (EXACT ? kk : (k | kk)) ? 1u : 0u);
-              if (jj == kps - 1) mma_commit(&sm->b_empty[s2]);
+              mma_kblock_ta(d, acol + j * (BK / 2), db_slot + (uint64_t)(jj * jj_desc), idesc,
+                            EXACT ? 0u : (first ^ 1u));
+              if (slot_done) mma_commit(&sm->b_empty[bs]);
               if (EXACT) mma_commit(&sm->acc_full[sl]);
             }
             __syncwarp();
-            if (jj == kps - 1) ++sb;
+            first = 0;
+            if (slot_done) {
+              jj = 0;
+              if (++bs == NB) { bs = 0; bpar ^= 1; }
+            } else {
+              ++jj;
+            }
             if (EXACT) {
-              last_acc = sl;
-              last_acc_par = (ks / NSL) & 1;
-              ++ks;
+              last_acc = (int)sl;
+              last_acc_par = slpar;
+              if (++sl == NSL) { sl = 0; slpar ^= 1; }
             }
           }
           if (!ok) break;
           if (elect_one()) mma_commit(&sm->a_empty[ga]);
           __syncwarp();
-          ++ag;
+          if (++ga == NG) { ga = 0; gpar ^= 1; }
         }
         if (!ok) break;
         if (!EXACT) {
