@@ -239,6 +239,241 @@ __global__ void __launch_bounds__(256) gemv_kernel(
   }
 }
 
+// ----------------------------------------------------------------------------
+// W13 with bf16 activations.  A pair of int4 codes becomes a bf16 pair
+// (136 + q_even, 136 + q_odd) in one lop3; fma.rn.f32.bf16 multiplies it by the
+// bf16 activations exactly and accumulates in f32.  136 times the chunk's
+// activation sum (f32, computed once per token when the expert's activations
+// are staged) is taken off per 32-weight chunk, before the gs64 scale:
+//   W1[n] . x = sum_chunks s_chunk * (sum_i (136 + q_i) x_i - 136 * sum_i x_i).
+// Each lane prefetches the next chunk's weights and scales before it uses the
+// current ones.
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
+  uint32_t d;
+  // (w & 0x000F000F) | 0x43004300: two offset-binary nibbles into bf16 128 + n.
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(d) : "r"(w));
+  return d;
+}
+
+__device__ __forceinline__ void mfma_pair(float &acc0, float &acc1, uint32_t q2, uint32_t x2) {
+  asm("{\n\t.reg .b16 ql, qh, xl, xh;\n\t"
+      "mov.b32 {ql, qh}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, ql, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, qh, xh, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(q2), "r"(x2));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
+    const __nv_bfloat16 *__restrict__ act, int act_stride, int T, int k, int E, int K,
+    int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
+    const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
+    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    float *__restrict__ out, int out_stride) {
+  extern __shared__ uint4 smem_v[];
+  // [NT][K/8] 16-byte groups of bf16 activations: group j of 32-wide chunk c at
+  // slot j ^ ((c >> 1) & 3), so 8 lanes reading the same j of chunks c..c+7
+  // hit 8 different 16-byte bank groups; then [NT][K/32] f32 chunk sums.
+  uint4 *xs = smem_v;
+  float *xsum = reinterpret_cast<float *>(smem_v + (size_t)NT * (K / 8));
+  const int n_active = *n_active_p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
+  const int n_routed = n_active - has_shared;
+  const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
+  const int items = n_routed * items_r + has_shared * items_s;
+  const int A = T * k;
+  const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+  const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+  const int chunks = K / 32;
+  int staged_e = -1, staged_b = -1;
+  const int rr[kRowsPerWarp] = {2 * warp, 2 * warp + 1, 16 + 2 * warp, 17 + 2 * warp};
+
+  for (int item = i0; item < i1; ++item) {
+    int e, g, p0, cnt;
+    const uint8_t *wq;
+    const float *ws;
+    if (item < n_routed * items_r) {
+      e = active[item / items_r];
+      g = item % items_r;
+      wq = wq_r + (size_t)e * rows_r * (K / 2);
+      ws = ws_r + (size_t)e * rows_r * (K / 64);
+      p0 = offsets[e];
+      cnt = offsets[e + 1] - p0;
+    } else {
+      e = E;
+      g = item - n_routed * items_r;
+      wq = wq_s;
+      ws = ws_s;
+      p0 = A;
+      cnt = T;
+    }
+    for (int b0 = 0; b0 < cnt; b0 += NT) {
+      const int nb = min(NT, cnt - b0);
+      if (e != staged_e || b0 != staged_b) {
+        __syncthreads();   // previous readers are done
+        // One thread per (token, chunk): 64 bytes in, swizzled out, chunk sum.
+        for (int i = threadIdx.x; i < NT * chunks; i += blockDim.x) {
+          const int tkn = i / chunks, c = i - tkn * chunks;
+          uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                        make_uint4(0, 0, 0, 0)};
+          float sum = 0.f;
+          if (tkn < nb) {
+            const int p = p0 + b0 + tkn;
+            const int src = (e < E) ? perm[p] / k : p - A;
+            const uint4 *row = reinterpret_cast<const uint4 *>(act + (size_t)src * act_stride) + c * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __ldg(row + j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                sum += __uint_as_float(u[m] << 16) + __uint_as_float(u[m] & 0xFFFF0000u);
+            }
+          }
+          uint4 *dst = xs + (size_t)tkn * (K / 8) + c * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j ^ ((c >> 1) & 3)] = v[j];
+          xsum[tkn * chunks + c] = sum;
+        }
+        __syncthreads();
+        staged_e = e;
+        staged_b = b0;
+      }
+      const uint8_t *wrow[kRowsPerWarp];
+      const float *srow[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const size_t row = (size_t)g * kRowsPerItem + rr[i];
+        wrow[i] = wq + row * (K / 2);
+        srow[i] = ws + row * (K / 64);
+      }
+      float acc[kRowsPerWarp][NT];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[i][t] = 0.f;
+      uint4 wv[kRowsPerWarp];
+      float sc[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        if (lane < chunks) {
+          wv[i] = ld_stream(wrow[i] + (size_t)lane * 16);
+          sc[i] = __ldg(srow[i] + (lane >> 1));
+        } else {
+          wv[i] = make_uint4(0, 0, 0, 0);
+          sc[i] = 0.f;
+        }
+      }
+      for (int c = lane; c < chunks; c += 32) {
+        // prefetch the next chunk of the same rows
+        uint4 wn[kRowsPerWarp];
+        float sn[kRowsPerWarp];
+        const int cn = c + 32;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          if (cn < chunks) {
+            wn[i] = ld_stream(wrow[i] + (size_t)cn * 16);
+            sn[i] = __ldg(srow[i] + (cn >> 1));
+          } else {
+            wn[i] = make_uint4(0, 0, 0, 0);
+            sn[i] = 0.f;
+          }
+        }
+        uint32_t xw[NT][16];
+        float xc[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint4 *src = xs + (size_t)t * (K / 8) + c * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 u = src[j ^ ((c >> 1) & 3)];
+            xw[t][4 * j] = u.x;
+            xw[t][4 * j + 1] = u.y;
+            xw[t][4 * j + 2] = u.z;
+            xw[t][4 * j + 3] = u.w;
+          }
+          xc[t] = 136.0f * xsum[t * chunks + c];
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          float pe[NT], po[NT];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) pe[t] = po[t] = 0.f;
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+              const uint32_t q2 = nib_pair_bf16(words[wi] >> (4 * pp));
+#pragma unroll
+              for (int t = 0; t < NT; ++t) mfma_pair(pe[t], po[t], q2, xw[t][4 * wi + pp]);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[i][t] = fmaf(sc[i], (pe[t] + po[t]) - xc[t], acc[i][t]);
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          wv[i] = wn[i];
+          sc[i] = sn[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[i][t] += __shfl_xor_sync(0xffffffffu, acc[i][t], o);
+      if (lane == 0) {
+        // 32-row group g = 128-row block g/4, quadrant g%4: features
+        // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
+        const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t < nb) {
+            const int p = p0 + b0 + t;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const float gg = acc[j][t], uu = acc[2 + j][t];
+              out[(size_t)p * out_stride + f0 + j] = gg / (1.0f + expf(-gg)) * uu;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int NT>
+cudaError_t launch_w13_bf16(const moe_handle *h, const __nv_bfloat16 *x, int T, cudaStream_t st) {
+  const int K = h->H;
+  const size_t smem = (size_t)NT * (K / 8) * 16 + (size_t)NT * (K / 32) * 4;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(gemv_w13_bf16_kernel<NT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kActSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w13_bf16_kernel<NT>, kWarps * 32,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int h_stride = h->I > h->Is ? h->I : h->Is;
+  gemv_w13_bf16_kernel<NT><<<h->num_sms * per_sm, kWarps * 32, smem, st>>>(
+      x, h->H, T, h->k, h->E, K, 2 * h->I, h->S ? 2 * h->Is : 0, h->ex.w13q, h->ex.w13s,
+      h->sh.w13q, h->sh.w13s, h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.h,
+      h_stride);
+  return cudaGetLastError();
+}
+
 template <int NT>
 cudaError_t launch_nt(int mode, const moe_handle *h, const void *act, int act_bf16, int act_stride,
                       int T, int K, int K_s, int rows_r, int rows_s, const uint8_t *wq_r, const float *ws_r,
@@ -285,6 +520,12 @@ cudaError_t launch_gemv(int mode, const moe_handle *h, const void *act, int act_
 }  // namespace
 
 cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t st) {
+  if (h->L.x_dtype == 1 && (size_t)4 * (h->H / 8) * 16 + (size_t)4 * (h->H / 32) * 4 <= (size_t)kActSmemBytes) {
+    const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
+    if (T >= 3) return launch_w13_bf16<4>(h, xb, T, st);
+    if (T == 2) return launch_w13_bf16<2>(h, xb, T, st);
+    return launch_w13_bf16<1>(h, xb, T, st);
+  }
   const int h_stride = h->I > h->Is ? h->I : h->Is;
   return launch_gemv(0, h, x, h->L.x_dtype == 1, h->H, T, h->H, h->H, 2 * h->I,
                      h->S ? 2 * h->Is : 0,

@@ -390,8 +390,9 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
     tl.K = p.K_s;
   }
   tl.nvalid = min(BN, cnt - tb * BN);
-  // A block of the shared expert past its rows (when rows_s < rows) has no work.
-  if (tl.shared && fb * BM >= p.rows_s) tl.nvalid = 0;
+  // Row blocks past the expert's rows (the routed and the shared expert may
+  // differ in size) have no work.
+  if (fb * BM >= (tl.shared ? p.rows_s : p.rows)) tl.nvalid = 0;
   return true;
 }
 
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_blocks = *p.n_blocks;
-  const int n_fb = p.rows / BM;
+  const int n_fb = (p.rows > p.rows_s ? p.rows : p.rows_s) / BM;
   const int n_tiles = n_blocks * n_fb;
   constexpr int NACC = EXACT ? NSL : 2;
 

@@ -28,6 +28,82 @@ __device__ __forceinline__ float load_x(const void *x, int x_is_bf16, size_t i) 
 // Small T (decode, MTP verify): split-K GEMV.  Block = 8 warps, one expert per
 // warp; blockIdx.y selects a contiguous H range.  x of the range is staged in
 // shared memory as f32.  Writes z_part[split][t][e].
+//
+// Every load of a thread is issued before its first use (x in 16-byte vectors;
+// the router row in batches of kMaxRowVec float4 per lane), so the block pays
+// one memory latency per phase rather than one per element.
+constexpr int kMaxRowVec = 12;
+
+template <int NT>
+__device__ __forceinline__ void stage_x(const void *__restrict__ x, int x_is_bf16, int T, int H,
+                                        int h0, int hps, float *xs) {
+  if (x_is_bf16) {
+    const int nv = hps / 8;                       // 8 bf16 per 16 bytes
+    for (int i = threadIdx.x; i < NT * nv; i += blockDim.x) {
+      const int t = i / nv, c = i - t * nv;
+      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+      if (t < T) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+                                  reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + h0) +
+                              c);
+        lo = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                         __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+        hi = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                         __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+      }
+      reinterpret_cast<float4 *>(xs + t * hps)[2 * c] = lo;
+      reinterpret_cast<float4 *>(xs + t * hps)[2 * c + 1] = hi;
+    }
+  } else {
+    const int nv = hps / 4;
+    for (int i = threadIdx.x; i < NT * nv; i += blockDim.x) {
+      const int t = i / nv, c = i - t * nv;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < T)
+        v = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) +
+                                                   (size_t)t * H + h0) +
+                  c);
+      reinterpret_cast<float4 *>(xs + t * hps)[c] = v;
+    }
+  }
+}
+
+// acc[t] = sum over this warp's H range of x[t][h] * wr_t[e][h], lanes reduced.
+template <int NT>
+__device__ __forceinline__ void row_dot(const float *__restrict__ wrow, const float *xs, int hps,
+                                        float acc[NT]) {
+  const int lane = threadIdx.x & 31;
+  const int nv = hps / 128;                       // float4 per lane
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int v0 = 0; v0 < nv; v0 += kMaxRowVec) {
+    float4 wv[kMaxRowVec];
+#pragma unroll
+    for (int v = 0; v < kMaxRowVec; ++v)
+      if (v0 + v < nv)
+        wv[v] = __ldg(reinterpret_cast<const float4 *>(wrow + (v0 + v) * 128 + lane * 4));
+#pragma unroll
+    for (int v = 0; v < kMaxRowVec; ++v) {
+      if (v0 + v < nv) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float4 xv =
+              *reinterpret_cast<const float4 *>(xs + t * hps + (v0 + v) * 128 + lane * 4);
+          acc[t] = fmaf(xv.x, wv[v].x, acc[t]);
+          acc[t] = fmaf(xv.y, wv[v].y, acc[t]);
+          acc[t] = fmaf(xv.z, wv[v].z, acc[t]);
+          acc[t] = fmaf(xv.w, wv[v].w, acc[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(256) router_gemv_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E,
@@ -36,34 +112,13 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(
   extern __shared__ float xs[];   // [NT][h_per_split]
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
-  for (int i = threadIdx.x; i < NT * h_per_split; i += blockDim.x) {
-    const int t = i / h_per_split, hh = i - t * h_per_split;
-    xs[i] = (t < T) ? load_x(x, x_is_bf16, (size_t)t * H + h0 + hh) : 0.f;
-  }
+  stage_x<NT>(x, x_is_bf16, T, H, h0, h_per_split, xs);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   if (e >= E) return;
-  const float *wrow = wr_t + (size_t)e * H + h0;
   float acc[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-  for (int hh = lane * 4; hh < h_per_split; hh += 128) {
-    const float4 wv = __ldg(reinterpret_cast<const float4 *>(wrow + hh));
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const float4 xv = *reinterpret_cast<const float4 *>(xs + t * h_per_split + hh);
-      acc[t] = fmaf(xv.x, wv.x, acc[t]);
-      acc[t] = fmaf(xv.y, wv.y, acc[t]);
-      acc[t] = fmaf(xv.z, wv.z, acc[t]);
-      acc[t] = fmaf(xv.w, wv.w, acc[t]);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-  }
+  row_dot<NT>(wr_t + (size_t)e * H + h0, xs, h_per_split, acc);
   if (lane == 0) {
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -244,32 +299,13 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   __shared__ int last;
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
-  for (int i = threadIdx.x; i < 4 * h_per_split; i += blockDim.x) {
-    const int t = i / h_per_split, hh = i - t * h_per_split;
-    xs[i] = (t < T) ? load_x(x, x_is_bf16, (size_t)t * H + h0 + hh) : 0.f;
-  }
+  stage_x<kGemvTokens>(x, x_is_bf16, T, H, h0, h_per_split, xs);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   if (e < E) {
-    const float *wrow = wr_t + (size_t)e * H + h0;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int hh = lane * 4; hh < h_per_split; hh += 128) {
-      const float4 wv = __ldg(reinterpret_cast<const float4 *>(wrow + hh));
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float4 xv = *reinterpret_cast<const float4 *>(xs + t * h_per_split + hh);
-        acc[t] = fmaf(xv.x, wv.x, acc[t]);
-        acc[t] = fmaf(xv.y, wv.y, acc[t]);
-        acc[t] = fmaf(xv.z, wv.z, acc[t]);
-        acc[t] = fmaf(xv.w, wv.w, acc[t]);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-    }
+    float acc[kGemvTokens];
+    row_dot<kGemvTokens>(wr_t + (size_t)e * H + h0, xs, h_per_split, acc);
     if (lane == 0) {
 #pragma unroll
       for (int t = 0; t < 4; ++t)
@@ -352,16 +388,36 @@ __global__ void __launch_bounds__(256) route_small_kernel(
       __syncwarp();
     }
   }
-  // Active experts (ascending, shared expert last) and one token block each.
+  // Active experts (ascending, shared expert last) and one token block each:
+  // the same per-thread runs, scanned over the non-empty flags.
+  __syncthreads();
+  int nz = 0;
+  for (int i = 0; i < per; ++i)
+    if (e0 + i < E && cnt[e0 + i] > 0) ++nz;
+  int inz = nz;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inz, o);
+    if (lane >= o) inz += n;
+  }
+  if (lane == 31) wsum[warp] = inz;
+  __syncthreads();
+  int nbase = 0, ntot = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+    if (i < warp) nbase += wsum[i];
+    ntot += wsum[i];
+  }
+  int apos = nbase + inz - nz;
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee < E && cnt[ee] > 0) {
+      active[apos] = ee;
+      tiles[apos] = ee << 16;
+      ++apos;
+    }
+  }
   if (threadIdx.x == 0) {
-    int na = 0;
-    for (int ee = 0; ee < E; ++ee)
-      if (cnt[ee] > 0) {
-        active[na] = ee;
-        tiles[na] = ee << 16;
-        ++na;
-      }
-    int nt = na;
+    int na = ntot, nt = ntot;
     if (n_shared) {
       active[na++] = E;
       tiles[nt++] = E << 16;

@@ -214,6 +214,20 @@ def test_edge_layouts(dev, E, k, mode):
     assert rel_l2(got, ref["out"]) <= GEMV_TOL
 
 
+@pytest.mark.parametrize("I,Is", [(1024, 2048), (2048, 1024)])
+@pytest.mark.parametrize("regime,T", [(1, 5), (2, 40), (3, 5)])
+def test_shared_expert_wider_or_narrower(dev, I, Is, regime, T):
+    """The shared expert's intermediate size differs from the routed ones'
+    (its W13 has more or fewer 128-row blocks than a routed expert's): every
+    expert path covers all of its rows."""
+    wl = Workload("shared%d_%d" % (I, Is), H=512, E=8, k=2, I=I, n_shared=1, I_shared=Is,
+                  router_mode=1, rsf=2.5, x_dtype=1, tokens=(T,), seed=61 + I // 1024,
+                  bias="normal", bias_sigma=0.1)
+    got, ref, h, _ = run_and_compare(wl, T, dev, regime=regime)
+    assert rel_l2(got, ref["out"]) <= (GEMV_TOL if regime != 2 else TC_TOL)
+    h.set_option(1, 0)
+
+
 def test_init_fault_injection_leaks_nothing(dev):
     import torch
     import expert_routing_grouped_gb300 as moe
