@@ -63,7 +63,54 @@ __device__ __forceinline__ void dequant8(uint32_t w, float2 q[4]) {
                     make_float2(-2056.0f, -136.0f));
 }
 
+// One item: 32 consecutive weight rows (group g) of one active expert e.
+struct Item {
+  const uint8_t *wq;   // the expert's packed rows
+  const float *ws;     // the expert's scales
+  int e, g, p0, cnt, K;
+};
+
+__device__ __forceinline__ Item item_at(int item, int n_routed, int items_r, int E, int A, int T,
+                                        int K_r, int K_s, int rows_r, const uint8_t *wq_r,
+                                        const float *ws_r, const uint8_t *wq_s, const float *ws_s,
+                                        const int32_t *active, const int32_t *offsets) {
+  Item it;
+  if (item < n_routed * items_r) {
+    it.K = K_r;
+    it.e = active[item / items_r];
+    it.g = item % items_r;
+    it.wq = wq_r + (size_t)it.e * rows_r * (K_r / 2);
+    it.ws = ws_r + (size_t)it.e * rows_r * (K_r / 64);
+    it.p0 = offsets[it.e];
+    it.cnt = offsets[it.e + 1] - it.p0;
+  } else {
+    it.K = K_s;
+    it.e = E;
+    it.g = item - n_routed * items_r;
+    it.wq = wq_s;
+    it.ws = ws_s;
+    it.p0 = A;
+    it.cnt = T;
+  }
+  return it;
+}
+
+// The weights and scales of chunk c of an item's four rows for this warp.
+__device__ __forceinline__ void load_chunk(const Item &it, const int rr[kRowsPerWarp], int c,
+                                           uint4 wv[kRowsPerWarp], float sc[kRowsPerWarp]) {
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    const size_t row = (size_t)it.g * kRowsPerItem + rr[i];
+    wv[i] = ld_stream(it.wq + row * (it.K / 2) + (size_t)c * 16);
+    sc[i] = __ldg(it.ws + row * (it.K / 64) + (c >> 1));
+  }
+}
+
 // mode 0: W13 + SwiGLU -> out = h;  mode 1: W2 times routing weight -> out = y.
+// Each lane keeps the next chunk's weights in flight while it works on the
+// current one; the last chunk of an item prefetches the first chunk of the
+// next item (when the item has one token batch), so short rows (W2) do not pay
+// a memory round trip per item.
 template <int NT>
 __global__ void __launch_bounds__(256) gemv_kernel(
     int mode, const void *__restrict__ act, int act_is_bf16, int act_stride, int T, int k, int E,
@@ -73,6 +120,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     const float *__restrict__ wts, float *__restrict__ out, int out_stride) {
   extern __shared__ float act_s[];   // [NT][K] activations of the current expert pass
+  __shared__ float wt_s[NT];         // W2: routing weights of the staged tokens
   const int n_active = *n_active_p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
@@ -98,30 +146,20 @@ __global__ void __launch_bounds__(256) gemv_kernel(
     for (int i = 0; i < kRowsPerWarp; ++i) rr[i] = kRowsPerWarp * warp + i;
   }
 
+  bool pre = false;                    // wv/sc already hold this item's first chunk
+  uint4 wv[kRowsPerWarp];
+  float sc[kRowsPerWarp];
   for (int item = i0; item < i1; ++item) {
-    int e, g, p0, cnt, K;
-    const uint8_t *wq;
-    const float *ws;
-    if (item < n_routed * items_r) {
-      K = K_r;
-      e = active[item / items_r];
-      g = item % items_r;
-      wq = wq_r + (size_t)e * rows_r * (K / 2);
-      ws = ws_r + (size_t)e * rows_r * (K / 64);
-      p0 = offsets[e];
-      cnt = offsets[e + 1] - p0;
-    } else {
-      K = K_s;
-      e = E;
-      g = item - n_routed * items_r;
-      wq = wq_s;
-      ws = ws_s;
-      p0 = A;
-      cnt = T;
-    }
+    const Item it = item_at(item, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r, ws_r, wq_s,
+                            ws_s, active, offsets);
+    const int e = it.e, g = it.g, p0 = it.p0, cnt = it.cnt, K = it.K;
     const int chunks = K / 32;   // 16-byte chunks per row
     for (int b0 = 0; b0 < cnt; b0 += NT) {
       const int nb = min(NT, cnt - b0);
+      if (!pre || b0 > 0) {
+        if (lane < chunks) load_chunk(it, rr, lane, wv, sc);
+      }
+      pre = false;
       if (e != staged_e || b0 != staged_b) {
         __syncthreads();   // previous readers are done
         for (int i = threadIdx.x; i < NT * (K / 4); i += blockDim.x) {
@@ -149,31 +187,36 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           const int cc = c4 >> 3, jj = c4 & 7;
           reinterpret_cast<float4 *>(act_s + (size_t)tkn * K)[cc * 8 + (jj ^ (cc & 7))] = v;
         }
+        if (mode == 1 && threadIdx.x < NT)
+          wt_s[threadIdx.x] =
+              (threadIdx.x < nb && e < E) ? wts[perm[p0 + b0 + threadIdx.x]] : 1.0f;
         __syncthreads();
         staged_e = e;
         staged_b = b0;
-      }
-      const uint8_t *wrow[kRowsPerWarp];
-      const float *srow[kRowsPerWarp];
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const size_t row = (size_t)g * kRowsPerItem + rr[i];
-        wrow[i] = wq + row * (K / 2);
-        srow[i] = ws + row * (K / 64);
       }
       float acc[kRowsPerWarp][NT];
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[i][t] = 0.f;
-#pragma unroll 2
       for (int c = lane; c < chunks; c += 32) {
-        uint4 wv[kRowsPerWarp];
-        float sc[kRowsPerWarp];
+        uint4 wn[kRowsPerWarp];
+        float sn[kRowsPerWarp];
+        const int cn = c + 32;
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
-          wv[i] = ld_stream(wrow[i] + (size_t)c * 16);
-          sc[i] = __ldg(srow[i] + (c >> 1));
+          wn[i] = make_uint4(0, 0, 0, 0);
+          sn[i] = 0.f;
+        }
+        if (cn < chunks) {
+          load_chunk(it, rr, cn, wn, sn);
+        } else if (b0 + NT >= cnt && item + 1 < i1) {
+          const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r,
+                                  ws_r, wq_s, ws_s, active, offsets);
+          if (lane < nx.K / 32) {
+            load_chunk(nx, rr, lane, wn, sn);
+            pre = true;
+          }
         }
         // activations of this chunk (32 K) for each token, as f32 pairs
         float2 xa[NT][16];
@@ -205,6 +248,11 @@ __global__ void __launch_bounds__(256) gemv_kernel(
 #pragma unroll
           for (int t = 0; t < NT; ++t) acc[i][t] = fmaf(sc[i], part[t].x + part[t].y, acc[i][t]);
         }
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          wv[i] = wn[i];
+          sc[i] = sn[i];
+        }
       }
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i)
@@ -227,7 +275,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
                 out[(size_t)p * out_stride + f0 + j] = gg / (1.0f + expf(-gg)) * uu;
               }
             } else {
-              const float wt = (e < E) ? wts[perm[p]] : 1.0f;
+              const float wt = wt_s[t];
 #pragma unroll
               for (int i = 0; i < kRowsPerWarp; ++i)
                 out[(size_t)p * out_stride + g * kRowsPerItem + rr[i]] = wt * acc[i][t];
@@ -292,27 +340,19 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
   int staged_e = -1, staged_b = -1;
   const int rr[kRowsPerWarp] = {2 * warp, 2 * warp + 1, 16 + 2 * warp, 17 + 2 * warp};
 
+  bool pre = false;                    // wv/sc already hold this item's first chunk
+  uint4 wv[kRowsPerWarp];
+  float sc[kRowsPerWarp];
   for (int item = i0; item < i1; ++item) {
-    int e, g, p0, cnt;
-    const uint8_t *wq;
-    const float *ws;
-    if (item < n_routed * items_r) {
-      e = active[item / items_r];
-      g = item % items_r;
-      wq = wq_r + (size_t)e * rows_r * (K / 2);
-      ws = ws_r + (size_t)e * rows_r * (K / 64);
-      p0 = offsets[e];
-      cnt = offsets[e + 1] - p0;
-    } else {
-      e = E;
-      g = item - n_routed * items_r;
-      wq = wq_s;
-      ws = ws_s;
-      p0 = A;
-      cnt = T;
-    }
+    const Item it = item_at(item, n_routed, items_r, E, A, T, K, K, rows_r, wq_r, ws_r, wq_s,
+                            ws_s, active, offsets);
+    const int e = it.e, g = it.g, p0 = it.p0, cnt = it.cnt;
     for (int b0 = 0; b0 < cnt; b0 += NT) {
       const int nb = min(NT, cnt - b0);
+      if (!pre || b0 > 0) {
+        if (lane < chunks) load_chunk(it, rr, lane, wv, sc);
+      }
+      pre = false;
       if (e != staged_e || b0 != staged_b) {
         __syncthreads();   // previous readers are done
         // One thread per (token, chunk): 64 bytes in, swizzled out, chunk sum.
@@ -344,45 +384,28 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
         staged_e = e;
         staged_b = b0;
       }
-      const uint8_t *wrow[kRowsPerWarp];
-      const float *srow[kRowsPerWarp];
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const size_t row = (size_t)g * kRowsPerItem + rr[i];
-        wrow[i] = wq + row * (K / 2);
-        srow[i] = ws + row * (K / 64);
-      }
       float acc[kRowsPerWarp][NT];
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[i][t] = 0.f;
-      uint4 wv[kRowsPerWarp];
-      float sc[kRowsPerWarp];
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        if (lane < chunks) {
-          wv[i] = ld_stream(wrow[i] + (size_t)lane * 16);
-          sc[i] = __ldg(srow[i] + (lane >> 1));
-        } else {
-          wv[i] = make_uint4(0, 0, 0, 0);
-          sc[i] = 0.f;
-        }
-      }
       for (int c = lane; c < chunks; c += 32) {
-        // prefetch the next chunk of the same rows
+        // prefetch the next chunk of the same rows, or the next item's first
         uint4 wn[kRowsPerWarp];
         float sn[kRowsPerWarp];
-        const int cn = c + 32;
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
-          if (cn < chunks) {
-            wn[i] = ld_stream(wrow[i] + (size_t)cn * 16);
-            sn[i] = __ldg(srow[i] + (cn >> 1));
-          } else {
-            wn[i] = make_uint4(0, 0, 0, 0);
-            sn[i] = 0.f;
-          }
+          wn[i] = make_uint4(0, 0, 0, 0);
+          sn[i] = 0.f;
+        }
+        const int cn = c + 32;
+        if (cn < chunks) {
+          load_chunk(it, rr, cn, wn, sn);
+        } else if (b0 + NT >= cnt && item + 1 < i1) {
+          const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K, K, rows_r, wq_r, ws_r,
+                                  wq_s, ws_s, active, offsets);
+          load_chunk(nx, rr, lane, wn, sn);
+          pre = true;
         }
         uint32_t xw[NT][16];
         float xc[NT];

@@ -38,6 +38,7 @@
 // Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
 // the device status word, flags the CTA to stop, and the kernel drains its
 // outstanding copies and MMAs (bounded), frees TMEM and returns.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -1202,8 +1203,12 @@ cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z
 
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
                            cudaStream_t st) {
-  combine_kernel<<<h->num_sms * 8, 256, 0, st>>>(T, h->H, h->k, h->S, h->ws.inv, h->ws.y, out,
-                                                 accumulate ? 1 : 0);
+  // One float4 per thread; no more CTAs than there is work (decode: a handful).
+  const long long work = (long long)T * (h->H / 4);
+  const int blocks = (int)std::min<long long>((long long)h->num_sms * 8, (work + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  combine_kernel<<<blocks, 256, 0, st>>>(T, h->H, h->k, h->S, h->ws.inv, h->ws.y, out,
+                                         accumulate ? 1 : 0);
   return cudaGetLastError();
 }
 

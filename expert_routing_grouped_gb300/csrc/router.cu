@@ -68,20 +68,33 @@ __device__ __forceinline__ void stage_x(const void *__restrict__ x, int x_is_bf1
   }
 }
 
-// acc[t] = sum over this warp's H range of x[t][h] * wr_t[e][h], lanes reduced.
+// The first batch of a warp's router-row loads, issued before the block stages
+// x so the two memory round trips overlap.
+__device__ __forceinline__ void row_prefetch(const float *__restrict__ wrow, int hps,
+                                             float4 wv[kMaxRowVec]) {
+  const int lane = threadIdx.x & 31;
+  const int nv = hps / 128;
+#pragma unroll
+  for (int v = 0; v < kMaxRowVec; ++v)
+    if (v < nv) wv[v] = __ldg(reinterpret_cast<const float4 *>(wrow + v * 128 + lane * 4));
+}
+
+// acc[t] = sum over this warp's H range of x[t][h] * wr_t[e][h], lanes reduced;
+// wv holds the row's first kMaxRowVec float4 per lane (row_prefetch).
 template <int NT>
 __device__ __forceinline__ void row_dot(const float *__restrict__ wrow, const float *xs, int hps,
-                                        float acc[NT]) {
+                                        float4 wv[kMaxRowVec], float acc[NT]) {
   const int lane = threadIdx.x & 31;
   const int nv = hps / 128;                       // float4 per lane
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
   for (int v0 = 0; v0 < nv; v0 += kMaxRowVec) {
-    float4 wv[kMaxRowVec];
+    if (v0 > 0) {
 #pragma unroll
-    for (int v = 0; v < kMaxRowVec; ++v)
-      if (v0 + v < nv)
-        wv[v] = __ldg(reinterpret_cast<const float4 *>(wrow + (v0 + v) * 128 + lane * 4));
+      for (int v = 0; v < kMaxRowVec; ++v)
+        if (v0 + v < nv)
+          wv[v] = __ldg(reinterpret_cast<const float4 *>(wrow + (v0 + v) * 128 + lane * 4));
+    }
 #pragma unroll
     for (int v = 0; v < kMaxRowVec; ++v) {
       if (v0 + v < nv) {
@@ -112,13 +125,15 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(
   extern __shared__ float xs[];   // [NT][h_per_split]
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
-  stage_x<NT>(x, x_is_bf16, T, H, h0, h_per_split, xs);
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
+  float4 wv[kMaxRowVec];
+  if (e < E) row_prefetch(wr_t + (size_t)e * H + h0, h_per_split, wv);
+  stage_x<NT>(x, x_is_bf16, T, H, h0, h_per_split, xs);
+  __syncthreads();
   if (e >= E) return;
   float acc[NT];
-  row_dot<NT>(wr_t + (size_t)e * H + h0, xs, h_per_split, acc);
+  row_dot<NT>(wr_t + (size_t)e * H + h0, xs, h_per_split, wv, acc);
   if (lane == 0) {
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -299,13 +314,15 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   __shared__ int last;
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
-  stage_x<kGemvTokens>(x, x_is_bf16, T, H, h0, h_per_split, xs);
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
+  float4 wv[kMaxRowVec];
+  if (e < E) row_prefetch(wr_t + (size_t)e * H + h0, h_per_split, wv);
+  stage_x<kGemvTokens>(x, x_is_bf16, T, H, h0, h_per_split, xs);
+  __syncthreads();
   if (e < E) {
     float acc[kGemvTokens];
-    row_dot<kGemvTokens>(wr_t + (size_t)e * H + h0, xs, h_per_split, acc);
+    row_dot<kGemvTokens>(wr_t + (size_t)e * H + h0, xs, h_per_split, wv, acc);
     if (lane == 0) {
 #pragma unroll
       for (int t = 0; t < 4; ++t)
