@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -69,7 +70,6 @@ constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
 constexpr int kDeqWarps = 8;
-constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
 static_assert(kACol0 + NG * kGroupCols <= 512, "TMEM columns");
 static_assert(NSL * kSliceCols <= (int)kACol0, "TMEM columns (exact mode)");
 
@@ -119,84 +119,11 @@ struct TcParams {
 };
 
 // --------------------------------------------------------------- PTX glue --
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: false if the CTA is stopping or the wait timed out (then the
-// status word and the CTA's abort flag are set).  The first test is inlined;
-// only a wait that has to poll calls the out-of-line loop.
-__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, SmemTC *sm,
-                                           int32_t *status) {
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*reinterpret_cast<volatile int *>(&sm->abort)) return false;
-      if (globaltimer() - t0 > kWaitNs) {
-        atomicExch(reinterpret_cast<int *>(&sm->abort), 1);
-        atomicExch(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
+// (mbarrier, TMA and elect helpers: ptx.cuh)
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
                                          int32_t *status) {
-  return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, sm, status);
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// One lane of a converged warp (elect.sync); the role loops run warp-wide so
-// descriptors, coordinates and barrier addresses stay warp-uniform.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
+  return moe::wait_bar(bar, parity, &sm->abort, status);
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -1134,7 +1061,11 @@ __global__ void split_planes_kernel(const float *__restrict__ w, __nv_bfloat16 *
 
 // ---------------------------------------------------------- host side --
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void *p = nullptr;
@@ -1152,7 +1083,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // swizzle (or none).
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, uint64_t cols,
               uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows,
-              bool swizzle = true) {
+              bool swizzle) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -1164,10 +1095,6 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t e
              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
-
-}  // namespace
 
 bool tc_path_available() { return get_encode() != nullptr; }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -112,6 +113,12 @@ cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumula
 cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
                                 cudaStream_t s);
 cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t s);
+// 2D tensor map over a row-major [rows][cols] array (row stride in elements),
+// box [box_rows][box_cols], 128-byte swizzle or none.  False if the driver
+// entry point is missing or the encoder rejects the arguments.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, uint64_t cols,
+              uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows,
+              bool swizzle = true);
 cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
                             cudaStream_t st);
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,

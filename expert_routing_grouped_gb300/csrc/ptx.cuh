@@ -1,0 +1,103 @@
+// ptx.cuh -- the mbarrier / TMA / elect glue shared by the persistent kernels
+// (tensor-core grouped GEMM, TMA-fed GEMV).  Every wait is bounded by
+// %globaltimer: a wait that gives up sets the device status word and the CTA's
+// abort flag, and returns false so the caller can drain and exit.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait
+
+static __device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+static __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+static __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+static __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+static __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+static __device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false if the CTA is stopping (*abort set) or the wait timed
+// out (then *status and *abort are set).  The first test is inlined; only a
+// wait that has to poll calls the out-of-line loop.
+static __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, int *abort,
+                                                  int32_t *status) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*reinterpret_cast<volatile int *>(abort)) return false;
+      if (globaltimer() - t0 > kWaitNs) {
+        atomicExch(abort, 1);
+        atomicExch(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+static __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *abort,
+                                                int32_t *status) {
+  return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort, status);
+}
+
+// Spins (bounded) until the phase of `parity` completes; for draining copies
+// before a CTA exits.
+static __device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity,
+                                                 unsigned long long t0) {
+  while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < kWaitNs) {
+  }
+}
+
+static __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                                   uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One lane of a converged warp (elect.sync); role loops run warp-wide so
+// coordinates and barrier addresses stay warp-uniform.
+static __device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+}  // namespace moe
