@@ -204,7 +204,7 @@ def make_layer(wl, layer, max_tokens, dev):
 
 # -------------------------------------------------------------- prefill --
 
-def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
+def bench_prefill(dev, steps, warmup, stream, name="glm_prefill", sync_all=None):
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
@@ -225,7 +225,7 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
     stage = {}
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    torch.cuda.synchronize()
+    (sync_all or torch.cuda.synchronize)()
     with ClockSampler(dev) as clk:
         t0 = time.perf_counter()
         for i in range(steps):
@@ -234,7 +234,7 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
             evs[i][1].record(stream)
             for name, ms in layer.stage_times():     # synchronises each step
                 stage.setdefault(name, []).append(ms)
-        torch.cuda.synchronize()
+        (sync_all or torch.cuda.synchronize)()
         wall = time.perf_counter() - t0
     step_ms = [a.elapsed_time(b) for a, b in evs]
     launches = layer.debug_view().launches - launches0
@@ -261,7 +261,7 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill"):
 
 # --------------------------------------------------------------- decode --
 
-def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None):
+def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None, sync_all=None):
     """The decode stack: per layer an RMS pre-norm and moe_forward_residual.
     The timed steps replay one CUDA graph of the whole stack (the library's
     launches are stream-ordered and capturable); a separate eager pass with
@@ -316,12 +316,13 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     cur = torch.cuda.current_stream()
+    (sync_all or torch.cuda.synchronize)()
     with ClockSampler(dev) as clk:
         for i in range(steps):
             evs[i][0].record(cur)
             g.replay()
             evs[i][1].record(cur)
-        torch.cuda.synchronize()
+        (sync_all or torch.cuda.synchronize)()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     # e2e: pinned host x -> device, the stack, result -> host, every step
     xh = torch.from_numpy(synth.bf16_to_f32(x)).pin_memory()
@@ -379,6 +380,35 @@ def cpu_baseline(wl, T, n_tokens, layers_per_step=1):
 
 # ------------------------------------------------------------------ main --
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+CSRC = os.path.join(ROOT, "expert_routing_grouped_gb300", "csrc")
+KERNEL_SOURCES = {"ggemm_w13_tc": ("ggemm_tc.cu", "ptx.cuh", "moe_internal.cuh"),
+                  "gemv_w13": ("gemv.cu", "moe_internal.cuh")}
+
+
+def source_digest(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic(kernel):
+    """DRAM bytes per launch (read + write) from the committed ncu capture of
+    this kernel, or None when there is none or the kernel's sources changed
+    since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            e = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not e or e.get("source_digest") != source_digest(kernel):
+        return None
+    return e.get("bytes_per_launch")
+
+
 def roofline_tc(res, pk, src):
     wl, T = res["wl"], res["T"]
     rows = T * wl.k + wl.n_shared * T
@@ -389,7 +419,8 @@ def roofline_tc(res, pk, src):
     ach = fl / (ms * 1e-3) / 1e12
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     return {"kernel": "ggemm_w13_tc", "bound": "tensor", "achieved": round(ach, 1),
-            "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+            "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "traffic": traffic("ggemm_w13_tc") if wl.name == "glm_prefill" else None,
             "peak_source": "%s bf16_tflops_sustained" % src,
             "per_launch": "2*(T*k+T)*H*2I = %.3g FLOP" % fl}
 
@@ -404,8 +435,57 @@ def roofline_gemv(res, pk, src):
     ach = by / (ms * 1e-3) / 1e9
     return {"kernel": "gemv_w13", "bound": "hbm", "achieved": round(ach, 1),
             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-            "traffic": None, "peak_source": "%s hbm_gbs" % src,
+            "traffic": traffic("gemv_w13") if wl.name == "glm_decode" else None,
+            "peak_source": "%s hbm_gbs" % src,
             "per_launch": "%.1f activated experts x 2*H*I*0.5625 B + x" % na}
+
+
+def make_line(pre, dec, world, reduce_max, pk, src, steps, warmup):
+    """The JSON line from the per-rank results.  Replicas: every rank ran the
+    same step on its own GPU; the step time is the maximum over ranks
+    (reduce_max) and the value counts the tokens of all ranks."""
+    head = pre if pre is not None else dec
+    ms = reduce_max(statistics.mean(head["step_ms"]))
+    tokens = head["T"] * world
+    value = tokens / (ms * 1e-3)
+    line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if head is pre else "f32", "data": "synthetic",
+            "config": {"workload": head["wl"].name, "T": head["T"],
+                       "layers_per_step": 1 if head is pre else head["layers"],
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (weights %.1f GB per step)"
+                             % ((layer_bytes(head["wl"], head["wl"].E + 1, head["T"]) if head is pre
+                                 else sum(layer_bytes(head["wl"], a, head["T"]) for a in head["n_active"])) / 1e9)},
+            "gpu_launches": int(head["launches"]),
+            "stage_ms": {k: round(v, 4) for k, v in head["stage"].items()},
+            "clocks": head["clocks"],
+            "e2e": {"value": head["T"] * world / reduce_max(head["e2e_s"]), "unit": "tokens/s",
+                    "h2d_bytes_per_step": head["h2d"], "d2h_bytes_per_step": head["d2h"]}}
+    line["roofline"] = roofline_tc(head, pk, src) if head is pre else roofline_gemv(head, pk, src)
+    if head is pre:
+        c = head["counts"]
+        line["config"]["expert_loads"] = {"max": int(c.max()), "empty": int((c == 0).sum()),
+                                          "cv": round(float(c.std() / c.mean()), 3)}
+        line["tflops"] = layer_flops(head["wl"], head["T"]) / (ms * 1e-3) / 1e12
+    if dec is not None and head is not dec:
+        dms = reduce_max(statistics.mean(dec["step_ms"]))
+        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
+        line["decode"] = {"workload": "%s x%d layers, CUDA-graph replay" % (dec["wl"].name, dec["layers"]),
+                          "T": dec["T"],
+                          "tokens_per_s": dec["T"] * world / (dms * 1e-3), "ms_per_step": dms,
+                          "us_per_layer": 1e3 * dms / dec["layers"],
+                          "hbm_gbs": byts * world / (dms * 1e-3) / 1e9,
+                          "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
+                          "roofline": roofline_gemv(dec, pk, src)}
+    elif head is dec:
+        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
+        line["hbm_gbs"] = byts * world / (ms * 1e-3) / 1e9
+        line["hbm_frac"] = byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]
+        line["us_per_layer"] = 1e3 * ms / dec["layers"]
+    return line
 
 
 def main():
@@ -453,6 +533,13 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     dev = torch.device("cuda", torch.cuda.current_device())
+
+    def sync_all():
+        # the timed region is bracketed by a device sync and, across ranks, a barrier
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
     import expert_routing_grouped_gb300 as moe  # noqa: F401  (no fallback: fails if unbuilt)
     stream = torch.cuda.Stream()
     pk, src = peaks()
@@ -462,15 +549,16 @@ def main():
     pre = dec = None
     if do_prefill:
         pre = bench_prefill(dev, args.steps, args.warmup, stream,
-                            "glm_prefill_small" if args.workload == "prefill_small" else "glm_prefill")
+                            "glm_prefill_small" if args.workload == "prefill_small" else "glm_prefill",
+                            sync_all=sync_all)
         if pre["regime"] != 2 and args.workload == "both":
             pre = None          # tensor-core path unavailable: decode becomes the headline
     if do_decode:
         if args.workload == "decode_small":
             dec = bench_decode(dev, args.steps, args.warmup, stream, name="glm_prefill_small",
-                               layers=1)
+                               layers=1, sync_all=sync_all)
         else:
-            dec = bench_decode(dev, args.steps, args.warmup, stream)
+            dec = bench_decode(dev, args.steps, args.warmup, stream, sync_all=sync_all)
 
     def reduce_max(v):
         if world == 1:
@@ -479,48 +567,8 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    line = make_line(pre, dec, world, reduce_max, pk, src, args.steps, args.warmup)
     head = pre if pre is not None else dec
-    ms = reduce_max(statistics.mean(head["step_ms"]))
-    tokens = head["T"] * world
-    value = tokens / (ms * 1e-3)
-    line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if head is pre else "f32", "data": "synthetic",
-            "config": {"workload": head["wl"].name, "T": head["T"],
-                       "layers_per_step": 1 if head is pre else head["layers"],
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (weights %.1f GB per step)"
-                             % ((layer_bytes(head["wl"], head["wl"].E + 1, head["T"]) if head is pre
-                                 else sum(layer_bytes(head["wl"], a, head["T"]) for a in head["n_active"])) / 1e9)},
-            "gpu_launches": int(head["launches"]),
-            "stage_ms": {k: round(v, 4) for k, v in head["stage"].items()},
-            "clocks": head["clocks"],
-            "e2e": {"value": head["T"] * world / reduce_max(head["e2e_s"]), "unit": "tokens/s",
-                    "h2d_bytes_per_step": head["h2d"], "d2h_bytes_per_step": head["d2h"]}}
-    line["roofline"] = roofline_tc(head, pk, src) if head is pre else roofline_gemv(head, pk, src)
-    if head is pre:
-        c = head["counts"]
-        line["config"]["expert_loads"] = {"max": int(c.max()), "empty": int((c == 0).sum()),
-                                          "cv": round(float(c.std() / c.mean()), 3)}
-        line["tflops"] = layer_flops(head["wl"], head["T"]) / (ms * 1e-3) / 1e12
-    if dec is not None and head is not dec:
-        dms = statistics.mean(dec["step_ms"])
-        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
-        line["decode"] = {"workload": "%s x%d layers, CUDA-graph replay" % (dec["wl"].name, dec["layers"]),
-                          "T": dec["T"],
-                          "tokens_per_s": dec["T"] / (dms * 1e-3), "ms_per_step": dms,
-                          "us_per_layer": 1e3 * dms / dec["layers"],
-                          "hbm_gbs": byts / (dms * 1e-3) / 1e9,
-                          "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                          "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
-                          "roofline": roofline_gemv(dec, pk, src)}
-    elif head is dec:
-        dms = ms
-        byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])
-        line["hbm_gbs"] = byts / (dms * 1e-3) / 1e9
-        line["hbm_frac"] = line["hbm_gbs"] / pk["hbm_gbs"]
-        line["us_per_layer"] = 1e3 * dms / dec["layers"]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(head["wl"], head["T"], 8 if head is pre else 1,
                                             1 if head is pre else head["layers"])

@@ -1,0 +1,81 @@
+"""The multi-GPU (replicas) path of bench.py on CPU ranks: two gloo processes
+build the JSON line from per-rank results the way the GPU ranks do, and the
+reference arm's extra ranks exit without work.  No GPU is touched."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _fake_results(rank):
+    """What bench_prefill / bench_decode return, with rank-dependent times."""
+    import synth
+    pre = {"wl": synth.BY_NAME["glm_prefill"], "T": 4096, "step_ms": [3.0 + rank] * 4,
+           "stage": {"w13": 2.0 + 0.5 * rank, "w2": 1.0}, "launches": 70, "regime": 2,
+           "counts": np.arange(1, 257, dtype=np.int32), "clocks": {"sm_mhz": 2070.0},
+           "e2e_s": 0.004 + 0.001 * rank, "h2d": 100, "d2h": 200}
+    dec = {"wl": synth.BY_NAME["glm_decode"], "T": 1, "step_ms": [0.6 + 0.2 * rank] * 4,
+           "layers": 8, "n_active": [9] * 8, "stage": {"w13": 0.03}, "launches": 400,
+           "clocks": {"sm_mhz": 2070.0}, "e2e_s": 0.001, "h2d": 1, "d2h": 1}
+    return pre, dec
+
+
+def _rank_main(rank, world, port, out_path):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+    def reduce_max(v):
+        t = torch.tensor([float(v)])
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pre, dec = _fake_results(rank)
+    pk = {"hbm_gbs": 6792.4, "bf16_tflops": 1898.0, "bf16_tflops_sustained": 1707.1}
+    line = bench.make_line(pre, dec, world, reduce_max, pk, "measured", 4, 3)
+    dist.barrier()
+    dist.destroy_process_group()
+    if rank == 0:
+        with open(out_path, "w") as f:
+            json.dump(line, f)
+
+
+def test_two_gloo_ranks_take_the_slowest_rank(tmp_path):
+    import torch.multiprocessing as mp
+    out = str(tmp_path / "line.json")
+    mp.start_processes(_rank_main, args=(2, _free_port(), out), nprocs=2, start_method="spawn")
+    line = json.load(open(out))
+    assert line["n_gpus"] == 2 and line["scaling"] == "weak"
+    assert line["config"]["parallelism"] == "replicas"
+    assert line["ms_per_step"] == pytest.approx(4.0)                 # max over ranks
+    assert line["value"] == pytest.approx(2 * 4096 / 4.0e-3)         # tokens of all ranks
+    assert line["e2e"]["value"] == pytest.approx(2 * 4096 / 0.005)
+    assert line["decode"]["ms_per_step"] == pytest.approx(0.8)
+    assert line["decode"]["tokens_per_s"] == pytest.approx(2 / 0.8e-3)
+    assert line["roofline"]["unit"] == "TFLOP/s"
+    for key in ("metric", "unit", "higher_is_better", "dtype", "data", "config", "gpu_launches",
+                "clocks", "e2e", "roofline", "vs_baseline", "steps", "warmup"):
+        assert key in line
+
+
+def test_reference_arm_extra_rank_exits_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
