@@ -18,20 +18,23 @@
 // Per CTA (one per SM, 16 warps):
 //   warp 0      TMA producer of raw int4 weight tiles (128 rows x 256 K, 128-byte
 //               swizzled) and their gs64 scales, 4 stages deep;
-//   warp 2      TMA producer of bf16 token tiles (up to 128 rows x 64 K, 128-byte
+//   warp 2      TMA producer of bf16 token tiles (up to 192 rows x 64 K, 128-byte
 //               swizzled, several K blocks per 32 KB slot for small tiles); the
 //               two producers run independently.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
-//               f32 accumulate) M=128, N=16..128, K=16 by one elected lane
+//               f32 accumulate) M=128, N=16..160, K=16 by one elected lane
 //               (the warp runs the loop, so operands stay uniform), commits
 //               to mbarriers.  A is read from TMEM, B from shared memory.
 //   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
 //   warps 8-15  dequant: raw int4 -> bf16(q * s), written straight into TMEM
 //               as the MMA's A operand with tcgen05.st (a warp owns one lane
 //               quadrant and half of each 64-K block: one row, 32 K per thread).
-// TMEM (512 columns): two 128-column accumulators, so the epilogue of one tile
-// overlaps the main loop of the next, and two 128-column A groups (4 K blocks
-// of 64 each), so the dequant of one raw stage overlaps the MMAs of the last.
+// TMEM (512 columns): two 160-column accumulators, so the epilogue of one tile
+// overlaps the main loop of the next, and two 64-column A groups (2 K blocks
+// of 64 each), so the dequant of one group overlaps the MMAs of the other.
+// An issuing thread pays ~110 clocks per MMA for any N up to 192, so the tile
+// is as wide as TMEM allows while both accumulators fit; 192-token tiles
+// (A groups then in columns 384-511) were not bitwise repeatable and are not used.
 // Keeping A out of shared memory leaves shared-memory bandwidth to the token
 // operand: per 64-K block the MMA reads N x 128 bytes of tokens that TMA wrote,
 // and nothing else but the 4.5 KB raw stage passes through it.
@@ -52,20 +55,17 @@ constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BN = kTileTokens;  // tokens per tile (MMA N, max)
 constexpr int BK = 64;           // K per bf16 block (128 bytes of a row)
 constexpr int RK = 256;          // K per raw int4 stage (128 bytes of a row)
-#ifndef MOE_TC_KPG
-#define MOE_TC_KPG 4
-#endif
-constexpr int KPG = MOE_TC_KPG;  // K blocks per A group (TMEM handoff unit)
+constexpr int KPG = 2;           // K blocks per A group (TMEM handoff unit)
 constexpr int GPS = RK / BK / KPG;  // A groups per raw stage
-constexpr int NG = 8 / KPG;      // A groups in TMEM (256 columns in all)
-constexpr int NB = 4;            // token slots
+constexpr int NG = 2;            // A groups in TMEM
+constexpr int NB = 3;            // token slots
 constexpr int NR = 4;            // raw stages
-constexpr int kSlotRows = 256;   // rows of 128 bytes per token slot (32 KB)
+constexpr int kSlotRows = 384;   // rows of 128 bytes per token slot (48 KB)
 constexpr int NSL = 16;          // exact mode: per-group accumulator slices
 constexpr int kSliceCols = 16;   // exact mode: columns per slice (MMA N)
-constexpr int NSE = 8;           // exact mode: scale stages read by the epilogue
-constexpr uint32_t kACol0 = 2 * BN;          // first TMEM column of the A groups
-constexpr uint32_t kGroupCols = KPG * BK / 2;  // 128 columns: 2 bf16 per column
+constexpr int NSE = 4;           // exact mode: scale stages read by the epilogue
+constexpr uint32_t kACol0 = 2 * BN;            // first TMEM column of the A groups
+constexpr uint32_t kGroupCols = KPG * BK / 2;  // 64 columns: 2 bf16 per column
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
@@ -75,7 +75,7 @@ static_assert(NSL * kSliceCols <= (int)kACol0, "TMEM columns (exact mode)");
 
 struct __align__(1024) SmemTC {
   uint8_t raw[NR][BM * 128];     // 4 x 16 KB
-  uint8_t b[NB][kSlotRows * 128];  // 4 x 32 KB
+  uint8_t b[NB][kSlotRows * 128];  // 3 x 48 KB
   float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
   float sce[NSE][BM * (RK / 64)];  // exact mode: the same scales, for the epilogue
   uint64_t raw_full[NR], raw_empty[NR];
@@ -87,19 +87,24 @@ struct __align__(1024) SmemTC {
   int abort;
 };
 
-// Token slots hold 32 KB: two 64-K blocks of a 128-row box, or more K blocks
-// of a smaller box (8 blocks of 32 rows, ...), so small tiles keep as many K
-// blocks in flight as large ones keep bytes.
+// Token boxes of 32, 64, 96 or 192 rows (the smallest that covers the tile's
+// operand rows); a 48 KB slot carries 8, 4, 4 or 2 K blocks of one box, so
+// small tiles keep as many K blocks in flight as large ones keep bytes (the
+// counts are powers of two: K / 64 is a multiple of 8).
+constexpr int kBoxRows[4] = {32, 64, 96, 192};
+constexpr int kBoxKps[4] = {8, 4, 4, 2};
 __device__ __forceinline__ int box_index(int nvalid) {
-  return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : 2;
+  return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 96 ? 2 : 3;
 }
+__device__ __forceinline__ int box_rows(int bi) { return bi == 0 ? 32 : bi == 1 ? 64 : bi == 2 ? 96 : 192; }
+__device__ __forceinline__ int box_kps(int bi) { return bi == 0 ? 8 : bi <= 2 ? 4 : 2; }
 
 struct TcParams {
   CUtensorMap map_w;       // raw weights of the routed experts [E * rows][K/2] u8
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
   CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
-  CUtensorMap map_b[3];    // bf16 token operand [R][K], boxes of 32/64/128 rows
+  CUtensorMap map_b[4];    // bf16 token operand [R][K], boxes of 32/64/96/192 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
   int planes;              // operand rows per token (exact mode: 2 for hi/lo planes)
   int K;                   // reduction length (H for W13, I for W2)
@@ -443,14 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         // Smallest box covering the tile's operand rows (planes per token);
         // one slot carries 256 / rows K blocks of it (K / 64 is a multiple of 8).
         const int bi = box_index(p.planes * tl.nvalid);
-        const int rows = 32 << bi, kps = kSlotRows / rows;
+        const int rows = box_rows(bi), kps = box_kps(bi);
         const int brow = p.planes * tl.p0;
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
           if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
           if (elect_one()) {
-            mbar_expect_tx(&sm->b_full[s2], kSlotRows * 128);
+            mbar_expect_tx(&sm->b_full[s2], kps * rows * 128);
             for (int j = 0; j < kps; ++j)
               tma_load_2d(sm->b[s2] + j * rows * 128, &p.map_b[bi], (k0 + j) * BK, brow,
                           &sm->b_full[s2]);
@@ -492,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         const int ncols = p.planes * tl.nvalid;
         const uint32_t idesc = idesc_bf16(BM, (ncols + 15) & ~15);
         const int bi = box_index(ncols);
-        const int kps_m1 = (kSlotRows >> 5 >> bi) - 1;          // K blocks per slot - 1
-        const uint32_t jj_desc = (uint32_t)((32 << bi) * 128) >> 4;
+        const int kps_m1 = box_kps(bi) - 1;                     // K blocks per slot - 1
+        const uint32_t jj_desc = (uint32_t)(box_rows(bi) * 128) >> 4;
         const uint32_t dacc = tmem + buf * BN;
         const int nkb = tl.K / BK;
         int jj = 0;
@@ -1185,8 +1190,8 @@ cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *ou
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
-  for (int i = 0; i < 3; ++i)
-    ok = ok && make_map(&p.map_b[i], w.xe, BF, 2, H, (uint64_t)2 * rows_x, H, BK, 32u << i);
+  for (int i = 0; i < 4; ++i)
+    ok = ok && make_map(&p.map_b[i], w.xe, BF, 2, H, (uint64_t)2 * rows_x, H, BK, kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
                       RK / 64, BM, false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
@@ -1221,9 +1226,9 @@ cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *ou
   ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 4; ++i)
     ok = ok && make_map(&p.map_b[i], w.he, BF, 2, h_stride, (uint64_t)2 * rows_x, h_stride, BK,
-                        32u << i);
+                        kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
                       false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
@@ -1280,8 +1285,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
-  for (int i = 0; i < 3; ++i)
-    ok = ok && make_map(&p.map_b[i], w.xp, BF, 2, H, (uint64_t)maxR, H, BK, 32u << i);
+  for (int i = 0; i < 4; ++i)
+    ok = ok && make_map(&p.map_b[i], w.xp, BF, 2, H, (uint64_t)maxR, H, BK, kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
                       RK / 64, BM, false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
@@ -1316,9 +1321,9 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 4; ++i)
     ok = ok && make_map(&p.map_b[i], w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK,
-                        32u << i);
+                        kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
                       false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,

@@ -15,7 +15,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
-constexpr int kTileTokens = 128;      // tokens per tensor-core tile (the MMA's N)
+constexpr int kTileTokens = 160;      // tokens per tensor-core tile (the MMA's N)
 constexpr int kExactTokens = 8;       // largest batch of the exact (f32-accumulate) tensor-core mode
 
 // Device status word codes (sticky until the next forward overwrites them).
