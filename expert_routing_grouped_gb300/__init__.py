@@ -12,7 +12,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_DEVICE, MOE_ERR_ARG = 0, -1, -2, -3, -4
-MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE = 1, 2, 3
+MOE_ERR_IO, MOE_ERR_ENGINE = -5, -6
+MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE, MOE_OPT_USAGE = 1, 2, 3, 4
 REGIME_AUTO, REGIME_GEMV, REGIME_TC, REGIME_TC_EXACT = 0, 1, 2, 3
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 X_F32, X_BF16 = 0, 1
@@ -22,7 +23,8 @@ MOE_DBG_IDX, MOE_DBG_W, MOE_DBG_COUNTS, MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_I
 EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual", "moe_forward_host",
            "moe_rmsnorm_bf16", "moe_set_option", "moe_debug_view", "moe_debug_read",
            "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror",
-           "moe_route_noalloc")
+           "moe_route_noalloc", "moe_usage_read", "moe_usage_reset", "moe_engine_id",
+           "moe_route_trace_write", "moe_route_trace_read")
 
 
 class MoeLayout(ctypes.Structure):
@@ -69,6 +71,11 @@ def _load():
         "moe_free": (None, [P]),
         "moe_strerror": (ctypes.c_char_p, [i]),
         "moe_route_noalloc": (i, [P, i, i, i, i, i, i, f, P, P, P, P, P]),
+        "moe_usage_read": (i, [P, P, i]),
+        "moe_usage_reset": (i, [P]),
+        "moe_engine_id": (ctypes.c_uint32, [ctypes.c_char_p]),
+        "moe_route_trace_write": (i, [ctypes.c_char_p, i, i, ctypes.c_uint32, P]),
+        "moe_route_trace_read": (i, [ctypes.c_char_p, i, i, ctypes.c_uint32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +180,17 @@ class MoELayer:
     def device_bytes(self):
         return lib.moe_device_bytes(self._handle)
 
+    def usage(self):
+        """numpy int64 [E]: assignments per expert over the forwards counted
+        since init or the last reset (needs MOE_OPT_USAGE = 1)."""
+        import numpy as np
+        a = np.zeros(self.layout.num_experts, np.int64)
+        _check(lib.moe_usage_read(self._handle, a.ctypes.data, a.size), "moe_usage_read")
+        return a
+
+    def usage_reset(self):
+        return _check(lib.moe_usage_reset(self._handle), "moe_usage_reset")
+
     def close(self):
         if self._handle:
             lib.moe_free(self._handle)
@@ -204,3 +222,32 @@ def route_noalloc(x, T, hidden, num_experts, top_k, x_dtype, router_mode, rsf, r
     return _check(lib.moe_route_noalloc(_ptr(x), T, hidden, num_experts, top_k, x_dtype,
                                         router_mode, rsf, _ptr(router_w_eh), _ptr(router_bias),
                                         _ptr(idx), _ptr(w), _stream(stream)), "moe_route_noalloc")
+
+
+def engine_id(name):
+    """FNV-1a 32-bit id of an engine name (moe_engine_id)."""
+    return lib.moe_engine_id(name.encode())
+
+
+def route_trace_write(path, counts, engine):
+    """Writes counts (int64 [n_layers][n_experts]) as a route_trace usage
+    history; engine is a name or a 32-bit id."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    if c.ndim != 2:
+        raise ValueError("counts must be [n_layers][n_experts]")
+    eid = engine_id(engine) if isinstance(engine, str) else int(engine)
+    return _check(lib.moe_route_trace_write(os.fsencode(path), c.shape[0], c.shape[1], eid,
+                                            c.ctypes.data), "moe_route_trace_write")
+
+
+def route_trace_read(path, n_layers, n_experts, engine=0):
+    """Reads a route_trace usage history: (counts int64 [n_layers][n_experts],
+    engine id found in the file, 0 if none).  engine 0 accepts any writer."""
+    import numpy as np
+    c = np.zeros((n_layers, n_experts), np.int64)
+    found = ctypes.c_uint32()
+    eid = engine_id(engine) if isinstance(engine, str) else int(engine)
+    _check(lib.moe_route_trace_read(os.fsencode(path), n_layers, n_experts, eid, c.ctypes.data,
+                                    ctypes.byref(found)), "moe_route_trace_read")
+    return c, found.value

@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
     const int32_t *__restrict__ idx, int T, int k, int E, int n_shared, int tile_m,
     int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
     int32_t *__restrict__ inv, int32_t *__restrict__ active, int32_t *__restrict__ n_active,
-    int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles, int32_t *__restrict__ status) {
+    int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles, int32_t *__restrict__ status,
+    unsigned long long *__restrict__ usage) {
   extern __shared__ int smem[];
   int *cnt = smem;                 // [E]
   int *base = cnt + E;             // [E]
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
     counts[tid] = c;
     offsets[tid] = off;
     base[tid] = off;
+    if (usage && c) usage[tid] += (unsigned long long)c;   // one writer per expert
   }
   if (tid == 0) offsets[E] = total;
   __syncthreads();
@@ -161,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
 
 }  // namespace
 
-cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t st) {
+cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned long long *usage,
+                            cudaStream_t st) {
   const size_t smem = (size_t)(2 + 32) * h->E * sizeof(int);
   static bool attr_set = false;   // per process; the attribute is per function
   if (!attr_set) {
@@ -174,7 +177,7 @@ cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t
   const moe::Workspace &w = h->ws;
   dispatch_kernel<<<1, kThreads, smem, st>>>(w.idx, T, h->k, h->E, h->S, tile_m, w.counts,
                                              w.offsets, w.perm, w.inv, w.active, w.n_active,
-                                             w.tiles, w.n_tiles, w.status);
+                                             w.tiles, w.n_tiles, w.status, usage);
   return cudaGetLastError();
 }
 

@@ -98,6 +98,7 @@ void carve(moe_handle *h, Carver &c) {
   w.n_tiles = c.take<int32_t>(2);
   w.status = c.take<int32_t>(1);
   w.ticket = c.take<int32_t>(1);
+  w.usage = c.take<unsigned long long>(E);
   w.h = c.take<float>(rows * Imax);
   w.hb = c.take<__nv_bfloat16>(rows * Imax);
   w.y = c.take<float>(rows * H);
@@ -212,12 +213,13 @@ void mark(moe_handle *h, const char *name, cudaStream_t st) {
 int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate,
                 cudaStream_t st) {
   int regime = choose_regime(h, T);
+  unsigned long long *usage = h->count_usage ? h->ws.usage : nullptr;
   h->n_ev = 0;
   cudaError_t err = cudaSuccess;
   mark(h, nullptr, st);
   if (T <= moe::kGemvTokens) {
     // One launch routes and groups (and clears the status word).
-    err = moe::launch_route_small(h, x, T, st);
+    err = moe::launch_route_small(h, x, T, usage, st);
     h->launches += 1;
     mark(h, "route", st);
   } else {
@@ -225,7 +227,7 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
     if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
     h->launches += 2;
     mark(h, "router", st);
-    if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
+    if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, usage, st);
     h->launches += 1;
     mark(h, "dispatch", st);
   }
@@ -304,7 +306,8 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   carve(h, c);
   rc = copy_weights(h, weights);
   if (rc == MOE_OK && (cudaMemset(h->ws.status, 0, 4) != cudaSuccess ||
-                       cudaMemset(h->ws.ticket, 0, 4) != cudaSuccess))
+                       cudaMemset(h->ws.ticket, 0, 4) != cudaSuccess ||
+                       cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess))
     rc = MOE_ERR_DEVICE;
   if (rc != MOE_OK) {
     cudaFree(h->pool);
@@ -329,7 +332,7 @@ __attribute__((visibility("default"))) int moe_route(moe_handle *h, const void *
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err = cudaMemsetAsync(h->ws.status, 0, sizeof(int32_t), st);
   if (err == cudaSuccess) err = moe::launch_router(h, x, T, st);
-  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, st);
+  if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, nullptr, st);
   h->last_T = T;
   h->last_regime = 0;
   h->last_stream = st;
@@ -395,7 +398,30 @@ __attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int opt
     h->n_ev = 0;
     return MOE_OK;
   }
+  if (option == MOE_OPT_USAGE) {
+    if (value != 0 && value != 1) return MOE_ERR_ARG;
+    h->count_usage = value;
+    return MOE_OK;
+  }
   return MOE_ERR_ARG;
+}
+
+__attribute__((visibility("default"))) int moe_usage_read(moe_handle *h, int64_t *host_counts,
+                                                          int n_experts) {
+  if (!h || !host_counts || n_experts != h->E) return MOE_ERR_ARG;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
+      cudaMemcpy(host_counts, h->ws.usage, (size_t)h->E * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_usage_reset(moe_handle *h) {
+  if (!h) return MOE_ERR_ARG;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess ||
+      cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
 }
 
 __attribute__((visibility("default"))) int moe_debug_view(moe_handle *h, moe_debug *d) {
@@ -477,6 +503,8 @@ __attribute__((visibility("default"))) const char *moe_strerror(int code) {
     case MOE_ERR_ROUTING: return "invalid routing layout";
     case MOE_ERR_DEVICE: return "CUDA error or device status";
     case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_IO: return "usage-history file error";
+    case MOE_ERR_ENGINE: return "usage history of another engine or shape";
     default: return "unknown error";
   }
 }

@@ -51,6 +51,7 @@ struct Workspace {
   int32_t *n_tiles;   // [2] tile count for W13 and W2 kernels
   int32_t *status;    // [1]
   int32_t *ticket;    // [1] last-CTA-done counter of the fused small-T routing (self-resetting)
+  unsigned long long *usage;  // [E] assignments per expert over the counted forwards
   // expert activations
   float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
   __nv_bfloat16 *hb;  // [max_tokens*k + S*max_tokens][I_max] bf16 (tensor-core path)
@@ -82,6 +83,7 @@ struct moe_handle {
   size_t pool_bytes;
   int regime_opt;                // MOE_OPT_REGIME
   int small_t_max;               // MOE_OPT_SMALL_T_MAX
+  int count_usage;               // MOE_OPT_USAGE
   int last_T;
   int last_regime;
   cudaStream_t last_stream;
@@ -99,10 +101,13 @@ namespace moe {
 
 // router.cu
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t s);
-// T <= 4: router, top-k and dispatch in one launch (also clears the status word)
-cudaError_t launch_route_small(const moe_handle *h, const void *x, int T, cudaStream_t s);
+// T <= 4: router, top-k and dispatch in one launch (also clears the status word).
+// usage (nullable): [E] counters the per-expert counts are added into.
+cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
+                               unsigned long long *usage, cudaStream_t s);
 // dispatch.cu
-cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, cudaStream_t s);
+cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned long long *usage,
+                            cudaStream_t s);
 // gemv.cu
 cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t s);
 cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t s);

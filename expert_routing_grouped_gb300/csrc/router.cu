@@ -309,7 +309,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(
     int32_t *__restrict__ idx, float *__restrict__ w, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
     int32_t *__restrict__ active, int32_t *__restrict__ n_active, int32_t *__restrict__ tiles,
-    int32_t *__restrict__ n_tiles, int32_t *__restrict__ status) {
+    int32_t *__restrict__ n_tiles, int32_t *__restrict__ status,
+    unsigned long long *__restrict__ usage) {
   extern __shared__ float xs[];   // [4][h_per_split]
   __shared__ int last;
   const int split = blockIdx.y;
@@ -379,6 +380,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
     const int ee = e0 + i;
     if (ee < E) {
       counts[ee] = cnt[ee];
+      if (usage && cnt[ee]) usage[ee] += (unsigned long long)cnt[ee];
       offsets[ee] = pos;
       base[ee] = pos;
       pos += cnt[ee];
@@ -455,7 +457,8 @@ int router_splits(int T, int E, int H, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_route_small(const moe_handle *h, const void *x, int T, cudaStream_t st) {
+cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
+                               unsigned long long *usage, cudaStream_t st) {
   const int E = h->E, H = h->H, k = h->k;
   const int splits = router_splits(T, E, H, h->num_sms);
   const int hps = H / splits;
@@ -474,7 +477,7 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T, cudaSt
     route_small_kernel<N><<<grid, 256, smem, st>>>(                                             \
         x, h->L.x_dtype == 1, T, H, E, k, h->L.router_mode, h->wr_t, h->bias,                   \
         h->L.routed_scaling_factor, hps, w.z_part, w.ticket, h->S, w.idx, w.w, w.counts,        \
-        w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status);          \
+        w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);   \
   } while (0)
   if (epl <= 1) MOE_RS(1);
   else if (epl <= 2) MOE_RS(2);

@@ -67,6 +67,10 @@ extern "C" {
 #define MOE_ERR_DEVICE (-3)   /* CUDA error, or a nonzero device status word     */
 #define MOE_ERR_ARG (-4)      /* NULL pointer, a size not a multiple of 64,
                                  unsupported dtype, bad option                  */
+#define MOE_ERR_IO (-5)       /* a usage-history file could not be opened,
+                                 written or parsed                              */
+#define MOE_ERR_ENGINE (-6)   /* a usage history written by another engine, or
+                                 for other dimensions                           */
 
 /* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st *moe_stream_t;
@@ -176,6 +180,11 @@ int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
 /* 1: record a CUDA event on the forward's stream at every stage boundary
  * (read the stage times with moe_stage_times); 0 (default): no events. */
 #define MOE_OPT_PROFILE 3
+/* 1: every moe_forward / moe_forward_residual / moe_forward_host call adds its
+ * per-expert assignment counts into the handle's 64-bit usage counters (read
+ * them with moe_usage_read); the dispatch kernel does the adding, so the option
+ * costs no launch.  moe_route (a look-ahead) never counts.  0 (default): off. */
+#define MOE_OPT_USAGE 4
 int moe_set_option(moe_handle *h, int option, int value);
 
 /* Fills *d with device pointers describing the last forward call. */
@@ -239,6 +248,60 @@ int moe_stage_times(moe_handle *h, float *ms, const char **names, int max, int *
 /* Synchronises the handle's last stream and returns its device status word
  * (0 when every kernel completed normally). */
 int moe_status(moe_handle *h, int32_t *status);
+
+/*
+ * Expert usage history (colibri tuning guide, gitcode.com, "learned cache":
+ * the engine records which experts each layer actually routed to and pins the
+ * hottest; "usage-history format": route_trace.h).
+ *
+ * moe_usage_read synchronises the handle's last stream and copies its usage
+ * counters, int64 [num_experts] (assignments per expert summed over the
+ * counted forwards since init or the last reset), into host memory;
+ * n_experts must equal the layout's.  moe_usage_reset synchronises and zeroes
+ * them.  Both return MOE_OK, MOE_ERR_ARG or MOE_ERR_DEVICE.
+ */
+int moe_usage_read(moe_handle *h, int64_t *host_counts, int n_experts);
+int moe_usage_reset(moe_handle *h);
+
+/* Engine identity of a usage history: the FNV-1a 32-bit hash of the engine's
+ * name (offset basis 2166136261, prime 16777619, one byte at a time).  The
+ * tuning guide gives one value: "glm_moe_dsa" -> 3815245270.  NULL -> 0. */
+uint32_t moe_engine_id(const char *name);
+
+/*
+ * Writes a usage history in the route_trace text format (colibri tuning guide,
+ * "usage-history format"): plain text, one record per line, each record
+ * exactly three decimal integers separated by single spaces:
+ *   -1 n_layers n_experts            header: dimensions
+ *   -2 1 engine_id                   header: format version 1, engine id
+ *   layer expert count               one per non-zero count, layer-major,
+ *                                    experts ascending
+ * Only non-zero counts are written.  A history with no non-zero count is a
+ * zero-byte file (no header either), so that a reader can tell "nothing
+ * recorded" from the file's size.  counts is host memory, int64
+ * [n_layers][n_experts], every value >= 0.  The file is created or truncated.
+ * Returns MOE_OK, MOE_ERR_ARG (NULL, n_layers < 1, n_experts < 1, a negative
+ * count) or MOE_ERR_IO.
+ */
+int moe_route_trace_write(const char *path, int n_layers, int n_experts, uint32_t engine_id,
+                          const int64_t *counts);
+
+/*
+ * Reads a route_trace file and ADDS its counts into counts (host, int64
+ * [n_layers][n_experts]; the caller zeroes it first for a plain read).
+ * Records whose first field is negative are headers: -1 must carry these
+ * dimensions, -2 this engine_id (else MOE_ERR_ENGINE and counts is left as it
+ * was); other negative record types are skipped, so that later header types
+ * stay readable.  engine_id 0 accepts a history from any engine (the guide
+ * trusts a file the user names explicitly, and checks one the engine found by
+ * itself); the dimensions are checked either way.  A file with no header (the older headerless form) is
+ * accepted as it stands.  A zero-byte file is an empty history: MOE_OK, no
+ * change.  A record without exactly three integer fields, or with a layer or
+ * expert out of range or a negative count, is MOE_ERR_IO (counts unchanged).
+ * *found_engine (optional) receives the -2 record's engine id, 0 if none.
+ */
+int moe_route_trace_read(const char *path, int n_layers, int n_experts, uint32_t engine_id,
+                         int64_t *counts, uint32_t *found_engine);
 
 /* Bytes of device memory the handle owns (weights + workspace). */
 size_t moe_device_bytes(const moe_handle *h);

@@ -83,6 +83,8 @@ def test_null_handle_calls():
     assert moe.lib.moe_set_option(None, 1, 0) == -4
     assert moe.lib.moe_debug_view(None, None) == -4
     assert moe.lib.moe_device_bytes(None) == 0
+    assert moe.lib.moe_usage_read(None, None, 8) == -4
+    assert moe.lib.moe_usage_reset(None) == -4
     moe.lib.moe_free(None)
     assert moe.lib.moe_rmsnorm_bf16(None, 0, 64, 1e-6, None, None) == 0     # dry run
     assert moe.lib.moe_rmsnorm_bf16(None, 2, 64, 1e-6, None, None) == -4
@@ -93,3 +95,5 @@ def test_strerror():
     assert moe.lib.moe_strerror(0) == b"ok"
     assert b"max_tokens" in moe.lib.moe_strerror(-1)
     assert moe.lib.moe_strerror(-2) == b"invalid routing layout"
+    assert b"usage-history" in moe.lib.moe_strerror(-5)
+    assert b"another engine" in moe.lib.moe_strerror(-6)

@@ -328,3 +328,46 @@ def test_tc_and_gemv_agree(dev):
     g = out.cpu().numpy()
     assert rel_l2(g, ref["out"]) <= GEMV_TOL
     assert rel_l2(got_tc, g) <= TC_TOL
+
+
+def test_usage_counters(dev):
+    """MOE_OPT_USAGE: the dispatch kernels add each counted forward's
+    per-expert assignment counts (the oracle's counting-sort counts) into the
+    handle's 64-bit counters, on both the fused small-T routing and the
+    separate dispatch kernel; moe_route, a look-ahead, does not count; the
+    counters written as a route_trace file read back unchanged."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["olmoe"]
+    h, Wr, bias = get_layer(wl, 64, dev)
+    L = oracle.layout(wl)
+    W = oracle.weights(L, Wr, bias)
+    h.usage_reset()
+    assert not h.usage().any()
+    h.set_option(moe.MOE_OPT_USAGE, 1)
+    expect = np.zeros(wl.E, np.int64)
+    for T in (1, 3, 4, 5, 37, 64):
+        x, _ = margin_x(wl, T, Wr, bias)
+        idx, _, _, _ = oracle.route(L, W, x)
+        expect += oracle.dispatch(idx, wl.E)[0]
+        out = torch.empty(T, wl.H, device=dev)
+        h.forward(to_device_x(wl, x, dev), T, out)
+        h.route(to_device_x(wl, x, dev), T)          # not counted
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    got = h.usage()
+    assert np.array_equal(got, expect)
+    assert got.sum() == (1 + 3 + 4 + 5 + 37 + 64) * wl.k
+    h.set_option(moe.MOE_OPT_USAGE, 0)
+    x, _ = margin_x(wl, 8, Wr, bias)
+    out = torch.empty(8, wl.H, device=dev)
+    h.forward(to_device_x(wl, x, dev), 8, out)
+    assert np.array_equal(h.usage(), expect)        # off: unchanged
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        p = os.path.join(d, "usage")
+        moe.route_trace_write(p, got[None, :], "olmoe")
+        back, found = moe.route_trace_read(p, 1, wl.E, "olmoe")
+    assert found == moe.engine_id("olmoe") and np.array_equal(back[0], expect)
+    h.usage_reset()
+    assert not h.usage().any()
