@@ -17,7 +17,8 @@ class Layout(ctypes.Structure):
                 ("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("shared_intermediate", ctypes.c_int32),
                 ("router_mode", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
-                ("routed_scaling_factor", ctypes.c_double)]
+                ("routed_scaling_factor", ctypes.c_double), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("top_p", ctypes.c_double)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -68,7 +69,8 @@ def layout(wl=None, **kw):
         kw = dict(num_experts=wl.E, top_k=wl.k, hidden=wl.H, intermediate=wl.I,
                   n_shared=wl.n_shared, shared_intermediate=wl.I_shared,
                   router_mode=wl.router_mode, x_dtype=wl.x_dtype,
-                  routed_scaling_factor=wl.rsf) | kw
+                  routed_scaling_factor=wl.rsf, n_group=wl.n_group,
+                  topk_group=wl.topk_group, top_p=wl.top_p) | kw
     return Layout(**kw)
 
 

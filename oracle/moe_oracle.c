@@ -33,7 +33,14 @@ static double x_at(const oracle_layout *L, const void *x, int t, int h) {
 static int check_layout(const oracle_layout *L) {
   if (!L) return -4;
   if (L->num_experts < 1 || L->top_k < 1 || L->top_k > L->num_experts) return -2;
-  if (L->router_mode != 0 && L->router_mode != 1) return -2;
+  if (L->router_mode < 0 || L->router_mode > 2) return -2;
+  if (L->n_group < 0 || !(L->top_p >= 0.0)) return -2;
+  if (L->n_group > 1) {
+    const int gsize = L->num_experts / L->n_group;
+    if (L->router_mode != 1 || L->num_experts % L->n_group || gsize < 2) return -2;
+    if (L->topk_group < 1 || L->topk_group > L->n_group) return -2;
+    if (L->top_k > L->topk_group * gsize) return -2;
+  }
   if (L->hidden <= 0 || L->intermediate <= 0) return -4;
   if (L->hidden % 64 || L->intermediate % 64) return -4;
   if (L->n_shared != 0 && L->n_shared != 1) return -4;
@@ -86,17 +93,33 @@ static int keyed_cmp(const void *a, const void *b) {
 }
 
 /*
- * Softmax mode (tutorial cf-1.com §2.1 step 2: "linear layer + softmax ->
+ * Softmax modes (tutorial cf-1.com §2.1 step 2: "linear layer + softmax ->
  * top-2 ids and weights"): logits l = z + b (b an additive logit bias, zero
  * when absent); p = softmax(l) over all E; select the k largest (softmax is
- * monotone, so the key is l itself); w_j = p[idx_j] / sum_sel p * rsf.
- * Reading: the selected weights are renormalised in both modes.
+ * monotone, so the key is l itself).  Mode 0: w_j = p[idx_j] / sum_sel p * rsf
+ * (Reading: renormalised over the selection).  Mode 2: w_j = p[idx_j] * rsf,
+ * the unrenormalised variant.
  *
- * Sigmoid + noaux_tc, n_group = 1 (teardown "Three key engineering decisions"
- * (1)): s = sigmoid(z); key = s + b (the selection bias enters selection
- * only); select the k largest keys; w_j = s[idx_j] / sum_sel s * rsf.
- * Reading: with one group, group-limited selection is the identity.
+ * Sigmoid + noaux_tc (teardown "Three key engineering decisions" (1)):
+ * s = sigmoid(z); key = s + b (the selection bias enters selection only);
+ * select the k largest keys; w_j = s[idx_j] / sum_sel s * rsf.  With
+ * n_group <= 1 every expert is eligible.  With n_group > 1 (Reading: the
+ * published group-limited noaux_tc): the experts form n_group contiguous groups
+ * of E / n_group; a group's score is the sum of its two largest keys; the
+ * topk_group groups with the largest scores (ties to the lower group) stay
+ * eligible, and the k experts are chosen among their members only.
+ *
+ * Adaptive expert top-p (colibri tuning guide, gitcode.com, knob table:
+ * "--topp", a lossy trim of the expert set).  Reading: with the slots in
+ * selection order and q_j = (slot j's weight before rsf) / (sum over the
+ * selection), slot j is kept while the cumulative share of the slots before
+ * it, C_j = q_0 + ... + q_{j-1}, is below top_p (slot 0 always).  Dropped
+ * slots get id -1 and weight 0.  Modes 0 and 1 renormalise the kept weights
+ * over the kept slots; mode 2 keeps its unrenormalised weights.
  */
+static int groups_on(const oracle_layout *L) { return L->n_group > 1; }
+static int top_p_on(const oracle_layout *L) { return L->top_p > 0.0 && L->top_p < 1.0; }
+
 OR_API int oracle_route_from_logits(const oracle_layout *L, const float *router_bias,
                                     const double *z, int T, int32_t *idx, double *w,
                                     double *key, double *gap) {
@@ -105,58 +128,117 @@ OR_API int oracle_route_from_logits(const oracle_layout *L, const float *router_
   if (T < 0 || (T > 0 && (!z || !idx || !w))) return -4;
   if (L->router_mode == 1 && !router_bias) return -4;
   const int E = L->num_experts, k = L->top_k;
+  const int G = groups_on(L) ? L->n_group : 1, gsize = E / G;
   keyed *ks = (keyed *)malloc(sizeof(keyed) * (size_t)E);
+  keyed *gs = (keyed *)malloc(sizeof(keyed) * (size_t)G);
   double *val = (double *)malloc(sizeof(double) * (size_t)E);
-  if (!ks || !val) {
+  int *eligible = (int *)malloc(sizeof(int) * (size_t)E);
+  double *kk = (double *)malloc(sizeof(double) * (size_t)E);   /* keys in expert order */
+  if (!ks || !gs || !val || !eligible || !kk) {
     free(ks);
+    free(gs);
     free(val);
+    free(eligible);
+    free(kk);
     return -1;
   }
   for (int t = 0; t < T; ++t) {
     const double *zt = z + (size_t)t * E;
-    if (L->router_mode == 0) {
+    if (L->router_mode != 1) {
       /* p = softmax(z + b) over all experts. */
       double m = -INFINITY;
       for (int e = 0; e < E; ++e) {
-        double l = zt[e] + (router_bias ? (double)router_bias[e] : 0.0);
-        ks[e].key = l;
-        ks[e].e = e;
-        if (l > m) m = l;
+        kk[e] = zt[e] + (router_bias ? (double)router_bias[e] : 0.0);
+        if (kk[e] > m) m = kk[e];
       }
       double sum = 0.0;
       for (int e = 0; e < E; ++e) {
-        val[e] = exp(ks[e].key - m);
+        val[e] = exp(kk[e] - m);
         sum += val[e];
       }
       for (int e = 0; e < E; ++e) val[e] /= sum;
     } else {
       for (int e = 0; e < E; ++e) {
         val[e] = sigmoid(zt[e]);
-        ks[e].key = val[e] + (double)router_bias[e];
-        ks[e].e = e;
+        kk[e] = val[e] + (double)router_bias[e];
       }
     }
     if (key)
-      for (int e = 0; e < E; ++e) key[(size_t)t * E + e] = ks[e].key;
-    qsort(ks, (size_t)E, sizeof(keyed), keyed_cmp);
+      for (int e = 0; e < E; ++e) key[(size_t)t * E + e] = kk[e];
+    double g = INFINITY;   /* decision margin */
+
+    /* Group-limited eligibility. */
+    for (int e = 0; e < E; ++e) eligible[e] = 1;
+    if (groups_on(L)) {
+      for (int gi = 0; gi < G; ++gi) {
+        for (int j = 0; j < gsize; ++j) {
+          ks[j].key = kk[gi * gsize + j];
+          ks[j].e = gi * gsize + j;
+        }
+        qsort(ks, (size_t)gsize, sizeof(keyed), keyed_cmp);
+        gs[gi].key = ks[0].key + ks[1].key;
+        gs[gi].e = gi;
+      }
+      qsort(gs, (size_t)G, sizeof(keyed), keyed_cmp);
+      for (int e = 0; e < E; ++e) eligible[e] = 0;
+      for (int j = 0; j < L->topk_group; ++j)
+        for (int i = 0; i < gsize; ++i) eligible[gs[j].e * gsize + i] = 1;
+      if (L->topk_group < G) {
+        for (int j = 0; j < L->topk_group; ++j) {
+          const double d = gs[j].key - gs[j + 1].key;
+          if (d < g) g = d;
+        }
+      }
+    }
+
+    /* Top-k over the eligible experts. */
+    int n = 0;
+    for (int e = 0; e < E; ++e)
+      if (eligible[e]) {
+        ks[n].key = kk[e];
+        ks[n].e = e;
+        ++n;
+      }
+    qsort(ks, (size_t)n, sizeof(keyed), keyed_cmp);
+    const int top = (k < n) ? k + 1 : n;
+    for (int j = 0; j + 1 < top; ++j) {
+      const double d = ks[j].key - ks[j + 1].key;
+      if (d < g) g = d;
+    }
+
+    /* Weights, then the top-p trim. */
     double sel = 0.0;
     for (int j = 0; j < k; ++j) sel += val[ks[j].e];
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = ks[j].e;
-      w[(size_t)t * k + j] = val[ks[j].e] / sel * L->routed_scaling_factor;
-    }
-    if (gap) {
-      int top = (k < E) ? k + 1 : E;
-      double g = INFINITY;
-      for (int j = 0; j + 1 < top; ++j) {
-        double d = ks[j].key - ks[j + 1].key;
+    int kept = k;
+    if (top_p_on(L)) {
+      double cum = 0.0;
+      for (int j = 1; j < k; ++j) {
+        cum += val[ks[j - 1].e] / sel;
+        const double d = fabs(cum - L->top_p);
         if (d < g) g = d;
+        if (kept == k && cum >= L->top_p) kept = j;
       }
-      gap[t] = g;
     }
+    double norm = 0.0;
+    for (int j = 0; j < kept; ++j) norm += val[ks[j].e];
+    for (int j = 0; j < k; ++j) {
+      const size_t a = (size_t)t * k + j;
+      if (j >= kept) {
+        idx[a] = -1;
+        w[a] = 0.0;
+      } else {
+        idx[a] = ks[j].e;
+        w[a] = (L->router_mode == 2 ? val[ks[j].e] : val[ks[j].e] / norm) *
+               L->routed_scaling_factor;
+      }
+    }
+    if (gap) gap[t] = g;
   }
   free(ks);
+  free(gs);
   free(val);
+  free(eligible);
+  free(kk);
   return 0;
 }
 
@@ -189,6 +271,7 @@ OR_API int oracle_dispatch(const int32_t *idx, int T, int k, int E, int32_t *cou
   const int A = T * k;
   for (int e = 0; e < E; ++e) counts[e] = 0;
   for (int a = 0; a < A; ++a) {
+    if (idx[a] == -1) continue;   /* a slot dropped by the top-p trim */
     if (idx[a] < 0 || idx[a] >= E) return -2;
     counts[idx[a]] += 1;
   }
@@ -198,6 +281,10 @@ OR_API int oracle_dispatch(const int32_t *idx, int T, int k, int E, int32_t *cou
   if (!fill) return -1;
   for (int a = 0; a < A; ++a) {
     int e = idx[a];
+    if (e == -1) {
+      inv[a] = -1;
+      continue;
+    }
     int pos = offsets[e] + fill[e]++;
     perm[pos] = a;
     inv[a] = pos;
@@ -326,7 +413,7 @@ OR_API int oracle_moe_forward(const oracle_layout *L, const oracle_weights *W,
 
   /* Step 4: gather each expert's group and run its FFN; skip empty experts
    * (tutorial cf-1.com §3.3 Step 4: "if expert_counts[i] == 0, skip"). */
-  for (int p = 0; p < A; ++p) {
+  for (int p = 0; p < offsets[E]; ++p) {   /* the real assignments */
     int t = perm[p] / k;
     for (int c = 0; c < H; ++c) xg[(size_t)p * H + c] = x_at(L, x, t, c);
   }
@@ -360,6 +447,7 @@ OR_API int oracle_moe_forward(const oracle_layout *L, const oracle_weights *W,
       double acc = 0.0;
       for (int j = 0; j < k; ++j) {
         int a = t * k + j;
+        if (inv[a] < 0) continue;   /* dropped by the top-p trim */
         acc += w[a] * yg[(size_t)inv[a] * H + c];
       }
       if (L->n_shared) acc += ys[(size_t)t * H + c];

@@ -52,9 +52,14 @@ typedef struct {
   int32_t intermediate;         /* I (multiple of 64)                     */
   int32_t n_shared;             /* 0 or 1                                 */
   int32_t shared_intermediate;  /* I of the shared expert                 */
-  int32_t router_mode;          /* 0 softmax, 1 sigmoid + noaux_tc        */
+  int32_t router_mode;          /* 0 softmax, 1 sigmoid + noaux_tc,
+                                   2 softmax without renormalisation      */
   int32_t x_dtype;              /* 0 f32, 1 bf16                          */
   double routed_scaling_factor; /* rsf                                    */
+  int32_t n_group;              /* 0 or 1: no groups; > 1: grouped noaux_tc
+                                   (sigmoid mode only), E % n_group == 0   */
+  int32_t topk_group;           /* groups kept when n_group > 1           */
+  double top_p;                 /* adaptive expert top-p; 0 or >= 1: off  */
 } oracle_layout;
 
 typedef struct {
@@ -75,8 +80,12 @@ int oracle_router_logits(const oracle_layout *L, const oracle_weights *W,
                          const void *x, int T, double *z);
 
 /* Steps 1-2: idx[T][k], w[T][k]; key[T][E] and gap[T] optional (may be NULL).
- * gap[t] = smallest difference between adjacent keys among the top-(k+1)
- * sorted keys (among all E when k == E). */
+ * gap[t] is the token's decision margin: the smallest difference between
+ * adjacent keys among the top-(k+1) sorted eligible keys (all of them when
+ * fewer), and, where they apply, between adjacent group scores among the
+ * top-(topk_group+1), and between the top-p threshold and each cumulative
+ * share it is compared with.  With top-p on, a dropped slot holds id -1 and
+ * weight 0. */
 int oracle_route(const oracle_layout *L, const oracle_weights *W, const void *x,
                  int T, int32_t *idx, double *w, double *key, double *gap);
 
@@ -85,7 +94,9 @@ int oracle_route_from_logits(const oracle_layout *L, const float *router_bias,
                              const double *z, int T, int32_t *idx, double *w,
                              double *key, double *gap);
 
-/* Step 3: counts[E], offsets[E+1], perm[T*k], inv[T*k]. */
+/* Step 3: counts[E], offsets[E+1], perm[T*k], inv[T*k].  An id of -1 (a slot
+ * the top-p trim dropped) is no assignment: not counted, inv = -1, and perm
+ * lists only the offsets[E] real assignments. */
 int oracle_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts,
                     int32_t *offsets, int32_t *perm, int32_t *inv);
 

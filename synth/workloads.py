@@ -11,6 +11,7 @@ from typing import Tuple
 
 ROUTER_SOFTMAX = 0
 ROUTER_SIGMOID = 1
+ROUTER_SOFTMAX_RAW = 2      # softmax top-k without renormalisation
 X_F32 = 0
 X_BF16 = 1
 
@@ -34,6 +35,9 @@ class Workload:
     bias_sigma: float = 0.0
     zipf_s: float = 0.0
     router_sigma: float = 0.02
+    n_group: int = 0            # > 1: grouped noaux_tc (sigmoid router)
+    topk_group: int = 0
+    top_p: float = 0.0          # adaptive expert top-p; 0: off
     scale_lo: float = 0.005
     scale_hi: float = 0.02
     notes: str = field(default="", compare=False)
@@ -74,5 +78,27 @@ GLM_PREFILL_SMALL = Workload("glm_prefill_small", H=6144, E=32, k=8, I=2048, n_s
                              tokens=(2048,), seed=6, bias="normal", bias_sigma=0.1,
                              notes="GLM-shaped layer with 32 experts, for kernel profiles")
 
-ALL = (TINY, OLMOE, MIXTRAL, GLM_DECODE, GLM_PREFILL, GLM_PREFILL_SMALL)
+# Router variants (the same shapes, other selection rules).
+TINY_GROUPED = Workload("tiny_grouped", H=512, E=8, k=2, I=1024, n_shared=0, I_shared=0,
+                        router_mode=ROUTER_SIGMOID, rsf=2.5, x_dtype=X_F32, tokens=(16,),
+                        seed=10, bias="normal", bias_sigma=0.1, n_group=4, topk_group=2,
+                        notes="tiny sigmoid layer, 4 groups of 2 experts, 2 groups kept")
+TINY_TOPP = Workload("tiny_topp", H=512, E=8, k=4, I=1024, n_shared=0, I_shared=0,
+                     router_mode=ROUTER_SOFTMAX, rsf=1.0, x_dtype=X_F32, tokens=(16,), seed=11,
+                     top_p=0.6, notes="tiny softmax layer with adaptive top-p 0.6")
+OLMOE_RAW = Workload("olmoe_raw", H=2048, E=64, k=8, I=1024, n_shared=0, I_shared=0,
+                     router_mode=ROUTER_SOFTMAX_RAW, rsf=1.0, x_dtype=X_BF16, tokens=(1, 64),
+                     seed=12, bias="normal", bias_sigma=0.5,
+                     notes="OLMoE-shaped, softmax top-k weights left unrenormalised")
+GLM_GROUPED = Workload("glm_grouped", H=6144, E=256, k=8, I=2048, n_shared=1, I_shared=2048,
+                       router_mode=ROUTER_SIGMOID, rsf=2.5, x_dtype=X_BF16, tokens=(1, 4, 512),
+                       seed=13, bias="normal", bias_sigma=0.1, n_group=8, topk_group=4,
+                       notes="GLM-shaped layer, grouped noaux_tc: 8 groups of 32, 4 kept")
+GLM_TOPP = Workload("glm_topp", H=6144, E=256, k=8, I=2048, n_shared=1, I_shared=2048,
+                    router_mode=ROUTER_SIGMOID, rsf=2.5, x_dtype=X_BF16, tokens=(1, 4, 512),
+                    seed=14, bias="normal", bias_sigma=0.1, top_p=0.7,
+                    notes="GLM-shaped layer with adaptive expert top-p 0.7")
+
+ALL = (TINY, OLMOE, MIXTRAL, GLM_DECODE, GLM_PREFILL, GLM_PREFILL_SMALL, TINY_GROUPED,
+       TINY_TOPP, OLMOE_RAW, GLM_GROUPED, GLM_TOPP)
 BY_NAME = {w.name: w for w in ALL}
