@@ -15,7 +15,7 @@ MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_DEVICE, MOE_ERR_ARG = 0, -1, -2,
 MOE_ERR_IO, MOE_ERR_ENGINE = -5, -6
 MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE, MOE_OPT_USAGE = 1, 2, 3, 4
 REGIME_AUTO, REGIME_GEMV, REGIME_TC, REGIME_TC_EXACT = 0, 1, 2, 3
-ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+ROUTER_SOFTMAX, ROUTER_SIGMOID, ROUTER_SOFTMAX_RAW = 0, 1, 2
 X_F32, X_BF16 = 0, 1
 
 MOE_DBG_IDX, MOE_DBG_W, MOE_DBG_COUNTS, MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV = range(6)
@@ -32,7 +32,9 @@ class MoeLayout(ctypes.Structure):
                 ("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("shared_intermediate", ctypes.c_int32),
                 ("router_mode", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
-                ("x_dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32)]
+                ("x_dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("top_p", ctypes.c_float)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -213,7 +215,8 @@ def layout_for(wl, max_tokens):
     return MoeLayout(num_experts=wl.E, top_k=wl.k, hidden=wl.H, intermediate=wl.I,
                      n_shared=wl.n_shared, shared_intermediate=wl.I_shared,
                      router_mode=wl.router_mode, routed_scaling_factor=wl.rsf,
-                     x_dtype=wl.x_dtype, max_tokens=max_tokens)
+                     x_dtype=wl.x_dtype, max_tokens=max_tokens, n_group=wl.n_group,
+                     topk_group=wl.topk_group, top_p=wl.top_p)
 
 
 def route_noalloc(x, T, hidden, num_experts, top_k, x_dtype, router_mode, rsf, router_w_eh,

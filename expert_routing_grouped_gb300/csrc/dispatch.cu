@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
   int bad = 0;
   for (int a = tid; a < A; a += kThreads) {
     const int e = idx[a];
+    if (e == -1) continue;   // a slot the top-p trim dropped: no assignment
     if (e < 0 || e >= E) {
       bad = 1;
       continue;
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
   for (int c0 = 0; c0 < A; c0 += kThreads) {
     const int a = c0 + tid;
     int e = (a < A) ? idx[a] : E;
-    if (e < 0 || e >= E) e = E;                  // invalid ids are not placed
+    if (e < 0 || e >= E) e = E;                  // dropped or invalid ids are not placed
+    if (a < A && e == E) inv[a] = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     if (e < E && (peers & lt_mask) == 0) wc[warp * E + e] = __popc(peers);

@@ -760,13 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x, int x_is_bf16,
                                                      int T, int H, int k, int n_shared,
                                                      const int32_t *__restrict__ perm,
+                                                     const int32_t *__restrict__ n_assigned,
                                                      const float *__restrict__ w,
                                                      __nv_bfloat16 *__restrict__ xp,
                                                      float *__restrict__ wperm) {
   const int A = T * k, R = A + n_shared * T;
+  const int n_routed = __ldg(n_assigned);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   for (int pr = warp; pr < R; pr += nwarps) {
+    if (pr >= n_routed && pr < A) continue;   // rows of slots the top-p trim dropped
     int t;
     float wt;
     if (pr < A) {
@@ -802,13 +805,16 @@ __global__ void __launch_bounds__(256) gather_exact_kernel(const void *__restric
                                                            int x_is_bf16, int T, int H, int k,
                                                            int n_shared,
                                                            const int32_t *__restrict__ perm,
+                                                           const int32_t *__restrict__ n_assigned,
                                                            const float *__restrict__ w,
                                                            __nv_bfloat16 *__restrict__ xe,
                                                            float *__restrict__ wperm) {
   const int A = T * k, R = A + n_shared * T;
+  const int n_routed = __ldg(n_assigned);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   for (int pr = warp; pr < R; pr += nwarps) {
+    if (pr >= n_routed && pr < A) continue;   // rows of slots the top-p trim dropped
     int t;
     float wt;
     if (pr < A) {
@@ -856,7 +862,9 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
     const int t = (int)(i / per_t), c = (int)(i - (long long)t * per_t);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)inv[t * k + j] * H) + c);
+      const int row = __ldg(inv + t * k + j);
+      if (row < 0) continue;   // a slot the top-p trim dropped
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)row * H) + c);
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -1174,7 +1182,8 @@ cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *ou
   cudaError_t err = set_tc_attrs();
   if (err != cudaSuccess) return err;
   moe_handle *hm = const_cast<moe_handle *>(h);
-  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm, w.w,
+  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm,
+                                                  w.offsets + h->E, w.w,
                                                   w.xe, w.wperm);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   hm->launches += 1;
@@ -1266,7 +1275,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   const int h_stride = I > Is ? I : Is;
   cudaError_t err = set_tc_attrs();
   if (err != cudaSuccess) return err;
-  gather_kernel<<<h->num_sms * 4, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm, w.w,
+  gather_kernel<<<h->num_sms * 4, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm,
+                                                w.offsets + h->E, w.w,
                                                 w.xp, w.wperm);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

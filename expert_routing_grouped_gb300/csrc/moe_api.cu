@@ -35,7 +35,14 @@ int validate_layout(const moe_layout *L) {
   if (!L) return MOE_ERR_ARG;
   if (L->num_experts < 1 || L->num_experts > moe::kMaxExperts) return MOE_ERR_ROUTING;
   if (L->top_k < 1 || L->top_k > L->num_experts || L->top_k > moe::kMaxTopK) return MOE_ERR_ROUTING;
-  if (L->router_mode != 0 && L->router_mode != 1) return MOE_ERR_ROUTING;
+  if (L->router_mode < 0 || L->router_mode > 2) return MOE_ERR_ROUTING;
+  if (L->n_group < 0 || L->n_group > 32 || !(L->top_p >= 0.f)) return MOE_ERR_ROUTING;
+  if (L->n_group > 1) {
+    const int gsz = L->num_experts / L->n_group;
+    if (L->router_mode != 1 || L->num_experts % L->n_group || gsz < 2 || L->topk_group < 1 ||
+        L->topk_group > L->n_group || L->top_k > L->topk_group * gsz)
+      return MOE_ERR_ROUTING;
+  }
   if (!(L->routed_scaling_factor > 0.f)) return MOE_ERR_ROUTING;
   if (L->hidden < 512 || L->hidden % 512) return MOE_ERR_ARG;
   if (L->intermediate < 1024 || L->intermediate % 1024) return MOE_ERR_ARG;

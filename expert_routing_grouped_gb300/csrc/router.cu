@@ -19,6 +19,20 @@
 namespace moe {
 namespace {
 
+// The router's selection rule, passed to the kernels by value.
+struct RouteRule {
+  int mode;         // 0 softmax, 1 sigmoid + noaux_tc, 2 softmax without renormalisation
+  int n_group;      // > 1: group-limited selection (mode 1)
+  int topk_group;   // groups kept
+  float top_p;      // in (0, 1): adaptive top-p trim
+  float rsf;
+};
+
+RouteRule route_rule(const moe_handle *h) {
+  return RouteRule{h->L.router_mode, h->L.n_group, h->L.topk_group, h->L.top_p,
+                   h->L.routed_scaling_factor};
+}
+
 __device__ __forceinline__ float load_x(const void *x, int x_is_bf16, size_t i) {
   if (x_is_bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i]);
   return reinterpret_cast<const float *>(x)[i];
@@ -193,18 +207,26 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(
 
 // ---------------------------------------------------------------------------
 // Top-k of one token by one warp; expert e lives in lane e % 32, slot e / 32.
-// Keys: softmax mode, l = z + b; sigmoid mode, s = sigmoid(z), key = s + b.
+// Keys: softmax modes, l = z + b; sigmoid mode, s = sigmoid(z), key = s + b.
+// With groups (sigmoid mode, n_group > 1), each group's score is the sum of
+// its two largest keys, and the keys of experts outside the topk_group best
+// groups (ties to the lower group) drop to -inf before the selection.
 // k rounds of a warp argmax (larger key first, lower id on ties) give the
-// slots in descending key order.  Weights are renormalised over the selection
-// and times rsf: softmax w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0); sigmoid
-// w_j = s_j / sum_i s_i.  Split partial logits are summed in split order;
-// `coherent` reads them through L2 (written by other CTAs of the same kernel).
+// slots in descending key order.  Weights, times rsf: mode 0
+// w_j = exp(l_j - l_0) / sum_sel exp(l_i - l_0); mode 2 the same numerator
+// over the sum across all E experts; mode 1 w_j = s_j / sum_sel s_i.  Top-p
+// keeps slot j while the shares of the slots before it sum below top_p (slot
+// 0 always), gives the dropped slots id -1 and weight 0, and (modes 0 and 1)
+// renormalises over the kept slots.  Split partial logits are summed in
+// split order; `coherent` reads them through L2 (written by other CTAs of the
+// same kernel).  Every sum runs in a fixed order.
 template <int EPL>
 __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int splits,
-                                           int zstride, int t, int E, int k, int mode,
-                                           const float *__restrict__ bias, float rsf,
+                                           int zstride, int t, int E, int k, const RouteRule r,
+                                           const float *__restrict__ bias,
                                            int32_t *__restrict__ idx_out,
                                            float *__restrict__ w_out, bool coherent) {
+  const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   float key[EPL], val[EPL];
 #pragma unroll
@@ -225,7 +247,7 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
       for (int s = 0; s < kRouterSplitMax; ++s)
         if (s < splits) zz += part[s];
       const float b = bias ? bias[e] : 0.f;
-      if (mode == 0) {
+      if (r.mode != 1) {
         key[i] = zz + b;
         val[i] = key[i];
       } else {
@@ -233,6 +255,55 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
         val[i] = sc;
         key[i] = sc + b;
       }
+    }
+  }
+  if (r.n_group > 1) {
+    // Lane g holds group g's score: the sum of its two largest keys.
+    const int gsz = E / r.n_group;
+    float my_gs = -INFINITY;
+    for (int g = 0; g < r.n_group; ++g) {
+      float a = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e >= g * gsz && e < (g + 1) * gsz) {
+          const float v = key[i];
+          if (v > a) {
+            b2 = a;
+            a = v;
+          } else if (v > b2) {
+            b2 = v;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {   // merge two top-2 lists
+        const float oa = __shfl_xor_sync(full, a, o), ob = __shfl_xor_sync(full, b2, o);
+        b2 = fmaxf(fminf(a, oa), fmaxf(b2, ob));
+        a = fmaxf(a, oa);
+      }
+      if (lane == g) my_gs = a + b2;
+    }
+    int gkept = 0;   // lane g: group g is eligible
+    for (int j = 0; j < r.topk_group; ++j) {
+      float bv = gkept ? -INFINITY : my_gs;
+      int bg = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(full, bv, o);
+        const int og = __shfl_xor_sync(full, bg, o);
+        if (ov > bv || (ov == bv && og < bg)) {
+          bv = ov;
+          bg = og;
+        }
+      }
+      if (lane == bg) gkept = 1;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      const int g = (e < E) ? e / gsz : 0;
+      if (!__shfl_sync(full, gkept, g)) key[i] = -INFINITY;
     }
   }
   int my_idx = -1;
@@ -250,8 +321,8 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const float ok = __shfl_xor_sync(full, bk, o);
+      const int oe = __shfl_xor_sync(full, be, o);
       if (ok > bk || (ok == bk && oe < be)) {
         bk = ok;
         be = oe;
@@ -267,32 +338,54 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
           key[i] = -INFINITY;
         }
     }
-    v = __shfl_sync(0xffffffffu, v, be & 31);
+    v = __shfl_sync(full, v, be & 31);
     if (lane == j) {
       my_idx = be;
       my_val = v;
     }
   }
-  // Renormalise over the selection, summing in slot order.
-  const float top = __shfl_sync(0xffffffffu, my_val, 0);
+  // Numerators, and the sum over the selection in slot order.
+  const float top = __shfl_sync(full, my_val, 0);
   float num = 0.f;
-  if (lane < k) num = (mode == 0) ? expf(my_val - top) : my_val;
+  if (lane < k) num = (r.mode != 1) ? expf(my_val - top) : my_val;
   float den = 0.f;
-  for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
+  for (int j = 0; j < k; ++j) den += __shfl_sync(full, num, j);
+  // Mode 2 divides by the sum over all experts (xor-butterfly: the same bits
+  // on every lane).
+  float all = 0.f;
+  if (r.mode == 2) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) all += expf(val[i] - top);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) all += __shfl_xor_sync(full, all, o);
+  }
+  int kept = k;
+  float norm = den;
+  if (r.top_p > 0.f && r.top_p < 1.f) {
+    float cum = 0.f;
+    for (int j = 1; j < k; ++j) {
+      cum += __shfl_sync(full, num, j - 1) / den;
+      if (kept == k && cum >= r.top_p) kept = j;
+    }
+    norm = 0.f;
+    for (int j = 0; j < kept; ++j) norm += __shfl_sync(full, num, j);
+  }
   if (lane < k) {
-    idx_out[(size_t)t * k + lane] = my_idx;
-    w_out[(size_t)t * k + lane] = num / den * rsf;
+    const bool keep = lane < kept;
+    idx_out[(size_t)t * k + lane] = keep ? my_idx : -1;
+    w_out[(size_t)t * k + lane] = keep ? num / (r.mode == 2 ? all : norm) * r.rsf : 0.f;
   }
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(256) router_topk_kernel(
-    const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k, int mode,
-    const float *__restrict__ bias, float rsf, int32_t *__restrict__ idx_out,
+__global__ void __launch_bounds__(256, 1) router_topk_kernel(
+    const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k,
+    const RouteRule r, const float *__restrict__ bias, int32_t *__restrict__ idx_out,
     float *__restrict__ w_out) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_token<EPL>(z_part, splits, zstride, t, E, k, mode, bias, rsf, idx_out, w_out, false);
+  topk_token<EPL>(z_part, splits, zstride, t, E, k, r, bias, idx_out, w_out, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -303,8 +396,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 // counting sort as dispatch.cu.  Also clears the status word first.
 template <int EPL>
 __global__ void __launch_bounds__(256) route_small_kernel(
-    const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, int mode,
-    const float *__restrict__ wr_t, const float *__restrict__ bias, float rsf, int h_per_split,
+    const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, const RouteRule r,
+    const float *__restrict__ wr_t, const float *__restrict__ bias, int h_per_split,
     float *__restrict__ z_part, int32_t *__restrict__ ticket, int n_shared,
     int32_t *__restrict__ idx, float *__restrict__ w, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
@@ -344,7 +437,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   if (threadIdx.x == 0) *status = kStatusOk;
   // Top-k: warp t handles token t.
   if (warp < T)
-    topk_token<EPL>(z_part, gridDim.y, kGemvTokens, warp, E, k, mode, bias, rsf, idx, w, true);
+    topk_token<EPL>(z_part, gridDim.y, kGemvTokens, warp, E, k, r, bias, idx, w, true);
   __syncthreads();
   // Stable counting sort of the A = T*k assignments (A <= 128, E <= 1024).
   __shared__ int cnt[kMaxExperts];
@@ -356,7 +449,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   for (int a = threadIdx.x; a < A; a += blockDim.x) {
     const int ea = __ldcg(idx + a);
     if (ea >= 0 && ea < E) atomicAdd(&cnt[ea], 1);
-    else atomicExch(status, kStatusBadExpert);
+    else if (ea != -1) atomicExch(status, kStatusBadExpert);   // -1: a slot top-p dropped
   }
   __syncthreads();
   // Exclusive scan of cnt over E: each thread owns a contiguous run of experts.
@@ -395,6 +488,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
       const int a = c0 + lane;
       int ea = (a < A) ? __ldcg(idx + a) : E;
       if (ea < 0 || ea >= E) ea = E;
+      if (a < A && ea == E) inv[a] = -1;
       const unsigned peers = __match_any_sync(0xffffffffu, ea);
       const int rank = __popc(peers & lt);
       if (ea < E) {
@@ -475,8 +569,8 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
       if (err != cudaSuccess) return err;                                                       \
     }                                                                                           \
     route_small_kernel<N><<<grid, 256, smem, st>>>(                                             \
-        x, h->L.x_dtype == 1, T, H, E, k, h->L.router_mode, h->wr_t, h->bias,                   \
-        h->L.routed_scaling_factor, hps, w.z_part, w.ticket, h->S, w.idx, w.w, w.counts,        \
+        x, h->L.x_dtype == 1, T, H, E, k, route_rule(h), h->wr_t, h->bias, hps, w.z_part,       \
+        w.ticket, h->S, w.idx, w.w, w.counts,                                                   \
         w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);   \
   } while (0)
   if (epl <= 1) MOE_RS(1);
@@ -519,8 +613,7 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
   const dim3 g2((T + 7) / 8);
 #define MOE_TOPK(N)                                                                          \
   router_topk_kernel<N><<<g2, 256, 0, st>>>(h->ws.z_part, splits, zstride, T, E, k,          \
-                                            h->L.router_mode, h->bias,                      \
-                                            h->L.routed_scaling_factor, h->ws.idx, h->ws.w)
+                                            route_rule(h), h->bias, h->ws.idx, h->ws.w)
   if (epl <= 1) MOE_TOPK(1);
   else if (epl <= 2) MOE_TOPK(2);
   else if (epl <= 4) MOE_TOPK(4);
@@ -582,7 +675,7 @@ extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
     int32_t *idx, float *w, moe_stream_t stream) {
   using namespace moe;
   if (num_experts < 1 || num_experts > kMaxExperts || top_k < 1 || top_k > num_experts ||
-      top_k > kMaxTopK || (router_mode != 0 && router_mode != 1) ||
+      top_k > kMaxTopK || router_mode < 0 || router_mode > 2 ||
       !(routed_scaling_factor > 0.f))
     return MOE_ERR_ROUTING;
   if (T < 0 || hidden < 512 || hidden % 512 || (x_dtype != 0 && x_dtype != 1))
@@ -620,8 +713,10 @@ extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
   const int epl = (E + 31) / 32;
   const dim3 g2((T + 7) / 8);
 #define MOE_TOPK_NA(N)                                                                      \
-  router_topk_kernel<N><<<g2, 256, 0, st>>>(z, splits, zstride, T, E, top_k, router_mode,  \
-                                            router_bias, routed_scaling_factor, idx, w)
+  router_topk_kernel<N><<<g2, 256, 0, st>>>(z, splits, zstride, T, E, top_k,               \
+                                            RouteRule{router_mode, 0, 0, 0.f,               \
+                                                      routed_scaling_factor},               \
+                                            router_bias, idx, w)
   if (epl <= 1) MOE_TOPK_NA(1);
   else if (epl <= 2) MOE_TOPK_NA(2);
   else if (epl <= 4) MOE_TOPK_NA(4);

@@ -11,6 +11,17 @@
  *               routed_scaling_factor; "System map": router, norm and bias f32.
  *               Colibri C + cuBLASLt tutorial, cf-1.com, §2.1 step 2: linear
  *               layer + softmax -> top-k ids and weights.)
+ *               Variants: softmax weights left unrenormalised (router_mode 2,
+ *               w_j = p_j * rsf with p the softmax over all E); group-limited
+ *               noaux_tc (n_group > 1: E/n_group contiguous experts per group,
+ *               a group scored by the sum of its two largest keys, the
+ *               topk_group best groups eligible, ties to the lower group); and
+ *               the adaptive expert top-p trim of the colibri tuning guide
+ *               (gitcode.com, knob table, "--topp"; lossy): with slots in
+ *               selection order and q_j each slot's share of the selected
+ *               weights, slot j is kept while q_0 + ... + q_{j-1} < top_p
+ *               (slot 0 always); a dropped slot gets id -1 and weight 0 and is
+ *               not dispatched; modes 0 and 1 renormalise over the kept slots.
  *   2. dispatch a counting sort that groups the T*k assignments by expert:
  *               per-expert counts, prefix-sum offsets, a permutation, and no
  *               allocation (tutorial cf-1.com §3.3 Step 3; pure-C Colibri
@@ -63,7 +74,8 @@ extern "C" {
 #define MOE_OK 0
 #define MOE_ERR_NOMEM (-1)    /* out of memory at init, or T > max_tokens        */
 #define MOE_ERR_ROUTING (-2)  /* invalid routing layout: top_k < 1 or > E,
-                                 E > 1024, unknown router_mode                  */
+                                 E > 1024, unknown router_mode, a group rule
+                                 that does not fit, top_p < 0 or NaN            */
 #define MOE_ERR_DEVICE (-3)   /* CUDA error, or a nonzero device status word     */
 #define MOE_ERR_ARG (-4)      /* NULL pointer, a size not a multiple of 64,
                                  unsupported dtype, bad option                  */
@@ -82,10 +94,17 @@ typedef struct moe_layout {
   int32_t intermediate;          /* I, a multiple of 1024 (routed experts)       */
   int32_t n_shared;              /* 0 or 1                                       */
   int32_t shared_intermediate;   /* I of the shared expert (multiple of 1024)    */
-  int32_t router_mode;           /* 0 softmax, 1 sigmoid + noaux_tc, n_group 1   */
+  int32_t router_mode;           /* 0 softmax, 1 sigmoid + noaux_tc, 2 softmax
+                                    without renormalisation                      */
   float routed_scaling_factor;   /* rsf (1.0 for plain softmax routers)          */
   int32_t x_dtype;               /* 0 f32, 1 bf16                                */
   int32_t max_tokens;            /* largest T a forward call may pass (>= 1)     */
+  /* Router variants; all zero gives the plain rules above. */
+  int32_t n_group;               /* 0 or 1: every expert eligible; 2..32: group-
+                                    limited noaux_tc (router_mode 1 only)        */
+  int32_t topk_group;            /* groups kept, 1..n_group (n_group > 1)        */
+  float top_p;                   /* adaptive expert top-p in (0, 1); 0 (or >= 1)
+                                    off                                          */
 } moe_layout;
 
 typedef struct moe_weights {
@@ -115,8 +134,10 @@ typedef struct moe_debug {
   const float *w;          /* [T][k] renormalised weights times rsf             */
   const int32_t *counts;   /* [E] assignments per expert                        */
   const int32_t *offsets;  /* [E+1] exclusive prefix sum of counts             */
-  const int32_t *perm;     /* [T*k] grouped position -> assignment t*k+j        */
-  const int32_t *inv;      /* [T*k] assignment -> grouped position              */
+  const int32_t *perm;     /* [T*k] grouped position -> assignment t*k+j; the
+                              first offsets[E] entries are meaningful          */
+  const int32_t *inv;      /* [T*k] assignment -> grouped position (-1 for a
+                              slot the top-p trim dropped)                     */
   const int32_t *status;   /* one int32 device status word (0 = ok)             */
   int32_t regime;          /* 1 GEMV path, 2 tensor-core path, 3 exact TC path  */
   int64_t launches;        /* kernels launched by this handle since moe_init    */
@@ -210,6 +231,7 @@ int moe_debug_view(moe_handle *h, moe_debug *d);
  *                of moe_weights.router_w)
  *   router_bias  [num_experts] f32 device, or NULL (softmax mode only)
  *   idx, w       [T][top_k] device outputs, as moe_debug.idx / moe_debug.w
+ * router_mode 0, 1 or 2; the group and top-p variants need a handle.
  * Limits: hidden a multiple of 512; num_experts <= 1024; top_k <= 32; for
  * T > 4, T * num_experts <= 1048576 (larger calls return MOE_ERR_NOMEM and
  * launch nothing).  T == 0 does nothing.

@@ -35,6 +35,7 @@ def oracle_layer(wl, layer, x, Wr, bias, rows=None):
     counts, offsets, perm, inv = oracle.dispatch(idx, wl.E)
     rows = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
     needed = np.unique(idx[rows])
+    needed = needed[needed >= 0]          # -1: a slot the top-p trim dropped
     L, W, _, _ = oracle_weights_for(wl, layer, Wr, bias, needed)
     out, _, _ = oracle.moe_forward(L, W, x[rows])
     return dict(idx=idx, w=w, key=key, gap=gap, counts=counts, offsets=offsets, perm=perm,

@@ -55,6 +55,15 @@ def _init(layout, weights=True):
     (dict(hidden=500), -4), (dict(hidden=0), -4), (dict(intermediate=1000), -4),
     (dict(n_shared=1, shared_intermediate=0), -4), (dict(n_shared=2), -4),
     (dict(x_dtype=5), -4), (dict(max_tokens=0), -4),
+    (dict(router_mode=2, n_group=2, topk_group=1), -2),              # groups need sigmoid
+    (dict(router_mode=1, n_group=3, topk_group=1), -2),              # 8 % 3
+    (dict(router_mode=1, n_group=8, topk_group=2), -2),              # groups of one
+    (dict(router_mode=1, n_group=4, topk_group=0), -2),
+    (dict(router_mode=1, n_group=4, topk_group=5), -2),
+    (dict(router_mode=1, n_group=4, topk_group=1, top_k=3), -2),     # k > 1 group of 2
+    (dict(router_mode=1, n_group=64, topk_group=1, num_experts=128), -2),   # > 32 groups
+    (dict(n_group=-1), -2), (dict(top_p=-0.5), -2), (dict(top_p=float("nan")), -2),
+    (dict(router_mode=4), -2),
 ])
 def test_init_rejects_bad_layout(kw, code):
     rc, h = _init(_layout(**kw))

@@ -44,6 +44,13 @@ def get_layer(wl, max_tokens, dev, layer=0):
     return _layers[key]
 
 
+def check_weights(w, ref_w):
+    """Routing weights within W_TOL relative; a dropped slot's weight is 0."""
+    live = ref_w != 0
+    assert np.all(w[~live] == 0)
+    assert np.max(np.abs(w[live] - ref_w[live]) / np.abs(ref_w[live])) < W_TOL
+
+
 def run_and_compare(wl, T, dev, regime=1, layer=0):
     """Forward through the given expert path (default: the small-T GEMV path)."""
     import torch
@@ -61,7 +68,7 @@ def run_and_compare(wl, T, dev, regime=1, layer=0):
     idx = h.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k)
     w = h.debug_read(moe.MOE_DBG_W).reshape(T, wl.k)
     assert np.array_equal(idx, ref["idx"])
-    assert np.max(np.abs(w - ref["w"]) / np.abs(ref["w"])) < W_TOL
+    check_weights(w, ref["w"])
     assert np.array_equal(h.debug_read(moe.MOE_DBG_COUNTS), ref["counts"])
     assert np.array_equal(h.debug_read(moe.MOE_DBG_OFFSETS), ref["offsets"])
     assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM), ref["perm"])
@@ -278,7 +285,9 @@ def run_tc(wl, T, dev, rows=None):
     assert h.status() == 0
     assert h.debug_view().regime == moe.REGIME_TC
     assert np.array_equal(h.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k), ref["idx"])
-    assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM), ref["perm"])
+    n_routed = int(ref["offsets"][-1])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_PERM)[:n_routed], ref["perm"][:n_routed])
+    assert np.array_equal(h.debug_read(moe.MOE_DBG_INV), ref["inv"])
     got = out.cpu().numpy()
     assert np.all(np.isfinite(got))
     return got, ref, h, xd
@@ -371,3 +380,65 @@ def test_usage_counters(dev):
     assert found == moe.engine_id("olmoe") and np.array_equal(back[0], expect)
     h.usage_reset()
     assert not h.usage().any()
+
+
+@pytest.mark.parametrize("name,T,regime", [
+    ("tiny_grouped", 16, 1), ("tiny_grouped", 16, 2), ("tiny_grouped", 5, 3),
+    ("tiny_topp", 16, 1), ("tiny_topp", 16, 2), ("tiny_topp", 3, 3),
+    ("olmoe_raw", 1, 1), ("olmoe_raw", 64, 1), ("olmoe_raw", 64, 2),
+    ("glm_grouped", 1, 1), ("glm_grouped", 4, 1), ("glm_grouped", 4, 3), ("glm_grouped", 24, 2),
+    ("glm_topp", 1, 1), ("glm_topp", 4, 1), ("glm_topp", 8, 3), ("glm_topp", 40, 2),
+])
+def test_router_variant_parity(dev, name, T, regime):
+    """Router variants end to end on each expert path: unrenormalised softmax
+    weights, group-limited noaux_tc and the adaptive top-p trim (dropped slots
+    id -1, not dispatched).  Ids, the grouping and (regimes 1, 3) the GEMV
+    tolerance or (regime 2) the tensor-core tolerance."""
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME[name]
+    if regime == moe.REGIME_TC:
+        got, ref, h, _ = run_tc(wl, T, dev)
+        check_weights(h.debug_read(moe.MOE_DBG_W).reshape(T, wl.k), ref["w"])
+        check_tc(got, ref["out"])
+    else:
+        got, ref, h, _ = run_and_compare(wl, T, dev, regime=regime)
+        assert rel_l2(got, ref["out"]) <= GEMV_TOL
+    assert h.debug_view().regime == regime
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+    if wl.top_p:
+        assert (ref["idx"] == -1).any() or T == 1
+        assert int(ref["offsets"][-1]) == int((ref["idx"] >= 0).sum())
+    if wl.n_group > 1:
+        gsz = wl.E // wl.n_group
+        assert all(len(set(row // gsz)) <= wl.topk_group for row in ref["idx"])
+
+
+@pytest.mark.parametrize("name,T,n", [("glm_grouped", 512, 10), ("glm_topp", 512, 10)])
+def test_router_variant_full_size_tc(dev, name, T, n):
+    """Prefill-sized batches of the group-limited and top-p routers through
+    the tensor-core path (routing of all tokens bit-exact, outputs sampled)."""
+    wl = synth.BY_NAME[name]
+    rows = _sample_rows(T, n, T + 1)
+    got, ref, _, _ = run_tc(wl, T, dev, rows=rows)
+    check_tc(got[rows], ref["out"])
+
+
+def test_router_variant_noalloc_raw_softmax(dev):
+    """moe_route_noalloc takes router_mode 2 (ids and weights as the oracle)."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["olmoe_raw"]
+    h, Wr, bias = get_layer(wl, 64, dev)
+    for T in (3, 64):
+        x, _ = margin_x(wl, T, Wr, bias)
+        L = oracle.layout(wl)
+        idx, w, _, _ = oracle.route(L, oracle.weights(L, Wr, bias), x)
+        wr_eh = torch.from_numpy(np.ascontiguousarray(Wr.T)).to(dev)
+        b = torch.from_numpy(np.asarray(bias, np.float32)).to(dev)
+        gi = torch.empty(T, wl.k, dtype=torch.int32, device=dev)
+        gw = torch.empty(T, wl.k, dtype=torch.float32, device=dev)
+        moe.route_noalloc(to_device_x(wl, x, dev), T, wl.H, wl.E, wl.k, wl.x_dtype, 2, wl.rsf,
+                          wr_eh, b, gi, gw)
+        torch.cuda.synchronize()
+        assert np.array_equal(gi.cpu().numpy(), idx)
+        check_weights(gw.cpu().numpy(), w)
