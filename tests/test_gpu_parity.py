@@ -261,13 +261,18 @@ def test_init_fault_injection_leaks_nothing(dev):
 # ------------------------------------------------------------ tensor cores --
 
 TC_TOL = 5e-3          # relative L2 on the bf16 tensor-core path
-TC_MAXABS = 2e-2       # times rms(ref)
+# Largest element error of a token, in units of that token's output rms.  The
+# bf16 path's error scales with each token's own expert outputs (rounding of
+# its h and of the weights), and the largest of N near-Gaussian errors whose
+# rms is at most TC_TOL of the signal is about sqrt(2 ln N) * TC_TOL, 5.8 *
+# TC_TOL for N = T*H up to 25M elements.
+TC_MAXABS = 6 * TC_TOL
 
 
 def check_tc(got, ref_out):
-    rms = float(np.sqrt(np.mean(ref_out ** 2)))
     assert rel_l2(got, ref_out) <= TC_TOL
-    assert np.max(np.abs(got - ref_out)) <= TC_MAXABS * rms
+    rms_t = np.sqrt(np.mean(np.asarray(ref_out, np.float64) ** 2, axis=1))
+    assert np.all(np.max(np.abs(got - ref_out), axis=1) <= TC_MAXABS * rms_t)
 
 
 def run_tc(wl, T, dev, rows=None):
