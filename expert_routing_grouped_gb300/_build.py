@@ -14,8 +14,8 @@ BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "libmoe.so")
 ROOT = os.path.dirname(HERE)
 SOURCES = ["router.cu", "dispatch.cu", "gemv.cu", "ggemm_tc.cu", "misc.cu", "moe_api.cu",
-           "route_trace.cu"]
-HEADERS = ["moe_internal.cuh", "ptx.cuh"]
+           "route_trace.cu", "decode_tc.cu"]
+HEADERS = ["moe_internal.cuh", "ptx.cuh", "tc.cuh"]
 
 NVCC_FLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",

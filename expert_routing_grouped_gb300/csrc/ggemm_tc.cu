@@ -47,6 +47,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
@@ -61,9 +62,6 @@ constexpr int NG = 2;            // A groups in TMEM
 constexpr int NB = 3;            // token slots
 constexpr int NR = 4;            // raw stages
 constexpr int kSlotRows = 384;   // rows of 128 bytes per token slot (48 KB)
-constexpr int NSL = 16;          // exact mode: per-group accumulator slices
-constexpr int kSliceCols = 16;   // exact mode: columns per slice (MMA N)
-constexpr int NSE = 4;           // exact mode: scale stages read by the epilogue
 constexpr uint32_t kACol0 = 2 * BN;            // first TMEM column of the A groups
 constexpr uint32_t kGroupCols = KPG * BK / 2;  // 64 columns: 2 bf16 per column
 constexpr int kThreads = 512;
@@ -71,18 +69,15 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
 constexpr int kDeqWarps = 8;
 static_assert(kACol0 + NG * kGroupCols <= 512, "TMEM columns");
-static_assert(NSL * kSliceCols <= (int)kACol0, "TMEM columns (exact mode)");
 
 struct __align__(1024) SmemTC {
   uint8_t raw[NR][BM * 128];     // 4 x 16 KB
   uint8_t b[NB][kSlotRows * 128];  // 3 x 48 KB
   float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
-  float sce[NSE][BM * (RK / 64)];  // exact mode: the same scales, for the epilogue
   uint64_t raw_full[NR], raw_empty[NR];
-  uint64_t sce_full[NSE], sce_empty[NSE];
   uint64_t a_full[NG], a_empty[NG];
   uint64_t b_full[NB], b_empty[NB];
-  uint64_t acc_full[NSL], acc_empty[NSL];
+  uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -106,7 +101,6 @@ struct TcParams {
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
   CUtensorMap map_b[4];    // bf16 token operand [R][K], boxes of 32/64/96/192 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
-  int planes;              // operand rows per token (exact mode: 2 for hi/lo planes)
   int K;                   // reduction length (H for W13, I for W2)
   int K_s;                 // the shared expert's reduction length (H, or Is for W2)
   int rows;                // weight rows per routed expert (2I or H)
@@ -115,7 +109,7 @@ struct TcParams {
   const int32_t *blocks;   // token blocks (expert << 16 | block index)
   const int32_t *n_blocks;
   const int32_t *offsets;  // [E+1]
-  __nv_bfloat16 *hb;       // W13 output [R][h_stride] (exact mode: [2R][h_stride], hi/lo)
+  __nv_bfloat16 *hb;       // W13 output [R][h_stride]
   int h_stride;
   float *y;                // W2 output [R][H]
   int H;
@@ -124,176 +118,12 @@ struct TcParams {
 };
 
 // --------------------------------------------------------------- PTX glue --
-// (mbarrier, TMA and elect helpers: ptx.cuh)
+// (mbarrier, TMA and elect helpers: ptx.cuh; tcgen05 descriptors, MMA issue,
+// tensor-memory loads and stores and the int4 decodes: tc.cuh)
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
                                          int32_t *status) {
   return moe::wait_bar(bar, parity, &sm->abort, status);
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (stride byte offset), start address in 16-byte units.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
-  d |= (uint64_t)1 << 16;                            // leading byte offset (unused: 16 B)
-  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset
-  d |= (uint64_t)1 << 46;                            // descriptor version
-  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: bf16 A and B (K-major), f32 accumulator.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4)                          // D format f32
-         | (1u << 7)                        // A format bf16
-         | (1u << 10)                       // B format bf16
-         | ((uint32_t)(N >> 3) << 17)       // N / 8
-         | ((uint32_t)(M >> 4) << 24);      // M / 16
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] . B[smem]^T: A in tensor memory, 128 lanes = 128 rows,
-// two bf16 per 32-bit column in K order.
-// One 64-K block: four K=16 MMAs, A columns a0 + 8 kk, B descriptor db + 2 kk
-// (32 bytes further along the swizzled row); the first accumulates only if
-// `accumulate`, the other three always.
-__device__ __forceinline__ void mma_kblock_ta(uint32_t tmem_d, uint32_t a0, uint64_t db,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.eq.b32 q, %3, %3;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}" ::"r"(tmem_d),
-      "r"(a0), "l"(db), "r"(idesc), "r"(accumulate), "r"(a0 + 8), "l"(db + 2), "r"(a0 + 16),
-      "l"(db + 4), "r"(a0 + 24), "l"(db + 6)
-      : "memory");
-}
-
-// Thread i of the warp writes 16 consecutive 32-bit columns of TMEM lane
-// (quadrant base + i).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// 32 lanes x 32 consecutive columns: thread i gets lane (quadrant base + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 lanes x 16 consecutive columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// ------------------------------------------------------------- dequant --
-
-// bf16x2 arithmetic on raw 32-bit registers.
-__device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ uint32_t lop_nib(uint32_t w) {
-  uint32_t d;
-  // (w & 0x000F000F) | 0x43004300: two offset-binary nibbles into bf16 128 + n.
-  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(d) : "r"(w));
-  return d;
-}
-
-// 8 weights of one library-layout word -> 4 bf16x2 words of bf16(q * s), with
-// s = s_hi + s_lo split into two bf16 (q * s_hi is exact inside the fused
-// multiply-add, q * s_lo contributes below bf16 resolution).
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_hi2, uint32_t s_lo2,
-                                             uint32_t out[4]) {
-  const uint32_t c136 = 0x43084308u;   // bf16x2 (136, 136)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t q = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
-    out[i] = hfma2_bf16(q, s_hi2, hmul2_bf16(q, s_lo2));
-  }
-}
-
-// 8 weights of one library-layout word -> 4 bf16x2 words of the exact codes q.
-__device__ __forceinline__ void dequant_word_q(uint32_t w, uint32_t out[4]) {
-  const uint32_t c136 = 0x43084308u;   // bf16x2 (136, 136)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) out[i] = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_splat(__nv_bfloat16 v) {
-  const uint16_t b = __bfloat16_as_ushort(v);
-  return (uint32_t)b | ((uint32_t)b << 16);
 }
 
 // --------------------------------------------------------------- tiles --
@@ -331,15 +161,8 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
 
 // --------------------------------------------------------------- kernel --
 //
-// EXACT = false (prefill): A = bf16(q * s) per weight, one accumulator per
-// tile (up to 128 tokens), bf16 h out of W13.
-// EXACT = true (decode, up to 8 tokens per expert): A = the exact int4 codes q,
-// each 64-K group accumulates into its own 16-column TMEM slice, and the
-// epilogue applies the group's f32 scale: out = sum_g s_g * (q_g . b_g), the
-// same sum as the f32 GEMV.  f32 operands enter as two bf16 planes (hi, lo:
-// two columns per token), so every product is exact and the accumulation is
-// f32; h goes out of W13 as such a plane pair.
-template <bool EXACT>
+// A = bf16(q * s) per weight (the scale applied in the dequant), one
+// accumulator per tile, bf16 h out of W13.
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   SmemTC *sm = reinterpret_cast<SmemTC *>(
@@ -348,16 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
   const int n_blocks = *p.n_blocks;
   const int n_fb = (p.rows > p.rows_s ? p.rows : p.rows_s) / BM;
   const int n_tiles = n_blocks * n_fb;
-  constexpr int NACC = EXACT ? NSL : 2;
+  constexpr int NACC = 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NR; ++i) {
       mbar_init(&sm->raw_full[i], 1);
       mbar_init(&sm->raw_empty[i], kDeqWarps);
-    }
-    for (int i = 0; i < NSE; ++i) {
-      mbar_init(&sm->sce_full[i], 1);
-      mbar_init(&sm->sce_empty[i], 4);
     }
     for (int i = 0; i < NG; ++i) {
       mbar_init(&sm->a_full[i], kDeqWarps);
@@ -390,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     {
       uint32_t rk = 0;
       uint32_t armed = 0, par = 0;        // per stage: a copy was issued / its parity
-      uint32_t armed3 = 0, par3 = 0;      // the same for the epilogue's scale stages
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
@@ -401,27 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           const int s = rk % NR;
           const uint32_t ph = (rk / NR) & 1;
           if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
+          fence_proxy_async();
           if (elect_one()) {
-            mbar_expect_tx(&sm->raw_full[s], BM * 128 + (EXACT ? 0 : BM * (RK / 64) * 4));
+            mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
             tma_load_2d(sm->raw[s], mw, r * 128, tl.wrow0, &sm->raw_full[s]);
-            if (!EXACT) tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
+            tma_load_2d(sm->sc[s], ms, r * (RK / 64), tl.wrow0, &sm->raw_full[s]);
           }
           __syncwarp();
           armed |= 1u << s;
           par = (par & ~(1u << s)) | (ph << s);
-          if (EXACT) {
-            // The scales go to the epilogue, which applies them per group.
-            const int s3 = rk % NSE;
-            const uint32_t ph3 = (rk / NSE) & 1;
-            if (!(ok = wait_bar(&sm->sce_empty[s3], ph3 ^ 1, sm, p.status))) break;
-            if (elect_one()) {
-              mbar_expect_tx(&sm->sce_full[s3], BM * (RK / 64) * 4);
-              tma_load_2d(sm->sce[s3], ms, r * (RK / 64), tl.wrow0, &sm->sce_full[s3]);
-            }
-            __syncwarp();
-            armed3 |= 1u << s3;
-            par3 = (par3 & ~(1u << s3)) | (ph3 << s3);
-          }
           ++rk;
         }
       }
@@ -429,10 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       const unsigned long long t0 = globaltimer();
       for (int s = 0; s < NR; ++s)
         while (((armed >> s) & 1) && !mbar_try_wait(&sm->raw_full[s], (par >> s) & 1) &&
-               globaltimer() - t0 < kWaitNs) {
-        }
-      for (int s = 0; s < NSE; ++s)
-        while (((armed3 >> s) & 1) && !mbar_try_wait(&sm->sce_full[s], (par3 >> s) & 1) &&
                globaltimer() - t0 < kWaitNs) {
         }
     }
@@ -445,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
-        // Smallest box covering the tile's operand rows (planes per token);
-        // one slot carries 256 / rows K blocks of it (K / 64 is a multiple of 8).
-        const int bi = box_index(p.planes * tl.nvalid);
+        // Smallest box covering the tile's token rows; one slot carries
+        // 256 / rows K blocks of it (K / 64 is a multiple of 8).
+        const int bi = box_index(tl.nvalid);
         const int rows = box_rows(bi), kps = box_kps(bi);
-        const int brow = p.planes * tl.p0;
+        const int brow = tl.p0;
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
@@ -480,7 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       uint32_t it = 0;
       uint32_t ga = 0, gpar = 0;          // A group and its phase
       uint32_t bs = 0, bpar = 0;          // token slot and its phase
-      uint32_t sl = 0, slpar = 0;         // exact mode: accumulator slice and its phase
       int last_acc = -1;
       uint32_t last_acc_par = 0;
       constexpr uint32_t kSlotDesc = (kSlotRows * 128) >> 4;   // descriptor units per slot
@@ -490,11 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
         const int buf = it & 1;
-        if (!EXACT) {
-          if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
-          tc_fence_after();
-        }
-        const int ncols = p.planes * tl.nvalid;
+        if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
+        tc_fence_after();
+        const int ncols = tl.nvalid;
         const uint32_t idesc = idesc_bf16(BM, (ncols + 15) & ~15);
         const int bi = box_index(ncols);
         const int kps_m1 = box_kps(bi) - 1;                     // K blocks per slot - 1
@@ -514,18 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
               if (!(ok = wait_bar(&sm->b_full[bs], bpar, sm, p.status))) break;
               db_slot = db0 + (uint64_t)(bs * kSlotDesc);
             }
-            uint32_t d = dacc;
-            if (EXACT) {
-              if (!(ok = wait_bar(&sm->acc_empty[sl], slpar ^ 1, sm, p.status))) break;
-              tc_fence_after();
-              d = tmem + sl * kSliceCols;
-            }
             const bool slot_done = (jj == kps_m1);
             if (elect_one()) {
-              mma_kblock_ta(d, acol + j * (BK / 2), db_slot + (uint64_t)(jj * jj_desc), idesc,
-                            EXACT ? 0u : (first ^ 1u));
+              mma_kblock_ta(dacc, acol + j * (BK / 2), db_slot + (uint64_t)(jj * jj_desc), idesc,
+                            first ^ 1u);
               if (slot_done) mma_commit(&sm->b_empty[bs]);
-              if (EXACT) mma_commit(&sm->acc_full[sl]);
             }
             __syncwarp();
             first = 0;
@@ -535,11 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
             } else {
               ++jj;
             }
-            if (EXACT) {
-              last_acc = (int)sl;
-              last_acc_par = slpar;
-              if (++sl == NSL) { sl = 0; slpar ^= 1; }
-            }
           }
           if (!ok) break;
           if (elect_one()) mma_commit(&sm->a_empty[ga]);
@@ -547,12 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           if (++ga == NG) { ga = 0; gpar ^= 1; }
         }
         if (!ok) break;
-        if (!EXACT) {
-          if (elect_one()) mma_commit(&sm->acc_full[buf]);
-          __syncwarp();
-          last_acc = buf;
-          last_acc_par = (it >> 1) & 1;
-        }
+        if (elect_one()) mma_commit(&sm->acc_full[buf]);
+        __syncwarp();
+        last_acc = buf;
+        last_acc_par = (it >> 1) & 1;
         ++it;
       }
       // Drain: the last commit covers every MMA issued before it.
@@ -568,77 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     const int q = warp - kEpiWarp0;       // TMEM lane quadrant
     const int row = q * 32 + lane;        // weight row of the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t it = 0, ks = 0, rk = 0;
+    uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       Tile tl;
       if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
       const int fb = (tl.wrow0 - (tl.shared ? 0 : tl.e * p.rows)) / BM;
-      if (EXACT) {
-        // acc[c] = sum over groups of s_g(row) * D_g[row][c], c = plane-major
-        // column (token c / planes, plane c % planes).
-        float acc[kSliceCols];
-#pragma unroll
-        for (int c = 0; c < kSliceCols; ++c) acc[c] = 0.f;
-        for (int rr = 0; ok && rr < tl.K / RK; ++rr) {
-          const int s3 = rk % NSE;
-          if (!(ok = wait_bar(&sm->sce_full[s3], (rk / NSE) & 1, sm, p.status))) break;
-          const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sce[s3][row * (RK / 64)]);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->sce_empty[s3]);
-          ++rk;
-#pragma unroll
-          for (int j = 0; j < RK / BK; ++j) {
-            const int sl = ks % NSL;
-            if (!(ok = wait_bar(&sm->acc_full[sl], (ks / NSL) & 1, sm, p.status))) break;
-            tc_fence_after();
-            float v[kSliceCols];
-            tmem_ld16(tmem + lane_base + sl * kSliceCols, v);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm->acc_empty[sl]);
-            ++ks;
-            const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
-#pragma unroll
-            for (int c = 0; c < kSliceCols; ++c) acc[c] = fmaf(sv, v[c], acc[c]);
-          }
-        }
-        if (!ok) break;
-        if (p.mode == 0) {
-          // lanes 0-15: g of features fb*64 + 16q + lane; lanes 16-31: u of the same.
-          const int feat = fb * 64 + q * 16 + (lane & 15);
-          auto put = [&](int tk, float gsum) {
-            const float u = __shfl_xor_sync(0xffffffffu, gsum, 16);
-            if (lane < 16) {
-              const float hval = gsum / (1.0f + expf(-gsum)) * u;
-              const __nv_bfloat16 hi = __float2bfloat16_rn(hval);
-              const __nv_bfloat16 lo = __float2bfloat16_rn(hval - __bfloat162float(hi));
-              const size_t r2 = 2 * (size_t)(tl.p0 + tk);
-              p.hb[r2 * p.h_stride + feat] = hi;
-              p.hb[(r2 + 1) * p.h_stride + feat] = lo;
-            }
-          };
-          if (p.planes == 2) {
-#pragma unroll
-            for (int tk = 0; tk < kSliceCols / 2; ++tk)
-              if (tk < tl.nvalid) put(tk, acc[2 * tk] + acc[2 * tk + 1]);
-          } else {
-#pragma unroll
-            for (int tk = 0; tk < kSliceCols; ++tk)
-              if (tk < tl.nvalid) put(tk, acc[tk]);
-          }
-        } else {
-          const int o = fb * BM + row;
-#pragma unroll
-          for (int tk = 0; tk < kSliceCols / 2; ++tk) {
-            if (tk < tl.nvalid) {
-              const int pr = tl.p0 + tk;
-              p.y[(size_t)pr * p.H + o] = (acc[2 * tk] + acc[2 * tk + 1]) * p.wperm[pr];
-            }
-          }
-        }
-        continue;
-      }
       const int buf = it & 1;
       if (!(ok = wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status))) break;
       tc_fence_after();
@@ -701,13 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
-        float4 sc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!EXACT) sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
+        const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
         uint4 c[RK / BK];
 #pragma unroll
         for (int j = 0; j < RK / BK; ++j)   // raw 16-byte chunk 2j + hh (128-byte swizzle)
           c[j] = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + hh) ^ (r & 7)) << 4));
+        fence_proxy_async();   // the raw reads before the stage's TMA refill
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->raw_empty[s]);
 #pragma unroll
@@ -716,25 +436,20 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           if (!(ok = wait_bar(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p.status))) break;
           tc_fence_after();
           const uint32_t acol = tmem + lane_base + kACol0 + ga * kGroupCols + hh * 16;
+          uint32_t o[KPG][16];
 #pragma unroll
           for (int jj = 0; jj < KPG; ++jj) {
             const int j = gi * KPG + jj;
             const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-            uint32_t o[16];
-            if (EXACT) {
+            const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
+            const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
+            const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
+            const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
 #pragma unroll
-              for (int wv = 0; wv < 4; ++wv) dequant_word_q(words[wv], o + 4 * wv);
-            } else {
-              const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
-              const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
-              const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
-              const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
-#pragma unroll
-              for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o + 4 * wv);
-            }
-            tmem_st16(acol + jj * (BK / 2), o);
+            for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o[jj] + 4 * wv);
           }
-          tmem_wait_st();
+          static_assert(KPG == 2, "two K blocks per A group");
+          tmem_st16x2(acol, o[0], acol + BK / 2, o[1]);   // includes the wait
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm->a_full[ga]);
@@ -799,8 +514,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
   }
 }
 
-// Exact mode: grouped row pr of x as operand planes -- x itself when it is
-// bf16 (planes = 1), else rows 2pr, 2pr+1 = bf16 hi, bf16(x - hi).
+// Decode tensor-core path (decode_tc.cu): grouped row pr of x as operand
+// planes -- x itself when it is bf16 (one plane), else rows 2pr, 2pr+1 = bf16
+// hi, bf16(x - hi) -- and the grouped routing weights.
 __global__ void __launch_bounds__(256) gather_exact_kernel(const void *__restrict__ x,
                                                            int x_is_bf16, int T, int H, int k,
                                                            int n_shared,
@@ -1156,12 +872,9 @@ namespace {
 cudaError_t set_tc_attrs() {
   static bool attr = false;   // per process; the attribute is per function
   if (!attr) {
-    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel<false>,
+    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(ggemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     attr = true;
   }
@@ -1169,100 +882,11 @@ cudaError_t set_tc_attrs() {
 }
 }  // namespace
 
-cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *out,
-                            bool accumulate, cudaStream_t st) {
+cudaError_t launch_gather_exact(const moe_handle *h, const void *x, int T, cudaStream_t st) {
   const moe::Workspace &w = h->ws;
-  const int E = h->E, H = h->H, I = h->I, k = h->k, S = h->S;
-  const int Is = S ? h->Is : I;
-  const int A = T * k;
-  const int rows_x = kExactTokens * (k + S);
-  const int h_stride = I > Is ? I : Is;
-  const int xplanes = h->L.x_dtype == 1 ? 1 : 2;
-  if (T > kExactTokens) return cudaErrorInvalidValue;
-  cudaError_t err = set_tc_attrs();
-  if (err != cudaSuccess) return err;
-  moe_handle *hm = const_cast<moe_handle *>(h);
-  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm,
-                                                  w.offsets + h->E, w.w,
-                                                  w.xe, w.wperm);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  hm->launches += 1;
-  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
-    hm->stage_names[hm->n_ev - 1] = "gather";
-    cudaEventRecord(hm->ev[hm->n_ev++], st);
-  }
-  TcParams p{};
-  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  // ---- W13 over x planes
-  bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
-  ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
-                      (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
-  for (int i = 0; i < 4; ++i)
-    ok = ok && make_map(&p.map_b[i], w.xe, BF, 2, H, (uint64_t)2 * rows_x, H, BK, kBoxRows[i]);
-  ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
-                      RK / 64, BM, false);
-  ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
-                      (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
-  if (!ok) return cudaErrorInvalidValue;
-  p.mode = 0;
-  p.planes = xplanes;
-  p.K = H;
-  p.K_s = H;
-  p.rows = 2 * I;
-  p.rows_s = 2 * Is;
-  p.E = E;
-  p.A = A;
-  p.T = T;
-  p.blocks = w.tiles;
-  p.n_blocks = w.n_tiles;
-  p.offsets = w.offsets;
-  p.hb = w.he;
-  p.h_stride = h_stride;
-  p.y = w.y;
-  p.H = H;
-  p.wperm = w.wperm;
-  p.status = w.status;
-  ggemm_kernel<true><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  hm->launches += 1;
-  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
-    hm->stage_names[hm->n_ev - 1] = "w13";
-    cudaEventRecord(hm->ev[hm->n_ev++], st);
-  }
-  // ---- W2 over h planes
-  ok = make_map(&p.map_w, h->ex.w2q, U8, 1, I / 2, (uint64_t)E * H, I / 2, 128, BM);
-  ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
-                      BM);
-  for (int i = 0; i < 4; ++i)
-    ok = ok && make_map(&p.map_b[i], w.he, BF, 2, h_stride, (uint64_t)2 * rows_x, h_stride, BK,
-                        kBoxRows[i]);
-  ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
-                      false);
-  ok = ok && make_map(&p.map_scs, S ? h->sh.w2s : h->ex.w2s, F32, 4, Is / 64, (uint64_t)H, Is / 64,
-                      RK / 64, BM, false);
-  if (!ok) return cudaErrorInvalidValue;
-  p.mode = 1;
-  p.planes = 2;
-  p.K = I;
-  p.K_s = Is;
-  p.rows = H;
-  p.rows_s = H;
-  ggemm_kernel<true><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  hm->launches += 1;
-  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
-    hm->stage_names[hm->n_ev - 1] = "w2";
-    cudaEventRecord(hm->ev[hm->n_ev++], st);
-  }
-  err = launch_combine(h, T, out, accumulate, st);
-  hm->launches += 1;
-  if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
-    hm->stage_names[hm->n_ev - 1] = "combine";
-    cudaEventRecord(hm->ev[hm->n_ev++], st);
-  }
-  return err;
+  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, h->H, h->k, h->S,
+                                                  w.perm, w.offsets + h->E, w.w, w.xe, w.wperm);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
@@ -1303,7 +927,6 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
                       (uint64_t)2 * (S ? Is : I), H / 64, RK / 64, BM, false);
   if (!ok) return cudaErrorInvalidValue;
   p.mode = 0;
-  p.planes = 1;
   p.K = H;
   p.K_s = H;
   p.rows = 2 * I;
@@ -1320,7 +943,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.H = H;
   p.wperm = w.wperm;
   p.status = w.status;
-  ggemm_kernel<false><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w13";
@@ -1344,7 +967,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.K_s = Is;
   p.rows = H;
   p.rows_s = H;
-  ggemm_kernel<false><<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
+  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w2";

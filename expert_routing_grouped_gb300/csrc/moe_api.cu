@@ -6,6 +6,7 @@
 // pure-C Colibri tutorial, trdm.cn, §2.2 and §3.2; Colibri C + cuBLASLt
 // tutorial, cf-1.com, §2.2 "Unified Memory Pool"), and copies the weights in.
 // moe_forward only launches kernels on the caller's stream.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -114,6 +115,16 @@ void carve(moe_handle *h, Carver &c) {
   const size_t rows_x = (size_t)moe::kExactTokens * (h->k + S);
   w.xe = c.take<__nv_bfloat16>(2 * rows_x * H);
   w.he = c.take<__nv_bfloat16>(2 * rows_x * Imax);
+  // Decode tensor-core kernel: row blocks of the larger pass (W13: 2I or 2Is
+  // rows per expert, W2: H) over the most experts a decode batch activates,
+  // and one partial-sum slot per (CTA, row block) segment and pipeline.
+  const size_t n_r = std::min<size_t>(E, (size_t)moe::kExactTokens * k);
+  const size_t rb13 = n_r * (2 * I / 128) + S * (2 * Is / 128);
+  const size_t rb2 = (n_r + S) * (H / 128);
+  h->dec_rb_max = (int)std::max(rb13, rb2);
+  const size_t slots = ((size_t)h->num_sms + h->dec_rb_max) * moe::kDecPipes;
+  w.dec_partial = c.take<float>(slots * 128 * moe::kDecTokens);
+  w.dec_ticket = c.take<int32_t>(2 * (size_t)h->dec_rb_max);
   w.x_stage = c.take<char>(maxT * H * h->x_elem);
   w.out_stage = c.take<float>(maxT * H);
 }
@@ -206,8 +217,8 @@ int choose_regime(const moe_handle *h, int T) {
   if (h->regime_opt == 1) return 1;
   if (h->regime_opt == 2) return 2;
   if (h->regime_opt == 3) return T <= moe::kExactTokens ? 3 : 1;
-  if (!moe::tc_path_available()) return 1;
-  return T <= h->small_t_max ? 1 : 2;
+  if (!moe::tc_path_available() || T <= h->small_t_max) return 1;
+  return T <= moe::kExactTokens ? 3 : 2;
 }
 
 // Records the boundary after a stage when tracing is on.
@@ -250,7 +261,7 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
       h->launches += 1;
       mark(h, "combine", st);
     } else if (regime == 3) {
-      err = moe::launch_tc_exact(h, x, T, out, accumulate, st);
+      err = moe::launch_decode_tc(h, x, T, out, accumulate, st);
     } else {
       err = moe::launch_tc_path(h, x, T, out, accumulate, st);
     }
@@ -292,7 +303,7 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   h->Is = layout->n_shared ? layout->shared_intermediate : 0;
   h->x_elem = layout->x_dtype == 1 ? 2 : 4;
   h->regime_opt = 0;
-  h->small_t_max = 4;
+  h->small_t_max = 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -314,7 +325,8 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   rc = copy_weights(h, weights);
   if (rc == MOE_OK && (cudaMemset(h->ws.status, 0, 4) != cudaSuccess ||
                        cudaMemset(h->ws.ticket, 0, 4) != cudaSuccess ||
-                       cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess))
+                       cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess ||
+                       cudaMemset(h->ws.dec_ticket, 0, 2 * (size_t)h->dec_rb_max * 4) != cudaSuccess))
     rc = MOE_ERR_DEVICE;
   if (rc != MOE_OK) {
     cudaFree(h->pool);

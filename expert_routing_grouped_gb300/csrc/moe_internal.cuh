@@ -17,6 +17,8 @@ constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
 constexpr int kTileTokens = 160;      // tokens per tensor-core tile (the MMA's N)
 constexpr int kExactTokens = 8;       // largest batch of the exact (f32-accumulate) tensor-core mode
+constexpr int kDecPipes = 4;          // decode tensor-core kernel: MMA pipelines per CTA
+constexpr int kDecTokens = kExactTokens;   // tokens per partial-sum row of that kernel
 
 // Device status word codes (sticky until the next forward overwrites them).
 enum Status : int32_t {
@@ -61,6 +63,8 @@ struct Workspace {
   // exact tensor-core mode (T <= kExactTokens): operands as bf16 (hi, lo) plane pairs
   __nv_bfloat16 *xe;  // [2 * kExactTokens*(k+S)][H] grouped x (one plane when x is bf16)
   __nv_bfloat16 *he;  // [2 * kExactTokens*(k+S)][I_max] h planes
+  float *dec_partial;  // decode kernel split-K partial sums [slots][pipeline][128][kDecTokens]
+  int32_t *dec_ticket; // decode kernel arrival counters [2][dec_rb_max] (W13, W2)
   // host-call staging
   void *x_stage;      // [max_tokens][H] (x dtype)
   float *out_stage;   // [max_tokens][H]
@@ -88,6 +92,7 @@ struct moe_handle {
   int last_regime;
   cudaStream_t last_stream;
   int num_sms;
+  int dec_rb_max;                // row blocks of the larger decode matrix pass
   // tracing
   int profile;                   // MOE_OPT_PROFILE
   static constexpr int kMaxStages = 8;
@@ -124,8 +129,13 @@ cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem, uint64_t cols,
               uint64_t rows, uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows,
               bool swizzle = true);
-cudaError_t launch_tc_exact(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
-                            cudaStream_t st);
+// Grouped x of a decode-sized batch as bf16 operand planes (xe) and the
+// per-row routing weights (wperm).
+cudaError_t launch_gather_exact(const moe_handle *h, const void *x, int T, cudaStream_t st);
+// decode_tc.cu: the exact tensor-core path for T <= kExactTokens (gather,
+// W13, W2, combine).
+cudaError_t launch_decode_tc(const moe_handle *h, const void *x, int T, float *out,
+                             bool accumulate, cudaStream_t st);
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out,
                            bool accumulate, cudaStream_t s);
 // misc.cu

@@ -81,6 +81,14 @@ static __device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity,
   }
 }
 
+// Orders this thread's generic-proxy accesses to shared memory before later
+// async-proxy (TMA, tcgen05) accesses once an mbarrier hands the buffer over.
+// A stage that threads read with ordinary loads and then release for a TMA
+// refill needs it: without it the refill can overwrite data still being read.
+static __device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 static __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                                    uint64_t *bar) {
   asm volatile(

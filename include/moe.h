@@ -190,13 +190,14 @@ int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
 int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                      moe_stream_t stream);
 
-/* Chooses the expert path: 0 automatic (T <= small_t_max -> the small-T
- * path, else tensor cores), 1 always the SIMT GEMV path, 2 always the
- * tensor-core path (bf16 weights, bf16 operands), 3 the exact tensor-core
- * path (T <= 8 only: exact int4 codes, f32 operands as bf16 hi/lo pairs, f32
- * group scales and accumulation; the small-T path's numerics on tensor cores). */
+/* Chooses the expert path: 0 automatic (T <= small_t_max -> the SIMT GEMV
+ * path, T <= 8 -> the exact tensor-core path, else tensor cores), 1 always
+ * the SIMT GEMV path, 2 always the tensor-core path (bf16 weights, bf16
+ * operands), 3 the exact tensor-core path (T <= 8 only, else the GEMV path:
+ * exact int4 codes, f32 operands as bf16 hi/lo pairs, f32 group scales and
+ * accumulation -- the GEMV path's numerics, on four MMA pipelines per SM). */
 #define MOE_OPT_REGIME 1
-/* Largest T that the automatic choice sends to the GEMV path (default 4). */
+/* Largest T that the automatic choice sends to the GEMV path (default 1). */
 #define MOE_OPT_SMALL_T_MAX 2
 /* 1: record a CUDA event on the forward's stream at every stage boundary
  * (read the stage times with moe_stage_times); 0 (default): no events. */

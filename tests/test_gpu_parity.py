@@ -447,3 +447,46 @@ def test_router_variant_noalloc_raw_softmax(dev):
         torch.cuda.synchronize()
         assert np.array_equal(gi.cpu().numpy(), idx)
         check_weights(gw.cpu().numpy(), w)
+
+
+def test_auto_regime_choice(dev):
+    """Automatic expert path: one token on the SIMT GEMV path, 2-8 on the exact
+    tensor-core decode path, more on the bf16 tensor-core path."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["glm_decode"]
+    h, Wr, bias = get_layer(wl, 16, dev)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+    for T, want in ((1, moe.REGIME_GEMV), (2, moe.REGIME_TC_EXACT), (8, moe.REGIME_TC_EXACT),
+                    (9, moe.REGIME_TC), (16, moe.REGIME_TC)):
+        x = torch.from_numpy(synth.x_rows(wl, T)).to(dev)
+        out = torch.empty(T, wl.H, device=dev)
+        h.forward(x, T, out)
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        assert h.debug_view().regime == want, (T, h.debug_view().regime)
+
+
+@pytest.mark.parametrize("T", [5, 8])
+def test_decode_tc_repeatable_stress(dev, T):
+    """The decode tensor-core kernel hands shared-memory stages between ordinary
+    loads and TMA refills, and splits K across CTAs: sixteen runs of the same
+    batch must agree to the bit (a missing proxy fence or a racy reduction
+    shows up here as a few rows that differ)."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["glm_decode"]
+    h, Wr, bias = get_layer(wl, 8, dev)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_TC_EXACT)
+    x = torch.from_numpy(synth.x_rows(wl, T)).to(dev)
+    outs = []
+    for _ in range(16):
+        out = torch.empty(T, wl.H, device=dev)
+        h.forward(x, T, out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    ref = outs[0].cpu().numpy()
+    for o in outs[1:]:
+        assert np.array_equal(o.cpu().numpy(), ref)
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
