@@ -90,9 +90,9 @@ void carve(moe_handle *h, Carver &c) {
     h->sh.w2s = c.take<float>(H * Is / 64);
   }
   moe::Workspace &w = h->ws;
-  const size_t zrows = maxT > (size_t)moe::kRouterSplitMax * moe::kGemvTokens
+  const size_t zrows = maxT > (size_t)moe::kRouterSplitMax * moe::kRouteTokens
                            ? maxT
-                           : (size_t)moe::kRouterSplitMax * moe::kGemvTokens;
+                           : (size_t)moe::kRouterSplitMax * moe::kRouteTokens;
   w.z_part = c.take<float>(zrows * E);
   w.idx = c.take<int32_t>(A);
   w.w = c.take<float>(A);
@@ -235,7 +235,7 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
   h->n_ev = 0;
   cudaError_t err = cudaSuccess;
   mark(h, nullptr, st);
-  if (T <= moe::kGemvTokens) {
+  if (T <= moe::kRouteTokens) {
     // One launch routes and groups (and clears the status word).
     err = moe::launch_route_small(h, x, T, usage, st);
     h->launches += 1;

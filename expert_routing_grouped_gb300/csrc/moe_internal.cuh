@@ -15,6 +15,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
+constexpr int kRouteTokens = 8;       // largest T of the fused routing launch
 constexpr int kTileTokens = 160;      // tokens per tensor-core tile (the MMA's N)
 constexpr int kExactTokens = 8;       // largest batch of the exact (f32-accumulate) tensor-core mode
 constexpr int kDecPipes = 4;          // decode tensor-core kernel: MMA pipelines per CTA
@@ -106,7 +107,8 @@ namespace moe {
 
 // router.cu
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t s);
-// T <= 4: router, top-k and dispatch in one launch (also clears the status word).
+// T <= kRouteTokens: router, top-k and dispatch in one launch (also clears the
+// status word).
 // usage (nullable): [E] counters the per-expert counts are added into.
 cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
                                unsigned long long *usage, cudaStream_t s);

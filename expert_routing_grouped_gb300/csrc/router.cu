@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(256, 1) router_topk_kernel(
 // nothing waits) reads every partial through L2, takes the top-k of each token
 // and groups the T*k <= 128 assignments by expert with the same stable
 // counting sort as dispatch.cu.  Also clears the status word first.
-template <int EPL>
+template <int EPL, int NT>
 __global__ void __launch_bounds__(256) route_small_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, const RouteRule r,
     const float *__restrict__ wr_t, const float *__restrict__ bias, int h_per_split,
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
     int32_t *__restrict__ active, int32_t *__restrict__ n_active, int32_t *__restrict__ tiles,
     int32_t *__restrict__ n_tiles, int32_t *__restrict__ status,
     unsigned long long *__restrict__ usage) {
-  extern __shared__ float xs[];   // [4][h_per_split]
+  extern __shared__ float xs[];   // [NT][h_per_split]
   __shared__ int last;
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
@@ -412,15 +412,15 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   const int e = blockIdx.x * 8 + warp;
   float4 wv[kMaxRowVec];
   if (e < E) row_prefetch(wr_t + (size_t)e * H + h0, h_per_split, wv);
-  stage_x<kGemvTokens>(x, x_is_bf16, T, H, h0, h_per_split, xs);
+  stage_x<NT>(x, x_is_bf16, T, H, h0, h_per_split, xs);
   __syncthreads();
   if (e < E) {
-    float acc[kGemvTokens];
-    row_dot<kGemvTokens>(wr_t + (size_t)e * H + h0, xs, h_per_split, wv, acc);
+    float acc[NT];
+    row_dot<NT>(wr_t + (size_t)e * H + h0, xs, h_per_split, wv, acc);
     if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (t < T) z_part[((size_t)split * kGemvTokens + t) * E + e] = acc[t];
+      for (int t = 0; t < NT; ++t)
+        if (t < T) z_part[((size_t)split * NT + t) * E + e] = acc[t];
     }
   }
   // Last-CTA-done: publish the partials, take a ticket.
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   if (threadIdx.x == 0) *status = kStatusOk;
   // Top-k: warp t handles token t.
   if (warp < T)
-    topk_token<EPL>(z_part, gridDim.y, kGemvTokens, warp, E, k, r, bias, idx, w, true);
+    topk_token<EPL>(z_part, gridDim.y, NT, warp, E, k, r, bias, idx, w, true);
   __syncthreads();
   // Stable counting sort of the A = T*k assignments (A <= 128, E <= 1024).
   __shared__ int cnt[kMaxExperts];
@@ -540,13 +540,20 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   }
 }
 
-int router_splits(int T, int E, int H, int num_sms) {
-  if (T > 4) return 1;
+// Split-K partitions of the GEMV router over H (T <= 4 on the route-only
+// path; any T <= kRouteTokens in the fused routing launch).
+int gemv_splits(int E, int H, int num_sms) {
   const int blocks_e = (E + 7) / 8;
   int s = 1;
-  // Split H until there are about two blocks per SM, keeping 128-float slices.
-  while (s < kRouterSplitMax && blocks_e * s < 2 * num_sms && (H % (2 * s * 128)) == 0) s *= 2;
+  // Split H until the grid covers the SMs once (two blocks fit per SM, so the
+  // grid stays one wave and the last block to finish -- which does the top-k
+  // and the grouping -- starts early), keeping 128-float slices.
+  while (s < kRouterSplitMax && blocks_e * s < num_sms && (H % (2 * s * 128)) == 0) s *= 2;
   return s;
+}
+
+int router_splits(int T, int E, int H, int num_sms) {
+  return T > 4 ? 1 : gemv_splits(E, H, num_sms);
 }
 
 }  // namespace
@@ -554,24 +561,30 @@ int router_splits(int T, int E, int H, int num_sms) {
 cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
                                unsigned long long *usage, cudaStream_t st) {
   const int E = h->E, H = h->H, k = h->k;
-  const int splits = router_splits(T, E, H, h->num_sms);
+  const int splits = gemv_splits(E, H, h->num_sms);
   const int hps = H / splits;
-  const size_t smem = (size_t)4 * hps * sizeof(float);
+  const int nt = T <= 4 ? 4 : kRouteTokens;
+  const size_t smem = (size_t)nt * hps * sizeof(float);
   const int epl = (E + 31) / 32;
   const dim3 grid((E + 7) / 8, splits);
   const moe::Workspace &w = h->ws;
-#define MOE_RS(N)                                                                               \
+#define MOE_RS2(N, NTT)                                                                         \
   do {                                                                                          \
     if (smem > 48 * 1024) {                                                                     \
-      cudaError_t err = cudaFuncSetAttribute(route_small_kernel<N>,                             \
+      cudaError_t err = cudaFuncSetAttribute(route_small_kernel<N, NTT>,                        \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,       \
                                              (int)smem);                                        \
       if (err != cudaSuccess) return err;                                                       \
     }                                                                                           \
-    route_small_kernel<N><<<grid, 256, smem, st>>>(                                             \
+    route_small_kernel<N, NTT><<<grid, 256, smem, st>>>(                                        \
         x, h->L.x_dtype == 1, T, H, E, k, route_rule(h), h->wr_t, h->bias, hps, w.z_part,       \
         w.ticket, h->S, w.idx, w.w, w.counts,                                                   \
         w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);   \
+  } while (0)
+#define MOE_RS(N)                                                                               \
+  do {                                                                                          \
+    if (nt == 4) MOE_RS2(N, 4);                                                                 \
+    else MOE_RS2(N, kRouteTokens);                                                              \
   } while (0)
   if (epl <= 1) MOE_RS(1);
   else if (epl <= 2) MOE_RS(2);
@@ -580,6 +593,7 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   else if (epl <= 16) MOE_RS(16);
   else MOE_RS(32);
 #undef MOE_RS
+#undef MOE_RS2
   return cudaGetLastError();
 }
 

@@ -54,10 +54,12 @@
  *                [H][Is/2],[H][Is/64]; NULL when n_shared == 0
  * Experts are contiguous by id (tutorial cf-1.com §3.1: base + id * size).
  *
- * Numerics.  Routing, dispatch and the small-T expert path (T <= 4 by default)
- * compute in f32.  The large-T expert path feeds the tensor cores with
- * bf16(q * s) weights and bf16 activations and accumulates in f32.  The
- * output is f32.  Results are bitwise identical from run to run.
+ * Numerics.  Routing, dispatch and the decode expert paths (T <= 8 by default:
+ * the SIMT GEMV path for one token, the exact tensor-core path for 2-8) compute
+ * in f32: exact int4 codes, f32 (or exactly split bf16 hi/lo) operands, f32
+ * group scales and accumulation.  The large-T expert path feeds the tensor
+ * cores with bf16(q * s) weights and bf16 activations and accumulates in f32.
+ * The output is f32.  Results are bitwise identical from run to run.
  *
  * Return codes (extending the pages' 0 / -1 / -2 / -3):
  */
@@ -262,10 +264,11 @@ int moe_route_noalloc(const void *x, int T, int hidden, int num_experts, int top
 int moe_debug_read(moe_handle *h, int field, void *host_dst, size_t bytes);
 
 /* Stage times of the last forward with MOE_OPT_PROFILE on (synchronises).
- * T <= 4: route (router, top-k and dispatch in one kernel), then w13, w2,
- * combine (small-T path) or gather, w13, w2, combine (tensor-core path).
- * T > 4: router, dispatch, then the same expert stages.  Writes up to `max` values in ms and the
- * stage count to *n; names[i] (optional) receives static strings. */
+ * T <= 8: route (router, top-k and dispatch in one kernel), then w13, w2,
+ * combine (GEMV path) or gather, w13, w2, combine (tensor-core paths).
+ * T > 8: router, dispatch, then the same expert stages.  Writes up to `max`
+ * values in ms and the stage count to *n; names[i] (optional) receives static
+ * strings. */
 int moe_stage_times(moe_handle *h, float *ms, const char **names, int max, int *n);
 
 /* Synchronises the handle's last stream and returns its device status word
