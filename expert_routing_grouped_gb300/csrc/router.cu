@@ -12,6 +12,7 @@
 // ggemm_tc.cu) so the selection matches an exact reference whenever the top
 // keys are separated by more than f32 rounding.  No TF32.
 // Every reduction runs in a fixed order, so results are bitwise reproducible.
+#include <algorithm>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -218,15 +219,31 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(
 // keeps slot j while the shares of the slots before it sum below top_p (slot
 // 0 always), gives the dropped slots id -1 and weight 0, and (modes 0 and 1)
 // renormalises over the kept slots.  Split partial logits are summed in
-// split order; `coherent` reads them through L2 (written by other CTAs of the
-// same kernel).  Every sum runs in a fixed order.
+// split order.  Every sum runs in a fixed order.
+
+// Selection key and score of one expert from its logit zz and bias b.
+__device__ __forceinline__ void key_of(float zz, float b, int mode, float &key, float &val) {
+  if (mode != 1) {
+    key = zz + b;
+    val = key;
+  } else {
+    const float sc = 1.0f / (1.0f + expf(-zz));
+    val = sc;
+    key = sc + b;
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int t, int E, int k,
+                                            const RouteRule r, int32_t *__restrict__ idx_out,
+                                            float *__restrict__ w_out);
+
 template <int EPL>
 __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int splits,
                                            int zstride, int t, int E, int k, const RouteRule r,
                                            const float *__restrict__ bias,
                                            int32_t *__restrict__ idx_out,
-                                           float *__restrict__ w_out, bool coherent) {
-  const unsigned full = 0xffffffffu;
+                                           float *__restrict__ w_out) {
   const int lane = threadIdx.x & 31;
   float key[EPL], val[EPL];
 #pragma unroll
@@ -238,25 +255,26 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
       // Issue all split loads before summing (in split order).
       float part[kRouterSplitMax];
 #pragma unroll
-      for (int s = 0; s < kRouterSplitMax; ++s) {
-        const float *src = z_part + ((size_t)s * zstride + t) * E + e;
-        part[s] = (s < splits) ? (coherent ? __ldcg(src) : *src) : 0.f;
-      }
+      for (int s = 0; s < kRouterSplitMax; ++s)
+        part[s] = (s < splits) ? z_part[((size_t)s * zstride + t) * E + e] : 0.f;
       float zz = 0.f;
 #pragma unroll
       for (int s = 0; s < kRouterSplitMax; ++s)
         if (s < splits) zz += part[s];
-      const float b = bias ? bias[e] : 0.f;
-      if (r.mode != 1) {
-        key[i] = zz + b;
-        val[i] = key[i];
-      } else {
-        const float sc = 1.0f / (1.0f + expf(-zz));
-        val[i] = sc;
-        key[i] = sc + b;
-      }
+      key_of(zz, bias ? bias[e] : 0.f, r.mode, key[i], val[i]);
     }
   }
+  topk_select<EPL>(key, val, t, E, k, r, idx_out, w_out);
+}
+
+// The selection of topk_token from the token's keys and scores (expert e in
+// lane e % 32, slot e / 32; -inf keys past E).
+template <int EPL>
+__device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int t, int E, int k,
+                                            const RouteRule r, int32_t *__restrict__ idx_out,
+                                            float *__restrict__ w_out) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
   if (r.n_group > 1) {
     // Lane g holds group g's score: the sum of its two largest keys.
     const int gsz = E / r.n_group;
@@ -385,7 +403,7 @@ __global__ void __launch_bounds__(256, 1) router_topk_kernel(
     float *__restrict__ w_out) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_token<EPL>(z_part, splits, zstride, t, E, k, r, bias, idx_out, w_out, false);
+  topk_token<EPL>(z_part, splits, zstride, t, E, k, r, bias, idx_out, w_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -435,9 +453,30 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   if (!last) return;
   __threadfence();
   if (threadIdx.x == 0) *status = kStatusOk;
-  // Top-k: warp t handles token t.
-  if (warp < T)
-    topk_token<EPL>(z_part, gridDim.y, NT, warp, E, k, r, bias, idx, w, true);
+  // Logits of every (token, expert) from the split partials (summed in split
+  // order, read through L2: other CTAs wrote them), their keys and scores into
+  // shared memory -- all threads at once, so the partials cost one round trip.
+  float *ks = xs, *vs = xs + T * E;
+  const int splits = gridDim.y;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
+    const int t = i / E, e = i - t * E;
+    float zz = 0.f;
+    for (int s = 0; s < splits; ++s) zz += __ldcg(z_part + ((size_t)s * NT + t) * E + e);
+    key_of(zz, bias ? bias[e] : 0.f, r.mode, ks[i], vs[i]);
+  }
+  __syncthreads();
+  // Top-k: warp t selects for token t.
+  if (warp < T) {
+    float key[EPL], val[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < E ? ks[warp * E + e] : -INFINITY;
+      val[i] = e < E ? vs[warp * E + e] : 0.f;
+    }
+    topk_select<EPL>(key, val, warp, E, k, r, idx, w);
+  }
   __syncthreads();
   // Stable counting sort of the A = T*k assignments (A <= 128, E <= 1024).
   __shared__ int cnt[kMaxExperts];
@@ -564,7 +603,8 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   const int splits = gemv_splits(E, H, h->num_sms);
   const int hps = H / splits;
   const int nt = T <= 4 ? 4 : kRouteTokens;
-  const size_t smem = (size_t)nt * hps * sizeof(float);
+  // x staging for the GEMV, then the keys and scores of the last CTA's top-k.
+  const size_t smem = (size_t)std::max(nt * hps, 2 * T * E) * sizeof(float);
   const int epl = (E + 31) / 32;
   const dim3 grid((E + 7) / 8, splits);
   const moe::Workspace &w = h->ws;
