@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_DEVICE, MOE_ERR_ARG = 0, -1, -2, -3, -4
 MOE_ERR_IO, MOE_ERR_ENGINE = -5, -6
-MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE, MOE_OPT_USAGE = 1, 2, 3, 4
+MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE, MOE_OPT_USAGE, MOE_OPT_PDL = 1, 2, 3, 4, 5
 REGIME_AUTO, REGIME_GEMV, REGIME_TC, REGIME_TC_EXACT = 0, 1, 2, 3
 ROUTER_SOFTMAX, ROUTER_SIGMOID, ROUTER_SOFTMAX_RAW = 0, 1, 2
 X_F32, X_BF16 = 0, 1

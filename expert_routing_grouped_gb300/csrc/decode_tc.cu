@@ -130,9 +130,9 @@ __device__ __forceinline__ void load_slot(const DecParams &p, const Geo &q, Cur 
     c.wbase = 0;
     c.p0 = p.A;
   } else {
-    c.e = __ldg(p.active + c.a);
+    c.e = __ldcg(p.active + c.a);
     c.wbase = c.e * p.rows;
-    c.p0 = __ldg(p.offsets + c.e);
+    c.p0 = __ldcg(p.offsets + c.e);
   }
 }
 
@@ -244,7 +244,7 @@ __device__ void finish_rb(const DecParams &p, const Geo &q, int pp, const Cur &c
       for (int t = 0; t < NT; ++t) tot[t] += __ldcg(src + t);
     }
   }
-  const int cnt = sh ? p.T : __ldg(p.offsets + c.e + 1) - c.p0;
+  const int cnt = sh ? p.T : __ldcg(p.offsets + c.e + 1) - c.p0;
   if (p.mode == 0) {
     // Rows of the block: quadrant qd holds the W1 rows of features rb*64 +
     // 16 qd + (lane & 15) in lanes 0-15 and the W3 rows of the same in 16-31.
@@ -265,7 +265,7 @@ __device__ void finish_rb(const DecParams &p, const Geo &q, int pp, const Cur &c
     const int o = c.rb * 128 + r;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
-      if (t < cnt) p.y[(size_t)(c.p0 + t) * p.H + o] = tot[t] * __ldg(p.wperm + c.p0 + t);
+      if (t < cnt) p.y[(size_t)(c.p0 + t) * p.H + o] = tot[t] * __ldcg(p.wperm + c.p0 + t);
   }
 }
 
@@ -273,6 +273,7 @@ __device__ void finish_rb(const DecParams &p, const Geo &q, int pp, const Cur &c
 // token (1: bf16 x; 2: hi/lo planes of f32 x or of h).
 template <int NT, int PL>
 __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant__ DecParams p) {
+  pdl_enter();
   constexpr int NC = NT * PL;                 // accumulator columns read back
   static_assert(NC <= 16, "16 MMA columns");
   extern __shared__ uint8_t smem_raw[];
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
   tc_fence_after();
 
   Geo q;
-  q.n_r = __ldg(p.n_active) - p.S;
+  q.n_r = __ldcg(p.n_active) - p.S;
   q.RB = p.rows / 128;
   q.G4 = p.K / 256;
   q.RBs = p.rows_s / 128;
@@ -467,7 +468,8 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
 }
 
 template <int PL>
-cudaError_t launch_pass(const DecParams &p, int T, int grid, cudaStream_t st) {
+cudaError_t launch_pass(const DecParams &p, int T, int grid, bool pdl, cudaStream_t st) {
+  cudaError_t err = cudaSuccess;
 #define MOE_DEC(NT)                                                                          \
   do {                                                                                       \
     static bool attr = false;                                                                \
@@ -478,14 +480,14 @@ cudaError_t launch_pass(const DecParams &p, int T, int grid, cudaStream_t st) {
       if (e != cudaSuccess) return e;                                                        \
       attr = true;                                                                           \
     }                                                                                        \
-    decode_tc_kernel<NT, PL><<<grid, DT, kDecSmem, st>>>(p);                                 \
+    err = launch_k(pdl, decode_tc_kernel<NT, PL>, dim3(grid), dim3(DT), kDecSmem, st, p);     \
   } while (0)
   if (T <= 1) MOE_DEC(1);
   else if (T <= 2) MOE_DEC(2);
   else if (T <= 4) MOE_DEC(4);
   else MOE_DEC(8);
 #undef MOE_DEC
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
@@ -543,7 +545,8 @@ cudaError_t launch_decode_tc(const moe_handle *h, const void *x, int T, float *o
   p.ticket = w.dec_ticket;
   p.ticket_other = w.dec_ticket + h->dec_rb_max;
   p.n_ticket_other = h->dec_rb_max;
-  err = xplanes == 1 ? launch_pass<1>(p, T, h->num_sms, st) : launch_pass<2>(p, T, h->num_sms, st);
+  err = xplanes == 1 ? launch_pass<1>(p, T, h->num_sms, h->pdl, st)
+                     : launch_pass<2>(p, T, h->num_sms, h->pdl, st);
   if (err != cudaSuccess) return err;
   hm->launches += 1;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
@@ -566,7 +569,7 @@ cudaError_t launch_decode_tc(const moe_handle *h, const void *x, int T, float *o
   p.K_s = Is;
   p.ticket = w.dec_ticket + h->dec_rb_max;
   p.ticket_other = w.dec_ticket;
-  err = launch_pass<2>(p, T, h->num_sms, st);
+  err = launch_pass<2>(p, T, h->num_sms, h->pdl, st);
   if (err != cudaSuccess) return err;
   hm->launches += 1;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {

@@ -57,6 +57,18 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
     int32_t *__restrict__ inv, int32_t *__restrict__ active, int32_t *__restrict__ n_active,
     int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles, int32_t *__restrict__ status,
     unsigned long long *__restrict__ usage) {
+  pdl_enter();
+  idx = after_wait(idx);
+  counts = after_wait(counts);
+  offsets = after_wait(offsets);
+  perm = after_wait(perm);
+  inv = after_wait(inv);
+  active = after_wait(active);
+  n_active = after_wait(n_active);
+  tiles = after_wait(tiles);
+  n_tiles = after_wait(n_tiles);
+  status = after_wait(status);
+  usage = after_wait(usage);
   extern __shared__ int smem[];
   int *cnt = smem;                 // [E]
   int *base = cnt + E;             // [E]
@@ -177,10 +189,9 @@ cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned lon
     attr_set = true;
   }
   const moe::Workspace &w = h->ws;
-  dispatch_kernel<<<1, kThreads, smem, st>>>(w.idx, T, h->k, h->E, h->S, tile_m, w.counts,
-                                             w.offsets, w.perm, w.inv, w.active, w.n_active,
-                                             w.tiles, w.n_tiles, w.status, usage);
-  return cudaGetLastError();
+  return launch_k(h->pdl, dispatch_kernel, dim3(1), dim3(kThreads), smem, st, w.idx, T, h->k, h->E,
+                  h->S, tile_m, w.counts, w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles,
+                  w.n_tiles, w.status, usage);
 }
 
 }  // namespace moe

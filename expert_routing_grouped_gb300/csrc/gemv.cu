@@ -119,6 +119,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(
     const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     const float *__restrict__ wts, float *__restrict__ out, int out_stride) {
+  pdl_enter();
+  act = after_wait(act);
+  active = after_wait(active);
+  n_active_p = after_wait(n_active_p);
+  offsets = after_wait(offsets);
+  perm = after_wait(perm);
+  wts = after_wait(wts);
+  out = after_wait(out);
   extern __shared__ float act_s[];   // [NT][K] activations of the current expert pass
   __shared__ float wt_s[NT];         // W2: routing weights of the staged tokens
   const int n_active = *n_active_p;
@@ -170,14 +178,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(
             // W13 reads the token's x row; W2 reads the grouped position's h row.
             const int src = (mode == 0) ? ((e < E) ? perm[p] / k : p - A) : p;
             if (act_is_bf16) {
-              const uint2 u = __ldg(reinterpret_cast<const uint2 *>(
+              const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(
                                         reinterpret_cast<const __nv_bfloat16 *>(act) +
                                         (size_t)src * act_stride) +
                                     c4);
               v = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                               __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
             } else {
-              v = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(act) +
+              v = __ldcg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(act) +
                                                          (size_t)src * act_stride) +
                         c4);
             }
@@ -321,6 +329,13 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
     const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     float *__restrict__ out, int out_stride) {
+  pdl_enter();
+  act = after_wait(act);
+  active = after_wait(active);
+  n_active_p = after_wait(n_active_p);
+  offsets = after_wait(offsets);
+  perm = after_wait(perm);
+  out = after_wait(out);
   extern __shared__ uint4 smem_v[];
   // [NT][K/8] 16-byte groups of bf16 activations: group j of 32-wide chunk c at
   // slot j ^ ((c >> 1) & 3), so 8 lanes reading the same j of chunks c..c+7
@@ -366,7 +381,7 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
             const int src = (e < E) ? perm[p] / k : p - A;
             const uint4 *row = reinterpret_cast<const uint4 *>(act + (size_t)src * act_stride) + c * 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __ldg(row + j);
+            for (int j = 0; j < 4; ++j) v[j] = __ldcg(row + j);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
@@ -490,11 +505,10 @@ cudaError_t launch_w13_bf16(const moe_handle *h, const __nv_bfloat16 *x, int T, 
       per_sm < 1)
     per_sm = 1;
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  gemv_w13_bf16_kernel<NT><<<h->num_sms * per_sm, kWarps * 32, smem, st>>>(
-      x, h->H, T, h->k, h->E, K, 2 * h->I, h->S ? 2 * h->Is : 0, h->ex.w13q, h->ex.w13s,
-      h->sh.w13q, h->sh.w13s, h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.h,
-      h_stride);
-  return cudaGetLastError();
+  return launch_k(h->pdl, gemv_w13_bf16_kernel<NT>, dim3(h->num_sms * per_sm), dim3(kWarps * 32),
+                  smem, st, x, h->H, T, h->k, h->E, K, 2 * h->I, h->S ? 2 * h->Is : 0,
+                  h->ex.w13q, h->ex.w13s, h->sh.w13q, h->sh.w13s, h->ws.active, h->ws.n_active,
+                  h->ws.offsets, h->ws.perm, h->ws.h, h_stride);
 }
 
 template <int NT>
@@ -518,10 +532,10 @@ cudaError_t launch_nt(int mode, const moe_handle *h, const void *act, int act_bf
       per_sm < 1)
     per_sm = 1;
   const int blocks = h->num_sms * per_sm;
-  gemv_kernel<NT><<<blocks, kWarps * 32, smem, st>>>(
-      mode, act, act_bf16, act_stride, T, h->k, h->E, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s, ws_s,
-      h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.w, out, out_stride);
-  return cudaGetLastError();
+  return launch_k(h->pdl, gemv_kernel<NT>, dim3(blocks), dim3(kWarps * 32), smem, st, mode, act,
+                  act_bf16, act_stride, T, h->k, h->E, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
+                  ws_s, h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.w, out,
+                  out_stride);
 }
 
 // Tokens per pass: up to 4, as many as fit 96 KB of f32 activations.

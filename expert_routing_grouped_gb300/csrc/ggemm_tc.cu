@@ -164,6 +164,7 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
 // A = bf16(q * s) per weight (the scale applied in the dequant), one
 // accumulator per tile, bf16 h out of W13.
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   SmemTC *sm = reinterpret_cast<SmemTC *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -479,8 +480,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
                                                      const float *__restrict__ w,
                                                      __nv_bfloat16 *__restrict__ xp,
                                                      float *__restrict__ wperm) {
+  pdl_enter();
+  perm = after_wait(perm);
+  n_assigned = after_wait(n_assigned);
+  w = after_wait(w);
+  xp = after_wait(xp);
+  wperm = after_wait(wperm);
   const int A = T * k, R = A + n_shared * T;
-  const int n_routed = __ldg(n_assigned);
+  const int n_routed = __ldcg(n_assigned);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   for (int pr = warp; pr < R; pr += nwarps) {
@@ -525,8 +532,14 @@ __global__ void __launch_bounds__(256) gather_exact_kernel(const void *__restric
                                                            const float *__restrict__ w,
                                                            __nv_bfloat16 *__restrict__ xe,
                                                            float *__restrict__ wperm) {
+  pdl_enter();
+  perm = after_wait(perm);
+  n_assigned = after_wait(n_assigned);
+  w = after_wait(w);
+  xe = after_wait(xe);
+  wperm = after_wait(wperm);
   const int A = T * k, R = A + n_shared * T;
-  const int n_routed = __ldg(n_assigned);
+  const int n_routed = __ldcg(n_assigned);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   for (int pr = warp; pr < R; pr += nwarps) {
@@ -571,6 +584,10 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
                                                       const int32_t *__restrict__ inv,
                                                       const float *__restrict__ y,
                                                       float *__restrict__ out, int accumulate) {
+  pdl_enter();
+  inv = after_wait(inv);
+  y = after_wait(y);
+  out = after_wait(out);
   const int A = T * k;
   const int per_t = H / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * per_t;
@@ -578,16 +595,16 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
     const int t = (int)(i / per_t), c = (int)(i - (long long)t * per_t);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-      const int row = __ldg(inv + t * k + j);
+      const int row = __ldcg(inv + t * k + j);
       if (row < 0) continue;   // a slot the top-p trim dropped
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)row * H) + c);
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + (size_t)row * H) + c);
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
       acc.w += v.w;
     }
     if (n_shared) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + (size_t)(A + t) * H) + c);
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + (size_t)(A + t) * H) + c);
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -658,6 +675,7 @@ __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *
 }
 
 __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant__ RtParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   SmemRT *sm = reinterpret_cast<SmemRT *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -853,8 +871,8 @@ cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z
   p.H = H;
   p.z = z;
   p.status = h->ws.status;
-  router_tc_kernel<<<dim3((E + BM - 1) / BM, (T + RT_N - 1) / RT_N), 256, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(false, router_tc_kernel, dim3((E + BM - 1) / BM, (T + RT_N - 1) / RT_N),
+                  dim3(256), smem, st, p);
 }
 
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
@@ -863,9 +881,8 @@ cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumula
   const long long work = (long long)T * (h->H / 4);
   const int blocks = (int)std::min<long long>((long long)h->num_sms * 8, (work + 255) / 256);
   if (blocks == 0) return cudaSuccess;
-  combine_kernel<<<blocks, 256, 0, st>>>(T, h->H, h->k, h->S, h->ws.inv, h->ws.y, out,
-                                         accumulate ? 1 : 0);
-  return cudaGetLastError();
+  return launch_k(h->pdl, combine_kernel, dim3(blocks), dim3(256), 0, st, T, h->H, h->k, h->S,
+                  h->ws.inv, h->ws.y, out, accumulate ? 1 : 0);
 }
 
 namespace {
@@ -884,9 +901,9 @@ cudaError_t set_tc_attrs() {
 
 cudaError_t launch_gather_exact(const moe_handle *h, const void *x, int T, cudaStream_t st) {
   const moe::Workspace &w = h->ws;
-  gather_exact_kernel<<<h->num_sms, 256, 0, st>>>(x, h->L.x_dtype == 1, T, h->H, h->k, h->S,
-                                                  w.perm, w.offsets + h->E, w.w, w.xe, w.wperm);
-  return cudaGetLastError();
+  return launch_k(h->pdl, gather_exact_kernel, dim3(h->num_sms), dim3(256), 0, st, x,
+                  h->L.x_dtype == 1, T, h->H, h->k, h->S, w.perm, w.offsets + h->E, w.w, w.xe,
+                  w.wperm);
 }
 
 cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out, bool accumulate,
@@ -899,10 +916,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   const int h_stride = I > Is ? I : Is;
   cudaError_t err = set_tc_attrs();
   if (err != cudaSuccess) return err;
-  gather_kernel<<<h->num_sms * 4, 256, 0, st>>>(x, h->L.x_dtype == 1, T, H, k, S, w.perm,
-                                                w.offsets + h->E, w.w,
-                                                w.xp, w.wperm);
-  err = cudaGetLastError();
+  err = launch_k(h->pdl, gather_kernel, dim3(h->num_sms * 4), dim3(256), 0, st, x,
+                 h->L.x_dtype == 1, T, H, k, S, w.perm, w.offsets + h->E, w.w, w.xp, w.wperm);
   if (err != cudaSuccess) return err;
   moe_handle *hm = const_cast<moe_handle *>(h);
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
@@ -943,8 +958,9 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.H = H;
   p.wperm = w.wperm;
   p.status = w.status;
-  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
+      cudaSuccess)
+    return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w13";
     cudaEventRecord(hm->ev[hm->n_ev++], st);
@@ -967,8 +983,9 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.K_s = Is;
   p.rows = H;
   p.rows_s = H;
-  ggemm_kernel<<<h->num_sms, kThreads, kSmemBytes, st>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
+      cudaSuccess)
+    return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
     hm->stage_names[hm->n_ev - 1] = "w2";
     cudaEventRecord(hm->ev[hm->n_ev++], st);

@@ -28,6 +28,7 @@ __global__ void transpose_kernel(const float *__restrict__ src, float *__restric
 __global__ void __launch_bounds__(1024) rmsnorm_bf16_kernel(const float *__restrict__ x, int H,
                                                             float eps,
                                                             __nv_bfloat16 *__restrict__ out) {
+  pdl_enter();
   __shared__ float part[32];
   const int t = blockIdx.x;
   const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)t * H);
@@ -166,8 +167,8 @@ cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, 
 cudaError_t launch_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
                                 cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_bf16_kernel<<<T, 1024, 0, s>>>(x, H, eps, reinterpret_cast<__nv_bfloat16 *>(out));
-  return cudaGetLastError();
+  return launch_k(false, rmsnorm_bf16_kernel, dim3(T), dim3(1024), 0, s, x, H, eps,
+                  reinterpret_cast<__nv_bfloat16 *>(out));
 }
 
 }  // namespace moe

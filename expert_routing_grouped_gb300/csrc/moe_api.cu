@@ -304,6 +304,7 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   h->x_elem = layout->x_dtype == 1 ? 2 : 4;
   h->regime_opt = 0;
   h->small_t_max = 1;
+  h->pdl = 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -415,6 +416,11 @@ __attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int opt
     }
     h->profile = value;
     h->n_ev = 0;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_PDL) {
+    if (value != 0 && value != 1) return MOE_ERR_ARG;
+    h->pdl = value;
     return MOE_OK;
   }
   if (option == MOE_OPT_USAGE) {

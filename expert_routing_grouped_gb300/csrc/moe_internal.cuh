@@ -71,6 +71,52 @@ struct Workspace {
   float *out_stage;   // [max_tokens][H]
 };
 
+// Programmatic dependent launch.  A kernel launched with launch_k(pdl = true)
+// may be scheduled while the previous kernel on the stream is still running;
+// it calls pdl_enter() first, which lets the next kernel be scheduled in turn
+// and then waits until the previous grid has finished and its writes are
+// visible -- so nothing it reads or writes can race with its predecessor,
+// and only the launch latency and the CTAs' start-up overlap.  Without the
+// launch attribute both instructions return at once.  The wait covers grids
+// only, not copies or memsets, so the first kernel of every library call is
+// launched plainly: only the library's own kernels within a call are chained.
+static __device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Workspace pointers of a chained kernel are taken through after_wait() once
+// pdl_enter() has returned.  A plain load through a const __restrict__
+// parameter counts as invariant for the kernel's whole life, so the compiler
+// may schedule it above the wait, where it reads what the previous forward
+// left there; a pointer that comes out of a volatile asm placed after the wait
+// carries no such guarantee, and every address derived from it depends on the
+// wait.  Data the predecessor wrote is read through L2 (plain loads or
+// __ldcg), not the read-only __ldg path: this grid is resident while it is
+// being written.
+template <typename T>
+static __device__ __forceinline__ T *after_wait(T *p) {
+  unsigned long long v = reinterpret_cast<unsigned long long>(p);
+  asm volatile("" : "+l"(v));
+  return reinterpret_cast<T *>(v);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args &&...args) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = pdl ? &attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace moe
 
 struct moe_handle {
@@ -88,6 +134,7 @@ struct moe_handle {
   size_t pool_bytes;
   int regime_opt;                // MOE_OPT_REGIME
   int small_t_max;               // MOE_OPT_SMALL_T_MAX
+  int pdl;                       // MOE_OPT_PDL
   int count_usage;               // MOE_OPT_USAGE
   int last_T;
   int last_regime;

@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E,
     const float *__restrict__ wr_t, int h_per_split, float *__restrict__ z_part,
     int zstride) {
+  pdl_enter();
   extern __shared__ float xs[];   // [NT][h_per_split]
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
@@ -164,6 +165,7 @@ constexpr int RG_BT = 64, RG_BE = 64, RG_BK = 16;
 __global__ void __launch_bounds__(256) router_gemm_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E,
     const float *__restrict__ wr_t, float *__restrict__ z) {
+  pdl_enter();
   __shared__ float xs[RG_BK][RG_BT + 4];
   __shared__ float ws[RG_BK][RG_BE + 4];
   const int t0 = blockIdx.y * RG_BT, e0 = blockIdx.x * RG_BE;
@@ -401,6 +403,10 @@ __global__ void __launch_bounds__(256, 1) router_topk_kernel(
     const float *__restrict__ z_part, int splits, int zstride, int T, int E, int k,
     const RouteRule r, const float *__restrict__ bias, int32_t *__restrict__ idx_out,
     float *__restrict__ w_out) {
+  pdl_enter();
+  z_part = after_wait(z_part);
+  idx_out = after_wait(idx_out);
+  w_out = after_wait(w_out);
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   topk_token<EPL>(z_part, splits, zstride, t, E, k, r, bias, idx_out, w_out);
@@ -424,6 +430,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(
     unsigned long long *__restrict__ usage) {
   extern __shared__ float xs[];   // [NT][h_per_split]
   __shared__ int last;
+  pdl_enter();
   const int split = blockIdx.y;
   const int h0 = split * h_per_split;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -608,18 +615,19 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   const int epl = (E + 31) / 32;
   const dim3 grid((E + 7) / 8, splits);
   const moe::Workspace &w = h->ws;
+  cudaError_t err = cudaSuccess;
 #define MOE_RS2(N, NTT)                                                                         \
   do {                                                                                          \
     if (smem > 48 * 1024) {                                                                     \
-      cudaError_t err = cudaFuncSetAttribute(route_small_kernel<N, NTT>,                        \
+      err = cudaFuncSetAttribute(route_small_kernel<N, NTT>,                                    \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,       \
                                              (int)smem);                                        \
       if (err != cudaSuccess) return err;                                                       \
     }                                                                                           \
-    route_small_kernel<N, NTT><<<grid, 256, smem, st>>>(                                        \
-        x, h->L.x_dtype == 1, T, H, E, k, route_rule(h), h->wr_t, h->bias, hps, w.z_part,       \
-        w.ticket, h->S, w.idx, w.w, w.counts,                                                   \
-        w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);   \
+    err = launch_k(false, route_small_kernel<N, NTT>, grid, dim3(256), smem, st, x,            \
+                   h->L.x_dtype == 1, T, H, E, k, route_rule(h), h->wr_t, h->bias, hps,         \
+                   w.z_part, w.ticket, h->S, w.idx, w.w, w.counts, w.offsets, w.perm, w.inv,     \
+                   w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);                  \
   } while (0)
 #define MOE_RS(N)                                                                               \
   do {                                                                                          \
@@ -634,7 +642,7 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   else MOE_RS(32);
 #undef MOE_RS
 #undef MOE_RS2
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t st) {
@@ -666,8 +674,8 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
   const int epl = (E + 31) / 32;
   const dim3 g2((T + 7) / 8);
 #define MOE_TOPK(N)                                                                          \
-  router_topk_kernel<N><<<g2, 256, 0, st>>>(h->ws.z_part, splits, zstride, T, E, k,          \
-                                            route_rule(h), h->bias, h->ws.idx, h->ws.w)
+  err = launch_k(h->pdl, router_topk_kernel<N>, g2, dim3(256), 0, st, h->ws.z_part, splits,   \
+                 zstride, T, E, k, route_rule(h), h->bias, h->ws.idx, h->ws.w)
   if (epl <= 1) MOE_TOPK(1);
   else if (epl <= 2) MOE_TOPK(2);
   else if (epl <= 4) MOE_TOPK(4);
@@ -675,7 +683,7 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
   else if (epl <= 16) MOE_TOPK(16);
   else MOE_TOPK(32);
 #undef MOE_TOPK
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace moe

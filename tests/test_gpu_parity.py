@@ -490,3 +490,42 @@ def test_decode_tc_repeatable_stress(dev, T):
     for o in outs[1:]:
         assert np.array_equal(o.cpu().numpy(), ref)
     h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+
+
+@pytest.mark.parametrize("T,regime", [(1, 0), (4, 0), (4, 1), (16, 0), (16, 1)])
+def test_pdl_bitwise_identical(dev, T, regime):
+    """Programmatic dependent launch changes scheduling only.  Forwards run
+    back to back with MOE_OPT_PDL on, alternating between two inputs, so a
+    chained kernel that read the workspace before its predecessor wrote it
+    would see the other input's values; every output must equal the
+    plain-launch output of its own input bit for bit (and chained residual
+    calls see each other)."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["glm_decode"]
+    h, Wr, bias = get_layer(wl, 16, dev)
+    h.set_option(moe.MOE_OPT_REGIME, regime)
+    xs = [torch.from_numpy(synth.x_rows(wl, T, attempts=np.full(T, a))).to(dev) for a in (0, 1)]
+    h.set_option(moe.MOE_OPT_PDL, 0)
+    ref = []
+    for x in xs:
+        out = torch.empty(T, wl.H, device=dev)
+        h.forward(x, T, out)
+        torch.cuda.synchronize()
+        ref.append(out.cpu().numpy())
+    assert not np.array_equal(ref[0], ref[1])
+    h.set_option(moe.MOE_OPT_PDL, 1)
+    outs = [torch.empty(T, wl.H, device=dev) for _ in range(6)]
+    for j, out in enumerate(outs):
+        h.forward(xs[j % 2], T, out)
+    resid = torch.zeros(T, wl.H, device=dev)
+    for j in range(3):
+        h.forward(xs[0], T, outs[0])   # the other input between residual calls
+        h.forward_residual(xs[1], T, resid)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
+    for j, out in enumerate(outs):
+        assert np.array_equal(out.cpu().numpy(), ref[j % 2]), j
+    three = ((ref[1] + ref[1]).astype(np.float32) + ref[1]).astype(np.float32)
+    assert np.array_equal(resid.cpu().numpy(), three)      # 0 + y + y + y, in call order
