@@ -105,7 +105,8 @@ void carve(moe_handle *h, Carver &c) {
   w.tiles = c.take<int32_t>(A / moe::kTileTokens + E + maxT / moe::kTileTokens + 2);
   w.n_tiles = c.take<int32_t>(2);
   w.status = c.take<int32_t>(1);
-  w.ticket = c.take<int32_t>(1);
+  w.ticket = c.take<int32_t>(1 + (E + 7) / 8);
+  w.route_kv = c.take<float>(2 * (size_t)moe::kRouteTokens * E);
   w.usage = c.take<unsigned long long>(E);
   w.h = c.take<float>(rows * Imax);
   w.hb = c.take<__nv_bfloat16>(rows * Imax);
@@ -325,7 +326,7 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   carve(h, c);
   rc = copy_weights(h, weights);
   if (rc == MOE_OK && (cudaMemset(h->ws.status, 0, 4) != cudaSuccess ||
-                       cudaMemset(h->ws.ticket, 0, 4) != cudaSuccess ||
+                       cudaMemset(h->ws.ticket, 0, (1 + (h->E + 7) / 8) * 4) != cudaSuccess ||
                        cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess ||
                        cudaMemset(h->ws.dec_ticket, 0, 2 * (size_t)h->dec_rb_max * 4) != cudaSuccess))
     rc = MOE_ERR_DEVICE;

@@ -53,7 +53,9 @@ struct Workspace {
   int32_t *tiles;     // [max_tiles] packed (expert, m-tile) for the tensor-core path
   int32_t *n_tiles;   // [2] tile count for W13 and W2 kernels
   int32_t *status;    // [1]
-  int32_t *ticket;    // [1] last-CTA-done counter of the fused small-T routing (self-resetting)
+  int32_t *ticket;    // [1 + ceil(E/8)] fused small-T routing, self-resetting: [0] the
+                      // last 8-expert block to finish, [1 + b] the last split of block b
+  float *route_kv;    // [2][kRouteTokens][E] fused small-T routing: keys, then scores
   unsigned long long *usage;  // [E] assignments per expert over the counted forwards
   // expert activations
   float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)

@@ -52,33 +52,61 @@ constexpr int kMaxRowVec = 12;
 template <int NT>
 __device__ __forceinline__ void stage_x(const void *__restrict__ x, int x_is_bf16, int T, int H,
                                         int h0, int hps, float *xs) {
+  constexpr int B = 4;   // vectors a thread loads before it converts and stores any
   if (x_is_bf16) {
     const int nv = hps / 8;                       // 8 bf16 per 16 bytes
-    for (int i = threadIdx.x; i < NT * nv; i += blockDim.x) {
-      const int t = i / nv, c = i - t * nv;
-      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-      if (t < T) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
-                                  reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + h0) +
-                              c);
-        lo = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                         __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-        hi = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
-                         __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+    for (int i0 = threadIdx.x; i0 < NT * nv; i0 += B * blockDim.x) {
+      uint4 u[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int i = i0 + b * blockDim.x;
+        const int t = i / nv, c = i - t * nv;
+        u[b] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < NT * nv && t < T)
+          u[b] = __ldg(reinterpret_cast<const uint4 *>(
+                           reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + h0) +
+                       c);
       }
-      reinterpret_cast<float4 *>(xs + t * hps)[2 * c] = lo;
-      reinterpret_cast<float4 *>(xs + t * hps)[2 * c + 1] = hi;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int i = i0 + b * blockDim.x;
+        if (i < NT * nv) {
+          const int t = i / nv, c = i - t * nv;
+          const float4 lo = make_float4(__uint_as_float(u[b].x << 16),
+                                        __uint_as_float(u[b].x & 0xFFFF0000u),
+                                        __uint_as_float(u[b].y << 16),
+                                        __uint_as_float(u[b].y & 0xFFFF0000u));
+          const float4 hi = make_float4(__uint_as_float(u[b].z << 16),
+                                        __uint_as_float(u[b].z & 0xFFFF0000u),
+                                        __uint_as_float(u[b].w << 16),
+                                        __uint_as_float(u[b].w & 0xFFFF0000u));
+          reinterpret_cast<float4 *>(xs + t * hps)[2 * c] = lo;
+          reinterpret_cast<float4 *>(xs + t * hps)[2 * c + 1] = hi;
+        }
+      }
     }
   } else {
     const int nv = hps / 4;
-    for (int i = threadIdx.x; i < NT * nv; i += blockDim.x) {
-      const int t = i / nv, c = i - t * nv;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < T)
-        v = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) +
-                                                   (size_t)t * H + h0) +
-                  c);
-      reinterpret_cast<float4 *>(xs + t * hps)[c] = v;
+    for (int i0 = threadIdx.x; i0 < NT * nv; i0 += B * blockDim.x) {
+      float4 v[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int i = i0 + b * blockDim.x;
+        const int t = i / nv, c = i - t * nv;
+        v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < NT * nv && t < T)
+          v[b] = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) +
+                                                        (size_t)t * H + h0) +
+                       c);
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int i = i0 + b * blockDim.x;
+        if (i < NT * nv) {
+          const int t = i / nv, c = i - t * nv;
+          reinterpret_cast<float4 *>(xs + t * hps)[c] = v[b];
+        }
+      }
     }
   }
 }
@@ -269,65 +297,70 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ z_part, int
   topk_select<EPL>(key, val, t, E, k, r, idx_out, w_out);
 }
 
-// The selection of topk_token from the token's keys and scores (expert e in
-// lane e % 32, slot e / 32; -inf keys past E).
+// Group-limited selection (n_group > 1): lane g of the warp computes group g's
+// score, the sum of its two largest keys; the keys of experts outside the
+// topk_group best groups (ties to the lower group) drop to -inf.
 template <int EPL>
-__device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int t, int E, int k,
-                                            const RouteRule r, int32_t *__restrict__ idx_out,
-                                            float *__restrict__ w_out) {
+__device__ __forceinline__ void group_mask(float key[EPL], int E, const RouteRule r) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
-  if (r.n_group > 1) {
-    // Lane g holds group g's score: the sum of its two largest keys.
-    const int gsz = E / r.n_group;
-    float my_gs = -INFINITY;
-    for (int g = 0; g < r.n_group; ++g) {
-      float a = -INFINITY, b2 = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e >= g * gsz && e < (g + 1) * gsz) {
-          const float v = key[i];
-          if (v > a) {
-            b2 = a;
-            a = v;
-          } else if (v > b2) {
-            b2 = v;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {   // merge two top-2 lists
-        const float oa = __shfl_xor_sync(full, a, o), ob = __shfl_xor_sync(full, b2, o);
-        b2 = fmaxf(fminf(a, oa), fmaxf(b2, ob));
-        a = fmaxf(a, oa);
-      }
-      if (lane == g) my_gs = a + b2;
-    }
-    int gkept = 0;   // lane g: group g is eligible
-    for (int j = 0; j < r.topk_group; ++j) {
-      float bv = gkept ? -INFINITY : my_gs;
-      int bg = lane;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(full, bv, o);
-        const int og = __shfl_xor_sync(full, bg, o);
-        if (ov > bv || (ov == bv && og < bg)) {
-          bv = ov;
-          bg = og;
-        }
-      }
-      if (lane == bg) gkept = 1;
-    }
+  const int gsz = E / r.n_group;
+  float my_gs = -INFINITY;
+  for (int g = 0; g < r.n_group; ++g) {
+    float a = -INFINITY, b2 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      const int g = (e < E) ? e / gsz : 0;
-      if (!__shfl_sync(full, gkept, g)) key[i] = -INFINITY;
+      if (e >= g * gsz && e < (g + 1) * gsz) {
+        const float v = key[i];
+        if (v > a) {
+          b2 = a;
+          a = v;
+        } else if (v > b2) {
+          b2 = v;
+        }
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {   // merge two top-2 lists
+      const float oa = __shfl_xor_sync(full, a, o), ob = __shfl_xor_sync(full, b2, o);
+      b2 = fmaxf(fminf(a, oa), fmaxf(b2, ob));
+      a = fmaxf(a, oa);
+    }
+    if (lane == g) my_gs = a + b2;
   }
-  int my_idx = -1;
-  float my_val = 0.f;
+  int gkept = 0;   // lane g: group g is eligible
+  for (int j = 0; j < r.topk_group; ++j) {
+    float bv = gkept ? -INFINITY : my_gs;
+    int bg = lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, o);
+      const int og = __shfl_xor_sync(full, bg, o);
+      if (ov > bv || (ov == bv && og < bg)) {
+        bv = ov;
+        bg = og;
+      }
+    }
+    if (lane == bg) gkept = 1;
+  }
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    const int g = (e < E) ? e / gsz : 0;
+    if (!__shfl_sync(full, gkept, g)) key[i] = -INFINITY;
+  }
+}
+
+// k rounds of a warp argmax (larger key first, lower id on ties): lane j < k
+// ends with slot j's expert and score.
+template <int EPL>
+__device__ __forceinline__ void argmax_rounds(float key[EPL], const float val[EPL], int k,
+                                              int &my_idx, float &my_val) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  my_idx = -1;
+  my_val = 0.f;
   for (int j = 0; j < k; ++j) {
     float bk = -INFINITY;
     int be = 0x7fffffff;
@@ -364,6 +397,19 @@ __device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int 
       my_val = v;
     }
   }
+}
+
+// Weights of the k slots (lane j < k holds slot j's expert and score), the
+// top-p trim, and the writes of token t's ids and weights.  val holds every
+// expert's score (mode 2 divides by the sum over all of them).  sidx (or
+// nullptr) also receives the ids.
+template <int EPL>
+__device__ __forceinline__ void slot_weights(int my_idx, float my_val, const float val[EPL], int t,
+                                             int E, int k, const RouteRule r,
+                                             int32_t *__restrict__ idx_out,
+                                             float *__restrict__ w_out, int *sidx) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
   // Numerators, and the sum over the selection in slot order.
   const float top = __shfl_sync(full, my_val, 0);
   float num = 0.f;
@@ -395,7 +441,21 @@ __device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int 
     const bool keep = lane < kept;
     idx_out[(size_t)t * k + lane] = keep ? my_idx : -1;
     w_out[(size_t)t * k + lane] = keep ? num / (r.mode == 2 ? all : norm) * r.rsf : 0.f;
+    if (sidx) sidx[t * k + lane] = keep ? my_idx : -1;
   }
+}
+
+// The selection of topk_token from the token's keys and scores (expert e in
+// lane e % 32, slot e / 32; -inf keys past E).
+template <int EPL>
+__device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int t, int E, int k,
+                                            const RouteRule r, int32_t *__restrict__ idx_out,
+                                            float *__restrict__ w_out) {
+  if (r.n_group > 1) group_mask<EPL>(key, E, r);
+  int my_idx;
+  float my_val;
+  argmax_rounds<EPL>(key, val, k, my_idx, my_val);
+  slot_weights<EPL>(my_idx, my_val, val, t, E, k, r, idx_out, w_out, nullptr);
 }
 
 template <int EPL>
@@ -413,16 +473,18 @@ __global__ void __launch_bounds__(256, 1) router_topk_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// T <= 4 in one launch: the split-K router GEMV of router_gemv_kernel, then the
-// last CTA to finish (an atomic ticket, reset by that CTA for the next call;
-// nothing waits) reads every partial through L2, takes the top-k of each token
-// and groups the T*k <= 128 assignments by expert with the same stable
-// counting sort as dispatch.cu.  Also clears the status word first.
+// T <= kRouteTokens in one launch: the split-K router GEMV of
+// router_gemv_kernel, then the last CTA to finish (an atomic ticket, reset by
+// that CTA for the next call; nothing waits) reads every partial through L2,
+// takes the top-k of each token and groups the T*k assignments by expert --
+// the stable counting sort of dispatch.cu, written out from ranks.  Also
+// clears the status word first.
 template <int EPL, int NT>
 __global__ void __launch_bounds__(256) route_small_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, const RouteRule r,
     const float *__restrict__ wr_t, const float *__restrict__ bias, int h_per_split,
-    float *__restrict__ z_part, int32_t *__restrict__ ticket, int n_shared,
+    float *__restrict__ z_part, int32_t *__restrict__ ticket, float *__restrict__ route_kv,
+    int n_shared,
     int32_t *__restrict__ idx, float *__restrict__ w, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
     int32_t *__restrict__ active, int32_t *__restrict__ n_active, int32_t *__restrict__ tiles,
@@ -448,11 +510,45 @@ __global__ void __launch_bounds__(256) route_small_kernel(
         if (t < T) z_part[((size_t)split * NT + t) * E + e] = acc[t];
     }
   }
-  // Last-CTA-done: publish the partials, take a ticket.
+  // Last-CTA-done.  For more than one token, two levels: the last split CTA
+  // of each 8-expert block sums the block's partials in split order (read
+  // through L2: other CTAs wrote them) and writes its keys and scores, and the
+  // last block to finish takes the top-k and groups.  For one token the extra
+  // round trip costs more than it saves: the last CTA of the whole grid sums
+  // every partial itself.  The tickets reset themselves for the next call;
+  // nothing waits.
+  const int splits = gridDim.y;
+  float *kg = route_kv, *vg = route_kv + kRouteTokens * E;   // [T][E] keys, scores
   __threadfence();
   __syncthreads();
+  if (T > 1) {
+    if (threadIdx.x == 0) {
+      last = (atomicAdd(ticket + 1 + blockIdx.x, 1) == splits - 1);
+      if (last) ticket[1 + blockIdx.x] = 0;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if ((int)threadIdx.x < T * 8) {
+      const int t = threadIdx.x >> 3, eb = blockIdx.x * 8 + (threadIdx.x & 7);
+      if (eb < E) {
+        const float b = bias ? __ldg(bias + eb) : 0.f;
+        float part[kRouterSplitMax];
+#pragma unroll
+        for (int sp = 0; sp < kRouterSplitMax; ++sp)
+          part[sp] = sp < splits ? __ldcg(z_part + ((size_t)sp * NT + t) * E + eb) : 0.f;
+        float zz = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kRouterSplitMax; ++sp)
+          if (sp < splits) zz += part[sp];
+        key_of(zz, b, r.mode, kg[t * E + eb], vg[t * E + eb]);
+      }
+    }
+    __threadfence();
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    const int n = gridDim.x * gridDim.y;
+    const int n = T > 1 ? (int)gridDim.x : (int)(gridDim.x * gridDim.y);
     last = (atomicAdd(ticket, 1) == n - 1);
     if (last) *ticket = 0;
   }
@@ -460,20 +556,47 @@ __global__ void __launch_bounds__(256) route_small_kernel(
   if (!last) return;
   __threadfence();
   if (threadIdx.x == 0) *status = kStatusOk;
-  // Logits of every (token, expert) from the split partials (summed in split
-  // order, read through L2: other CTAs wrote them), their keys and scores into
-  // shared memory -- all threads at once, so the partials cost one round trip.
+  // Every (token, expert) key and score into shared memory; a batch's loads
+  // are all issued before its stores or sums.
   float *ks = xs, *vs = xs + T * E;
-  const int splits = gridDim.y;
-#pragma unroll 4
-  for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
-    const int t = i / E, e = i - t * E;
-    float zz = 0.f;
-    for (int s = 0; s < splits; ++s) zz += __ldcg(z_part + ((size_t)s * NT + t) * E + e);
-    key_of(zz, bias ? bias[e] : 0.f, r.mode, ks[i], vs[i]);
+  if (T > 1) {
+    constexpr int U = 8;
+    for (int i0 = threadIdx.x; i0 < T * E; i0 += U * blockDim.x) {
+      float a[U], b[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        a[u] = i < T * E ? __ldcg(kg + i) : 0.f;
+        b[u] = i < T * E ? __ldcg(vg + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < T * E) {
+          ks[i] = a[u];
+          vs[i] = b[u];
+        }
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const float b = bias ? __ldg(bias + e) : 0.f;
+      float part[kRouterSplitMax];
+#pragma unroll
+      for (int sp = 0; sp < kRouterSplitMax; ++sp)
+        part[sp] = sp < splits ? __ldcg(z_part + (size_t)sp * NT * E + e) : 0.f;
+      float zz = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < kRouterSplitMax; ++sp)
+        if (sp < splits) zz += part[sp];
+      key_of(zz, b, r.mode, ks[e], vs[e]);
+    }
   }
   __syncthreads();
-  // Top-k: warp t selects for token t.
+  // Top-k, weights and the top-p trim: warp t for token t (T <= 8 warps).
+  const int A = T * k;
+  int *sidx = reinterpret_cast<int *>(vs + T * E);   // [A] ids after the top-p trim
+  int *sg = sidx + A;                                // [A] 2 id + (first of its expert)
   if (warp < T) {
     float key[EPL], val[EPL];
 #pragma unroll
@@ -482,107 +605,70 @@ __global__ void __launch_bounds__(256) route_small_kernel(
       key[i] = e < E ? ks[warp * E + e] : -INFINITY;
       val[i] = e < E ? vs[warp * E + e] : 0.f;
     }
-    topk_select<EPL>(key, val, warp, E, k, r, idx, w);
+    if (r.n_group > 1) group_mask<EPL>(key, E, r);
+    int my_idx;
+    float my_val;
+    argmax_rounds<EPL>(key, val, k, my_idx, my_val);
+    slot_weights<EPL>(my_idx, my_val, val, warp, E, k, r, idx, w, sidx);
   }
   __syncthreads();
-  // Stable counting sort of the A = T*k assignments (A <= 128, E <= 1024).
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int base[kMaxExperts];
-  __shared__ int wsum[8];
-  const int A = T * k;
-  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
+  // Stable grouping of the A = T*k assignments by expert, the result of the
+  // counting sort written out from ranks: assignment a goes to position
+  // (assignments to smaller experts) + (earlier assignments to its expert).
+  // Slots top-p dropped (-1) are left out; any other id outside [0, E) sets
+  // the bad-expert status and is left out too.
   for (int a = threadIdx.x; a < A; a += blockDim.x) {
-    const int ea = __ldcg(idx + a);
-    if (ea >= 0 && ea < E) atomicAdd(&cnt[ea], 1);
-    else if (ea != -1) atomicExch(status, kStatusBadExpert);   // -1: a slot top-p dropped
-  }
-  __syncthreads();
-  // Exclusive scan of cnt over E: each thread owns a contiguous run of experts.
-  const int per = (E + blockDim.x - 1) / blockDim.x;
-  const int e0 = threadIdx.x * per;
-  int run = 0;
-  for (int i = 0; i < per; ++i)
-    if (e0 + i < E) run += cnt[e0 + i];
-  int incl = run;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int wbase = 0;
-  for (int i = 0; i < warp; ++i) wbase += wsum[i];
-  int pos = wbase + incl - run;
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee < E) {
-      counts[ee] = cnt[ee];
-      if (usage && cnt[ee]) usage[ee] += (unsigned long long)cnt[ee];
-      offsets[ee] = pos;
-      base[ee] = pos;
-      pos += cnt[ee];
+    const int ea = sidx[a];
+    const bool ok = ea >= 0 && ea < E;
+    int before = 0, same = 0;
+#pragma unroll 8
+    for (int b = 0; b < A; ++b) {
+      const int eb = sidx[b];
+      before += ((uint32_t)eb < (uint32_t)ea) ? 1 : 0;   // ids below 0 do not count
+      same += (b < a && eb == ea) ? 1 : 0;
+    }
+    sg[a] = 2 * ea + ((ok && same == 0) ? 1 : 0);
+    if (ok) {
+      perm[before + same] = a;
+      inv[a] = before + same;
+    } else {
+      inv[a] = -1;
+      if (ea != -1) atomicExch(status, kStatusBadExpert);
     }
   }
-  if (threadIdx.x == blockDim.x - 1) offsets[E] = pos;
   __syncthreads();
-  // Scatter in ascending assignment order (warp 0, 32 assignments at a time).
-  if (warp == 0) {
-    const unsigned lt = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < A; c0 += 32) {
-      const int a = c0 + lane;
-      int ea = (a < A) ? __ldcg(idx + a) : E;
-      if (ea < 0 || ea >= E) ea = E;
-      if (a < A && ea == E) inv[a] = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, ea);
-      const int rank = __popc(peers & lt);
-      if (ea < E) {
-        const int p = base[ea] + rank;
-        perm[p] = a;
-        inv[a] = p;
+  // Per expert: its count, its first position, its place in the active list
+  // (ascending ids, the shared expert last, one token block each); expert
+  // E - 1 also writes the totals.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0, below = 0, dist = 0;
+#pragma unroll 8
+    for (int b = 0; b < A; ++b) {
+      const int v = sg[b];
+      const int eb = v >> 1;
+      const int lt = ((uint32_t)eb < (uint32_t)e) ? 1 : 0;   // ids below 0 do not count
+      c += (eb == e) ? 1 : 0;
+      below += lt;
+      dist += lt & v;
+    }
+    counts[e] = c;
+    offsets[e] = below;
+    if (usage && c) usage[e] += (unsigned long long)c;
+    if (c > 0) {
+      active[dist] = e;
+      tiles[dist] = e << 16;
+    }
+    if (e == E - 1) {
+      offsets[E] = below + c;
+      int na = dist + (c > 0 ? 1 : 0);
+      if (n_shared) {
+        active[na] = E;
+        tiles[na] = E << 16;
+        ++na;
       }
-      __syncwarp();
-      if (ea < E && (peers & lt) == 0) base[ea] += __popc(peers);
-      __syncwarp();
+      *n_active = na;
+      n_tiles[0] = na;
     }
-  }
-  // Active experts (ascending, shared expert last) and one token block each:
-  // the same per-thread runs, scanned over the non-empty flags.
-  __syncthreads();
-  int nz = 0;
-  for (int i = 0; i < per; ++i)
-    if (e0 + i < E && cnt[e0 + i] > 0) ++nz;
-  int inz = nz;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inz, o);
-    if (lane >= o) inz += n;
-  }
-  if (lane == 31) wsum[warp] = inz;
-  __syncthreads();
-  int nbase = 0, ntot = 0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
-    if (i < warp) nbase += wsum[i];
-    ntot += wsum[i];
-  }
-  int apos = nbase + inz - nz;
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee < E && cnt[ee] > 0) {
-      active[apos] = ee;
-      tiles[apos] = ee << 16;
-      ++apos;
-    }
-  }
-  if (threadIdx.x == 0) {
-    int na = ntot, nt = ntot;
-    if (n_shared) {
-      active[na++] = E;
-      tiles[nt++] = E << 16;
-    }
-    *n_active = na;
-    n_tiles[0] = nt;
   }
 }
 
@@ -610,8 +696,9 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   const int splits = gemv_splits(E, H, h->num_sms);
   const int hps = H / splits;
   const int nt = T <= 4 ? 4 : kRouteTokens;
-  // x staging for the GEMV, then the keys and scores of the last CTA's top-k.
-  const size_t smem = (size_t)std::max(nt * hps, 2 * T * E) * sizeof(float);
+  // x staging for the GEMV; then the last CTA's keys and scores and its two
+  // grouping arrays.
+  const size_t smem = (size_t)std::max(nt * hps, 2 * T * E + 2 * T * k) * sizeof(float);
   const int epl = (E + 31) / 32;
   const dim3 grid((E + 7) / 8, splits);
   const moe::Workspace &w = h->ws;
@@ -626,8 +713,8 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
     }                                                                                           \
     err = launch_k(false, route_small_kernel<N, NTT>, grid, dim3(256), smem, st, x,            \
                    h->L.x_dtype == 1, T, H, E, k, route_rule(h), h->wr_t, h->bias, hps,         \
-                   w.z_part, w.ticket, h->S, w.idx, w.w, w.counts, w.offsets, w.perm, w.inv,     \
-                   w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);                  \
+                   w.z_part, w.ticket, w.route_kv, h->S, w.idx, w.w, w.counts, w.offsets,       \
+                   w.perm, w.inv, w.active, w.n_active, w.tiles, w.n_tiles, w.status, usage);   \
   } while (0)
 #define MOE_RS(N)                                                                               \
   do {                                                                                          \

@@ -99,6 +99,13 @@ GLM_TOPP = Workload("glm_topp", H=6144, E=256, k=8, I=2048, n_shared=1, I_shared
                     seed=14, bias="normal", bias_sigma=0.1, top_p=0.7,
                     notes="GLM-shaped layer with adaptive expert top-p 0.7")
 
+# Many fine-grained experts with a wide top-k (the routing limits: 1024
+# experts, 16 slots, so a token has more than 256 segment candidates).
+WIDE = Workload("wide", H=512, E=1024, k=16, I=1024, n_shared=1, I_shared=1024,
+                router_mode=ROUTER_SIGMOID, rsf=2.5, x_dtype=X_F32, tokens=(1, 8, 24), seed=15,
+                bias="normal", bias_sigma=0.1,
+                notes="1024 small experts, top-16, sigmoid with bias, shared expert")
+
 ALL = (TINY, OLMOE, MIXTRAL, GLM_DECODE, GLM_PREFILL, GLM_PREFILL_SMALL, TINY_GROUPED,
-       TINY_TOPP, OLMOE_RAW, GLM_GROUPED, GLM_TOPP)
+       TINY_TOPP, OLMOE_RAW, GLM_GROUPED, GLM_TOPP, WIDE)
 BY_NAME = {w.name: w for w in ALL}

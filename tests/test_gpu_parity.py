@@ -393,6 +393,7 @@ def test_usage_counters(dev):
     ("olmoe_raw", 1, 1), ("olmoe_raw", 64, 1), ("olmoe_raw", 64, 2),
     ("glm_grouped", 1, 1), ("glm_grouped", 4, 1), ("glm_grouped", 4, 3), ("glm_grouped", 24, 2),
     ("glm_topp", 1, 1), ("glm_topp", 4, 1), ("glm_topp", 8, 3), ("glm_topp", 40, 2),
+    ("wide", 1, 1), ("wide", 8, 1), ("wide", 8, 3), ("wide", 24, 2),
 ])
 def test_router_variant_parity(dev, name, T, regime):
     """Router variants end to end on each expert path: unrenormalised softmax
