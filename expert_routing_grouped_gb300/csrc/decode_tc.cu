@@ -194,19 +194,21 @@ __device__ __forceinline__ bool bar_vote_or(int id, bool v) {
 }
 
 // TMA for SU c into stage `stage`: the int4 tile, the four operand tiles and
-// the scales.
+// the scales.  Weights and scales are read once per pass: they enter L2 as
+// evict-first (policy pol), so the split-K partial sums written during the
+// pass are still in L2 when the row blocks are finished.
 template <int PL>
 __device__ __forceinline__ void issue_su(const DecParams &p, const Geo &q, SmemDec *sm, int stage,
-                                         const Cur &c) {
+                                         const Cur &c, uint64_t pol) {
   const bool sh = c.a >= q.n_r;
   const int wrow0 = c.wbase + c.rb * 128;
   DecStage &st = sm->st[stage];
   uint64_t *bar = &sm->full[stage];
   mbar_expect_tx(bar, kStageTx);
-  tma_load_2d(st.w, sh ? &p.map_ws : &p.map_w, c.s * 128, wrow0, bar);
+  tma_load_2d_hint(st.w, sh ? &p.map_ws : &p.map_w, c.s * 128, wrow0, bar, pol);
 #pragma unroll
   for (int g = 0; g < DP; ++g) tma_load_2d(st.b[g], &p.map_b, (c.s * 4 + g) * 64, PL * c.p0, bar);
-  tma_load_2d(st.sc, sh ? &p.map_ss : &p.map_s, c.s * 4, wrow0, bar);
+  tma_load_2d_hint(st.sc, sh ? &p.map_ss : &p.map_s, c.s * 4, wrow0, bar, pol);
 }
 
 __device__ __forceinline__ float *partial_row(const DecParams &p, int cta, int rbi, int pipe,
@@ -325,6 +327,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
   if (n > 0 && warp == kProdWarp) {
     // ------------------------------------------------------ TMA producer
     Cur cp = cur_at(p, q, u0);
+    const uint64_t pol = l2_evict_first_policy();
     uint32_t jp = 0;
     for (; jp < n; ++jp) {
       // SU jp goes into the stage SU jp - NS used, once all decode warps released it.
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
         break;
       }
       fence_proxy_async();
-      if (elect_one()) issue_su<PL>(p, q, sm, stage, cp);
+      if (elect_one()) issue_su<PL>(p, q, sm, stage, cp, pol);
       __syncwarp();
       cur_next(p, q, cp, jp + 1 < n);
     }

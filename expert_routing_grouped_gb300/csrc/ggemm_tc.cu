@@ -87,7 +87,6 @@ struct __align__(1024) SmemTC {
 // small tiles keep as many K blocks in flight as large ones keep bytes (the
 // counts are powers of two: K / 64 is a multiple of 8).
 constexpr int kBoxRows[4] = {32, 64, 96, 192};
-constexpr int kBoxKps[4] = {8, 4, 4, 2};
 __device__ __forceinline__ int box_index(int nvalid) {
   return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 96 ? 2 : 3;
 }

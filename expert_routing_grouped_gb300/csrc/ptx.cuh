@@ -98,6 +98,24 @@ static __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap 
       : "memory");
 }
 
+// An L2 policy that evicts the lines it covers first: for data read once
+// (decode weights), so it does not push the workspace out of L2.
+static __device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_2d with an L2 cache policy.
+static __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x,
+                                                        int y, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // One lane of a converged warp (elect.sync); role loops run warp-wide so
 // coordinates and barrier addresses stay warp-uniform.
 static __device__ __forceinline__ bool elect_one() {

@@ -121,6 +121,17 @@ def test_tc_exact_path_parity(dev, name, T):
     h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_AUTO)
 
 
+@pytest.mark.parametrize("name,T", [("olmoe", t) for t in range(1, 9)] + [("glm_decode", 7)])
+def test_fused_route_every_small_T(dev, name, T):
+    """The fused routing launch at every T it serves (one reduction level at
+    T = 1, two above): ids, weights and the grouping bit-exact, the layer
+    within the GEMV tolerance.  OLMoE-shaped Zipf routing repeats experts
+    across tokens, so the grouping sees counts above one."""
+    wl = synth.BY_NAME[name]
+    got, ref, _, _ = run_and_compare(wl, T, dev)
+    assert rel_l2(got, ref["out"]) <= GEMV_TOL
+
+
 def test_gemv_path_parity_olmoe_64(dev):
     """OLMoE-shaped T=64 (Zipf routing) forced onto the GEMV path."""
     import expert_routing_grouped_gb300 as moe
