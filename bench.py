@@ -1,14 +1,15 @@
 """Benchmark of the MoE-layer forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload both|prefill|decode]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--decode-tokens T] [--impl ours|reference] [--no-cpu-baseline]
 
 Workloads (seeded synthetic inputs, no dataset, no trained weights):
   prefill  one GLM-5.2-style layer (H 6144, 256 routed experts + 1 shared,
            top-8, I 2048, sigmoid + noaux_tc, rsf 2.5, int4 gs64) on a batch of
            T = 4096 tokens with Zipf(1.2) expert loads.  Step = one layer pass.
   decode   the GLM-5.2-style decode stack: 8 such layers with an f32 residual and
-           an RMS pre-norm between layers, T = 1 token.  Step = the 8 layers.
+           an RMS pre-norm between layers, T = 1 token (--decode-tokens 2-8: the
+           MTP-verify sizes, on the decode tensor-core kernel).  Step = the 8 layers.
 With --workload both (default) the JSON line's headline is the prefill step and
 a "decode" object carries the decode step.  Metric: MoE-layer tokens/s.
 
@@ -271,7 +272,7 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     import synth
     wl = synth.BY_NAME[name]
     n_layers = layers or wl.layers
-    built = [make_layer(wl, l if wl.layers > 1 else 0, 4, dev)[0] for l in range(n_layers)]
+    built = [make_layer(wl, l if wl.layers > 1 else 0, max(4, T), dev)[0] for l in range(n_layers)]
     x = synth.x_rows(wl, T)
     x32 = torch.from_numpy(synth.bf16_to_f32(x)).to(dev)
     resid = torch.empty(T, wl.H, device=dev)
@@ -336,7 +337,8 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
         torch.cuda.synchronize()
         if i >= 2:
             e2e.append(time.perf_counter() - t1)
-    res = dict(wl=wl, T=T, step_ms=step_ms, layers=n_layers,
+    regime = built[0].debug_view().regime   # the expert path the automatic choice took
+    res = dict(wl=wl, T=T, step_ms=step_ms, layers=n_layers, regime=regime,
                stage={k: statistics.mean(v) for k, v in stage.items()},
                launches=per_replay * steps, n_active=n_active, clocks=clk.summary(),
                e2e_s=statistics.median(e2e), h2d=T * wl.H * 4, d2h=T * wl.H * 4)
@@ -433,9 +435,11 @@ def roofline_gemv(res, pk, src):
     na = statistics.mean(res["n_active"])
     by = na * 2 * wl.H * wl.I * 9 // 16 + T * wl.H * 2
     ach = by / (ms * 1e-3) / 1e9
-    return {"kernel": "gemv_w13", "bound": "hbm", "achieved": round(ach, 1),
+    gemv = res.get("regime", 1) == 1
+    return {"kernel": "gemv_w13" if gemv else "decode_tc_w13", "bound": "hbm",
+            "achieved": round(ach, 1),
             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-            "traffic": traffic("gemv_w13") if wl.name == "glm_decode" else None,
+            "traffic": traffic("gemv_w13") if gemv and wl.name == "glm_decode" and T == 1 else None,
             "peak_source": "%s hbm_gbs" % src,
             "per_launch": "%.1f activated experts x 2*H*I*0.5625 B + x" % na}
 
@@ -497,6 +501,9 @@ def main():
                     choices=["both", "prefill", "decode", "prefill_small", "decode_small"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-tokens", type=int, default=1, choices=range(1, 9),
+                    help="tokens per decode step (1: the GEMV path; 2-8: the decode "
+                         "tensor-core kernel, as for MTP verification)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -508,7 +515,7 @@ def main():
         if rank != 0:
             return
         wl = synth.BY_NAME["glm_prefill" if args.workload != "decode" else "glm_decode"]
-        T = 4096 if wl.name == "glm_prefill" else 1
+        T = 4096 if wl.name == "glm_prefill" else args.decode_tokens
         x = synth.x_rows(wl, T)
         for _ in range(min(args.warmup, 1)):
             oracle_sample(wl, np.arange(1), x)
@@ -555,10 +562,11 @@ def main():
             pre = None          # tensor-core path unavailable: decode becomes the headline
     if do_decode:
         if args.workload == "decode_small":
-            dec = bench_decode(dev, args.steps, args.warmup, stream, name="glm_prefill_small",
-                               layers=1, sync_all=sync_all)
+            dec = bench_decode(dev, args.steps, args.warmup, stream, T=args.decode_tokens,
+                               name="glm_prefill_small", layers=1, sync_all=sync_all)
         else:
-            dec = bench_decode(dev, args.steps, args.warmup, stream, sync_all=sync_all)
+            dec = bench_decode(dev, args.steps, args.warmup, stream, T=args.decode_tokens,
+                               sync_all=sync_all)
 
     def reduce_max(v):
         if world == 1:

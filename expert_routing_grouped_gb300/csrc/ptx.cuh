@@ -43,6 +43,22 @@ static __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t par
   return ok != 0;
 }
 
+// The same test, letting the thread sleep until the phase completes (or
+// kSuspendNs passes): a polling warp then takes no issue slots from the
+// warps that share its scheduler.
+constexpr uint32_t kSuspendNs = 20000;
+static __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 static __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -56,7 +72,7 @@ static __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity
                                                   int32_t *status) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*reinterpret_cast<volatile int *>(abort)) return false;
       if (globaltimer() - t0 > kWaitNs) {
