@@ -209,11 +209,13 @@ int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
  * them with moe_usage_read); the dispatch kernel does the adding, so the option
  * costs no launch.  moe_route (a look-ahead) never counts.  0 (default): off. */
 #define MOE_OPT_USAGE 4
-/* 1 (default): launch the forward's kernels with programmatic dependent
- * launch -- each may be scheduled while its predecessor on the stream is still
- * running, and waits (griddepcontrol) for it to finish before touching memory,
- * so launch latency and start-up overlap the predecessor's tail.  The same
- * results bit for bit; 0: plain launches. */
+/* 1 (default): launch every kernel of a call after the first with
+ * programmatic dependent launch -- it may be scheduled while its predecessor
+ * on the stream is still running, and waits (griddepcontrol) for it to finish
+ * before touching memory, so launch latency and start-up overlap the
+ * predecessor's tail.  The first kernel of a call is launched plainly (the
+ * wait covers kernels, not the caller's copies or memsets before it).  The
+ * same results bit for bit; 0: plain launches. */
 #define MOE_OPT_PDL 5
 int moe_set_option(moe_handle *h, int option, int value);
 
