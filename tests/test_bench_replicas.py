@@ -79,3 +79,20 @@ def test_reference_arm_extra_rank_exits_without_work():
                         "--gpus", "2", "--steps", "1", "--warmup", "1"],
                        capture_output=True, text=True, env=env, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_decode_roofline_names_the_kernel_of_its_path():
+    """The decode roofline entry names the kernel the automatic choice ran:
+    the GEMV at one token, the decode tensor-core kernel at 2-8 (whose DRAM
+    traffic the committed capture does not cover)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    pk = {"hbm_gbs": 6792.4, "bf16_tflops": 1898.0, "bf16_tflops_sustained": 1707.1}
+    base = {"wl": synth.BY_NAME["glm_decode"], "stage": {"w13": 0.1}, "n_active": [30]}
+    tc = bench.roofline_gemv(dict(base, T=4, regime=3), pk, "measured")
+    assert tc["kernel"] == "decode_tc_w13" and tc["traffic"] is None and tc["bound"] == "hbm"
+    gv = bench.roofline_gemv(dict(base, T=1, regime=1), pk, "measured")
+    assert gv["kernel"] == "gemv_w13"
+    assert gv["achieved"] == pytest.approx((30 * 2 * 6144 * 2048 * 9 // 16 + 6144 * 2) / 0.1e-3 / 1e9,
+                                           rel=1e-3)
