@@ -483,6 +483,9 @@ def make_line(pre, dec, world, reduce_max, pk, src, steps, warmup):
                           "hbm_gbs": byts * world / (dms * 1e-3) / 1e9,
                           "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
                           "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
+                          "e2e": {"value": dec["T"] * world / reduce_max(dec["e2e_s"]),
+                                  "unit": "tokens/s", "h2d_bytes_per_step": dec["h2d"],
+                                  "d2h_bytes_per_step": dec["d2h"]},
                           "roofline": roofline_gemv(dec, pk, src)}
     elif head is dec:
         byts = sum(layer_bytes(dec["wl"], a, dec["T"]) for a in dec["n_active"])

@@ -67,6 +67,7 @@ def test_two_gloo_ranks_take_the_slowest_rank(tmp_path):
     assert line["e2e"]["value"] == pytest.approx(2 * 4096 / 0.005)
     assert line["decode"]["ms_per_step"] == pytest.approx(0.8)
     assert line["decode"]["tokens_per_s"] == pytest.approx(2 / 0.8e-3)
+    assert line["decode"]["e2e"]["value"] == pytest.approx(2 / 0.001)   # host buffers, every step
     assert line["roofline"]["unit"] == "TFLOP/s"
     for key in ("metric", "unit", "higher_is_better", "dtype", "data", "config", "gpu_launches",
                 "clocks", "e2e", "roofline", "vs_baseline", "steps", "warmup"):
