@@ -7,15 +7,18 @@
 // to perm[offsets[e] + r], where r counts the assignments of expert e with a
 // smaller a, so each expert's group lists its tokens in ascending order.
 //
-// One CTA of 1024 threads.  Assignments are taken in chunks of 1024 in
-// ascending order; inside a chunk, __match_any_sync ranks a lane among the
-// lanes of its warp holding the same expert, and a per-(warp, expert) count
-// table turns that into a rank across the chunk.
+// Three launches (T > 8; the fused routing launch groups smaller batches):
+// ranks and counts over contiguous ranges of assignments, one CTA per range;
+// one CTA that scans the counts into offsets and per-range bases; a scatter
+// over the same ranges.  Ranges and ranks both ascend, so the order is the
+// stable one.
 //
 // Also produced here, for the expert kernels: the ascending list of experts
 // that received tokens (the shared expert, id E, appended last), and the
 // tensor-core token blocks: one entry per tile_m tokens of every non-empty
 // group (the shared expert's included), costliest first.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -51,91 +54,110 @@ __device__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
   return r;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
-    const int32_t *__restrict__ idx, int T, int k, int E, int n_shared, int tile_m,
-    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-    int32_t *__restrict__ inv, int32_t *__restrict__ active, int32_t *__restrict__ n_active,
-    int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles, int32_t *__restrict__ status,
-    unsigned long long *__restrict__ usage) {
+// Phase 1 of the dispatch, one CTA per contiguous range of assignments (CTA c
+// takes [c A / C, (c + 1) A / C)): each assignment's rank among the earlier
+// assignments of its expert inside the range goes to inv[a] (-1 for a dropped
+// or invalid id), and the range's per-expert counts to part[c][e].  Inside a
+// chunk of 1024, __match_any_sync ranks a lane among the lanes of its warp
+// holding the same expert, and a per-(warp, expert) count table turns that
+// into a rank across the chunk.
+__global__ void __launch_bounds__(kThreads, 1) dispatch_rank_kernel(
+    const int32_t *__restrict__ idx, int A, int E, int32_t *__restrict__ inv,
+    int32_t *__restrict__ part, int32_t *__restrict__ status) {
   pdl_enter();
   idx = after_wait(idx);
-  counts = after_wait(counts);
-  offsets = after_wait(offsets);
-  perm = after_wait(perm);
   inv = after_wait(inv);
-  active = after_wait(active);
-  n_active = after_wait(n_active);
-  tiles = after_wait(tiles);
-  n_tiles = after_wait(n_tiles);
+  part = after_wait(part);
   status = after_wait(status);
-  usage = after_wait(usage);
   extern __shared__ int smem[];
-  int *cnt = smem;                 // [E]
-  int *base = cnt + E;             // [E]
-  int *wc = base + E;              // [32][E]
-  __shared__ int warp_sums[32];
-  __shared__ int total;
+  int *run = smem;                 // [E] assignments of each expert so far in this range
+  int *wc = run + E;               // [32][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int A = T * k;
-
-  for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+  const int a0 = (int)((long long)A * blockIdx.x / gridDim.x);
+  const int a1 = (int)((long long)A * (blockIdx.x + 1) / gridDim.x);
+  for (int e = tid; e < E; e += kThreads) run[e] = 0;
   for (int i = tid; i < 32 * E; i += kThreads) wc[i] = 0;
   __syncthreads();
-  int bad = 0;
-  for (int a = tid; a < A; a += kThreads) {
-    const int e = idx[a];
-    if (e == -1) continue;   // a slot the top-p trim dropped: no assignment
-    if (e < 0 || e >= E) {
-      bad = 1;
-      continue;
-    }
-    atomicAdd(&cnt[e], 1);
-  }
-  if (bad) atomicExch(status, kStatusBadExpert);
-  __syncthreads();
-
-  // offsets = exclusive scan of counts (E <= 1024: one expert per thread).
-  const int c = (tid < E) ? cnt[tid] : 0;
-  const int off = block_exclusive_scan(c, warp_sums, &total);
-  if (tid < E) {
-    counts[tid] = c;
-    offsets[tid] = off;
-    base[tid] = off;
-    if (usage && c) usage[tid] += (unsigned long long)c;   // one writer per expert
-  }
-  if (tid == 0) offsets[E] = total;
-  __syncthreads();
-
-  // Stable scatter, chunk by chunk.
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < A; c0 += kThreads) {
+  int bad = 0;
+  for (int c0 = a0; c0 < a1; c0 += kThreads) {
     const int a = c0 + tid;
-    int e = (a < A) ? idx[a] : E;
+    int e = (a < a1) ? idx[a] : E;
+    if (a < a1 && e != -1 && (e < 0 || e >= E)) bad = 1;
     if (e < 0 || e >= E) e = E;                  // dropped or invalid ids are not placed
-    if (a < A && e == E) inv[a] = -1;
+    if (a < a1 && e == E) inv[a] = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     if (e < E && (peers & lt_mask) == 0) wc[warp * E + e] = __popc(peers);
     __syncthreads();
-    if (tid < E) {
-      int run = base[tid];
+    for (int x = tid; x < E; x += kThreads) {
+      int r = run[x];
       for (int w = 0; w < 32; ++w) {
-        const int n = wc[w * E + tid];
-        wc[w * E + tid] = run;
-        run += n;
+        const int n = wc[w * E + x];
+        wc[w * E + x] = r;
+        r += n;
       }
-      base[tid] = run;
+      run[x] = r;
     }
     __syncthreads();
-    if (e < E) {
-      const int pos = wc[warp * E + e] + rank;
-      perm[pos] = a;
-      inv[a] = pos;
-    }
+    if (e < E) inv[a] = wc[warp * E + e] + rank;
     __syncthreads();
     for (int i = tid; i < 32 * E; i += kThreads) wc[i] = 0;
     __syncthreads();
   }
+  if (bad) atomicExch(status, kStatusBadExpert);
+  for (int x = tid; x < E; x += kThreads) part[(size_t)blockIdx.x * E + x] = run[x];
+}
+
+// Phase 2, one CTA: per-expert totals over the C ranges, counts, offsets (a
+// block-wide exclusive scan), usage; part[c][e] becomes the first position of
+// range c's assignments of expert e (offsets[e] plus the earlier ranges'
+// counts).  Also the ascending list of experts that received tokens (the
+// shared expert, id E, appended last) and the tensor-core token blocks: one
+// entry per tile_m tokens of every non-empty group (the shared expert's
+// included), costliest first.
+__global__ void __launch_bounds__(kThreads, 1) dispatch_scan_kernel(
+    int T, int E, int n_shared, int tile_m, int C, int32_t *__restrict__ part,
+    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ active,
+    int32_t *__restrict__ n_active, int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
+    unsigned long long *__restrict__ usage) {
+  pdl_enter();
+  part = after_wait(part);
+  counts = after_wait(counts);
+  offsets = after_wait(offsets);
+  active = after_wait(active);
+  n_active = after_wait(n_active);
+  tiles = after_wait(tiles);
+  n_tiles = after_wait(n_tiles);
+  usage = after_wait(usage);
+  __shared__ int warp_sums[32];
+  __shared__ int total;
+  const int tid = threadIdx.x;
+  // Totals (E <= 1024: one expert per thread), the loads of 8 ranges at a time
+  // issued before their sums.
+  int c = 0;
+  if (tid < E) {
+    for (int r0 = 0; r0 < C; r0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (r0 + u < C) ? part[(size_t)(r0 + u) * E + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c += v[u];
+    }
+  }
+  const int off = block_exclusive_scan(c, warp_sums, &total);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = off;
+    if (usage && c) usage[tid] += (unsigned long long)c;   // one writer per expert
+    int pos = off;
+    for (int r = 0; r < C; ++r) {
+      const int n = part[(size_t)r * E + tid];
+      part[(size_t)r * E + tid] = pos;
+      pos += n;
+    }
+  }
+  if (tid == 0) offsets[E] = total;
 
   // Ascending list of non-empty experts; the shared expert (id E) goes last.
   const int flag = (tid < E && c > 0) ? 1 : 0;
@@ -175,23 +197,59 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(
   if (tid == 0) n_tiles[0] = ntot;
 }
 
+// Phase 3, the ranges of phase 1: assignment a of range c and expert e goes to
+// position part[c][e] + its rank: perm[pos] = a, inv[a] = pos.
+__global__ void __launch_bounds__(kThreads) dispatch_scatter_kernel(
+    const int32_t *__restrict__ idx, int A, int E, const int32_t *__restrict__ part,
+    int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
+  pdl_enter();
+  idx = after_wait(idx);
+  part = after_wait(part);
+  perm = after_wait(perm);
+  inv = after_wait(inv);
+  const int a0 = (int)((long long)A * blockIdx.x / gridDim.x);
+  const int a1 = (int)((long long)A * (blockIdx.x + 1) / gridDim.x);
+  for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
+    const int e = idx[a];
+    const int r = inv[a];
+    if (e < 0 || e >= E || r < 0) continue;
+    const int pos = part[(size_t)blockIdx.x * E + e] + r;
+    perm[pos] = a;
+    inv[a] = pos;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned long long *usage,
                             cudaStream_t st) {
-  const size_t smem = (size_t)(2 + 32) * h->E * sizeof(int);
+  const int E = h->E, A = T * h->k;
+  // Ranges of at least 1024 assignments, one CTA per SM at most.
+  const int C = std::max(1, std::min(h->num_sms, (A + kThreads - 1) / kThreads));
+  const size_t smem = (size_t)(1 + 32) * E * sizeof(int);
   static bool attr_set = false;   // per process; the attribute is per function
   if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(dispatch_kernel,
+    cudaError_t err = cudaFuncSetAttribute(dispatch_rank_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)((2 + 32) * kMaxExperts * sizeof(int)));
+                                           (int)((1 + 32) * kMaxExperts * sizeof(int)));
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
   const moe::Workspace &w = h->ws;
-  return launch_k(h->pdl, dispatch_kernel, dim3(1), dim3(kThreads), smem, st, w.idx, T, h->k, h->E,
-                  h->S, tile_m, w.counts, w.offsets, w.perm, w.inv, w.active, w.n_active, w.tiles,
-                  w.n_tiles, w.status, usage);
+  // part[C][E] lives in the router's logit buffer: the top-k has read the
+  // logits when the dispatch runs, and the buffer has max(max_tokens, 128) >= C
+  // rows of E entries.
+  int32_t *part = reinterpret_cast<int32_t *>(w.z_part);
+  cudaError_t err = launch_k(h->pdl, dispatch_rank_kernel, dim3(C), dim3(kThreads), smem, st,
+                             w.idx, A, E, w.inv, part, w.status);
+  if (err == cudaSuccess)
+    err = launch_k(h->pdl, dispatch_scan_kernel, dim3(1), dim3(kThreads), 0, st, T, E, h->S,
+                   tile_m, C, part, w.counts, w.offsets, w.active, w.n_active, w.tiles,
+                   w.n_tiles, usage);
+  if (err == cudaSuccess)
+    err = launch_k(h->pdl, dispatch_scatter_kernel, dim3(C), dim3(kThreads), 0, st, w.idx, A, E,
+                   part, w.perm, w.inv);
+  return err;
 }
 
 }  // namespace moe

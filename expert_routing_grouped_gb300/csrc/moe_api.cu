@@ -247,7 +247,7 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
     h->launches += 2;
     mark(h, "router", st);
     if (err == cudaSuccess) err = moe::launch_dispatch(h, T, moe::kTileTokens, usage, st);
-    h->launches += 1;
+    h->launches += 3;   // ranks, scan, scatter
     mark(h, "dispatch", st);
   }
   if (err == cudaSuccess) {
