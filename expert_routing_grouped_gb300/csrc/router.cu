@@ -4,8 +4,10 @@
 // The router stays f32 (colibrì engine teardown, text-matrix.pages.dev,
 // "System map": norm/router/bias are kept in f32 because they are small and
 // sensitive).  Scoring is softmax (Colibri C + cuBLASLt tutorial, cf-1.com,
-// §2.1 step 2) or sigmoid with a noaux_tc selection bias, n_group = 1, scaled
-// by routed_scaling_factor (teardown "Three key engineering decisions" (1)).
+// §2.1 step 2) or sigmoid with a noaux_tc selection bias (n_group = 1, or
+// group-limited with n_group > 1), scaled by routed_scaling_factor (teardown
+// "Three key engineering decisions" (1)); softmax without renormalisation and
+// an adaptive top-p trim are the variants the tuning guide names.
 //
 // Logits carry f32 rounding (plain f32 FMA here; for large T with bf16
 // activations, tensor cores over three bf16 planes of the f32 weights, see
@@ -474,11 +476,13 @@ __global__ void __launch_bounds__(256, 1) router_topk_kernel(
 
 // ---------------------------------------------------------------------------
 // T <= kRouteTokens in one launch: the split-K router GEMV of
-// router_gemv_kernel, then the last CTA to finish (an atomic ticket, reset by
-// that CTA for the next call; nothing waits) reads every partial through L2,
-// takes the top-k of each token and groups the T*k assignments by expert --
-// the stable counting sort of dispatch.cu, written out from ranks.  Also
-// clears the status word first.
+// router_gemv_kernel, then self-resetting atomic tickets (nothing waits): for
+// T > 1 the last split CTA of each 8-expert block sums that block's partials
+// into keys and scores, and the last block to finish loads them; for T = 1
+// the last CTA of the grid sums every partial itself.  That CTA takes the
+// top-k of each token and groups the T*k assignments by expert -- the stable
+// counting sort of dispatch.cu, written out from ranks.  It also clears the
+// status word.
 template <int EPL, int NT>
 __global__ void __launch_bounds__(256) route_small_kernel(
     const void *__restrict__ x, int x_is_bf16, int T, int H, int E, int k, const RouteRule r,
