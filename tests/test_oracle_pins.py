@@ -87,6 +87,29 @@ def test_topk_matches_bruteforce(mode, E, k):
         assert gap[t] == pytest.approx(np.min(srt[:top - 1] - srt[1:top]), rel=1e-12)
 
 
+@pytest.mark.parametrize("mode,E,k", [(1, 256, 8), (1, 1024, 16), (0, 1024, 16), (0, 64, 8)])
+def test_topk_large_E_matches_library_sort(mode, E, k):
+    """At the sizes the GPU serves (up to 1024 experts, 16 slots) the selection
+    is the first k of numpy's stable sort of (-key, id) over the oracle's own
+    keys, which match their definition (z + b, or sigmoid(z) + b).  Softmax
+    logits are rounded so that equal keys occur: ties go to the lower id.
+    Catches a wrong slot order, a lost tie rule or an off-by-one at large E."""
+    rng = np.random.default_rng(1000 + E + k + 7 * mode)
+    L = small_layout(E=E, k=k, mode=mode, rsf=2.5 if mode else 1.0)
+    z = np.round(rng.normal(0, 1.0, size=(48, E)), 2)
+    b = rng.normal(0, 0.1, size=E).astype(np.float32) if mode else None
+    idx, _, key, _ = oracle.route_from_logits(L, b, z)
+    want = logistic(z) + b.astype(np.float64) if mode else z
+    np.testing.assert_allclose(key, want, rtol=1e-14, atol=1e-15)
+    ties = 0
+    for t in range(z.shape[0]):
+        order = np.lexsort((np.arange(E), -key[t]))[:k]   # key descending, then id ascending
+        assert list(idx[t]) == list(order)
+        ties += len(key[t][order]) - len(np.unique(key[t][order]))
+    if mode == 0:
+        assert ties > 0   # the rounding produced equal keys among the selected slots
+
+
 def test_topk_ties_go_to_lowest_index():
     L = small_layout(E=6, k=3)
     z = np.array([[1.0, 2.0, 2.0, 0.5, 2.0, 1.0]])
