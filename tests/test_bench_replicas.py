@@ -97,3 +97,25 @@ def test_decode_roofline_names_the_kernel_of_its_path():
     assert gv["kernel"] == "gemv_w13"
     assert gv["achieved"] == pytest.approx((30 * 2 * 6144 * 2048 * 9 // 16 + 6144 * 2) / 0.1e-3 / 1e9,
                                            rel=1e-3)
+
+
+def test_algorithmic_units_match_the_published_per_layer_figures():
+    """bench.py's bytes and FLOPs of a layer reproduce the per-layer workload
+    table of the scope: a GLM-shaped decode layer with 9 activated experts
+    (8 routed + shared) at T = 1 moves 197.4 MB; the prefill layer at T = 4096
+    does 2.80 TFLOP (routed 2.47 + shared 0.31 + router 0.013)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    dec = synth.BY_NAME["glm_decode"]
+    assert bench.layer_bytes(dec, 9, 1) / 1e6 == pytest.approx(197.4, abs=0.05)
+    pre = synth.BY_NAME["glm_prefill"]
+    fl = bench.layer_flops(pre, 4096)
+    assert fl / 1e12 == pytest.approx(2.80, abs=0.005)
+    routed = 2 * 4096 * 8 * 3 * 6144 * 2048
+    shared = 2 * 4096 * 1 * 3 * 6144 * 2048
+    router = 2 * 4096 * 6144 * 256
+    assert (routed / 1e12, shared / 1e12, router / 1e12) == (
+        pytest.approx(2.47, abs=0.005), pytest.approx(0.31, abs=0.005),
+        pytest.approx(0.013, abs=0.0005))
+    assert fl == routed + shared + router
