@@ -119,3 +119,50 @@ def test_algorithmic_units_match_the_published_per_layer_figures():
         pytest.approx(2.47, abs=0.005), pytest.approx(0.31, abs=0.005),
         pytest.approx(0.013, abs=0.0005))
     assert fl == routed + shared + router
+
+
+def test_clock_records_are_judged_and_a_bad_region_is_measured_once_more():
+    """A timed region that saw a hardware or thermal slowdown, or sat well
+    below the maximum SM clock with no reason given, is measured once more
+    (single process); sw_power_cap is kept.  The second record is the one
+    reported, the rejected one beside it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}
+    assert bench.clocks_ok(ok)
+    assert bench.clocks_ok(dict(ok, sm_mhz=1455.0, reasons=["sw_power_cap"]))
+    assert not bench.clocks_ok(dict(ok, reasons=["hw_slowdown"]))
+    assert not bench.clocks_ok(dict(ok, reasons=["sw_thermal_slowdown", "sw_power_cap"]))
+    assert not bench.clocks_ok(dict(ok, sm_mhz=1200.0))          # a leftover clock lock
+
+    records = [dict(ok, reasons=["hw_thermal_slowdown"]), ok]
+
+    class FakeSampler:
+        def __init__(self, dev):
+            self.rec = records.pop(0)
+
+        def __enter__(self):
+            return self
+
+        def __exit__(self, *a):
+            return False
+
+        def summary(self):
+            return dict(self.rec)
+
+    runs = []
+    out, c = bench.timed_region(None, lambda: runs.append(1) or len(runs), sampler=FakeSampler)
+    assert len(runs) == 2 and out == 2
+    assert c["remeasured"] and c["rejected"]["reasons"] == ["hw_thermal_slowdown"]
+    assert c["reasons"] == []
+
+    records[:] = [ok]
+    runs.clear()
+    out, c = bench.timed_region(None, lambda: runs.append(1) or len(runs), sampler=FakeSampler)
+    assert len(runs) == 1 and "remeasured" not in c
+
+    records[:] = [dict(ok, reasons=["hw_slowdown"])]    # several ranks: no retry, reported as is
+    runs.clear()
+    out, c = bench.timed_region(None, lambda: runs.append(1) or len(runs), retry=False,
+                                sampler=FakeSampler)
+    assert len(runs) == 1 and c["reasons"] == ["hw_slowdown"]
