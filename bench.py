@@ -623,7 +623,7 @@ def main():
 
     line = make_line(pre, dec, world, reduce_max, pk, src, args.steps, args.warmup)
     head = pre if pre is not None else dec
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the host baseline: N = 1 only
         line["cpu_baseline"] = cpu_baseline(head["wl"], head["T"], 8 if head is pre else 1,
                                             1 if head is pre else head["layers"])
     if world > 1:
