@@ -490,7 +490,7 @@ cudaError_t launch_pass(const DecParams &p, int T, int grid, bool pdl, cudaStrea
   else if (T <= 4) MOE_DEC(4);
   else MOE_DEC(8);
 #undef MOE_DEC
-  return err != cudaSuccess ? err : cudaGetLastError();
+  return err;
 }
 
 }  // namespace

@@ -846,8 +846,7 @@ bool tc_path_available() { return get_encode() != nullptr; }
 
 cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
                                 cudaStream_t st) {
-  split_planes_kernel<<<152 * 4, 256, 0, st>>>(wr_t, planes, n);
-  return cudaGetLastError();
+  return launch_k(false, split_planes_kernel, dim3(152 * 4), dim3(256), 0, st, wr_t, planes, n);
 }
 
 cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t st) {

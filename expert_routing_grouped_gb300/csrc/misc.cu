@@ -143,25 +143,24 @@ __global__ void repack_words_kernel(uint32_t *__restrict__ w, long long n_words)
 
 cudaError_t launch_repack_w13(const uint8_t *w1, const uint8_t *w3, uint8_t *dst, long long n_exp,
                               int I, int kb, cudaStream_t s) {
-  repack_w13_kernel<<<152 * 8, 256, 0, s>>>(w1, w3, dst, n_exp, I, kb);
-  return cudaGetLastError();
+  return launch_k(false, repack_w13_kernel, dim3(152 * 8), dim3(256), 0, s, w1, w3, dst, n_exp, I,
+                  kb);
 }
 
 cudaError_t launch_repack_w13_scales(const float *s1, const float *s3, float *dst, long long n_exp,
                                      int I, int groups, cudaStream_t s) {
-  repack_w13_scales_kernel<<<152 * 8, 256, 0, s>>>(s1, s3, dst, n_exp, I, groups);
-  return cudaGetLastError();
+  return launch_k(false, repack_w13_scales_kernel, dim3(152 * 8), dim3(256), 0, s, s1, s3, dst,
+                  n_exp, I, groups);
 }
 
 cudaError_t launch_repack_words(uint8_t *w, long long n_bytes, cudaStream_t s) {
-  repack_words_kernel<<<152 * 8, 256, 0, s>>>(reinterpret_cast<uint32_t *>(w), n_bytes / 4);
-  return cudaGetLastError();
+  return launch_k(false, repack_words_kernel, dim3(152 * 8), dim3(256), 0, s,
+                  reinterpret_cast<uint32_t *>(w), n_bytes / 4);
 }
 
 cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, cudaStream_t s) {
   const dim3 grid((E + 31) / 32, (H + 31) / 32), block(32, 8);
-  transpose_kernel<<<grid, block, 0, s>>>(src, dst, H, E);
-  return cudaGetLastError();
+  return launch_k(false, transpose_kernel, grid, block, 0, s, src, dst, H, E);
 }
 
 cudaError_t launch_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,

@@ -273,10 +273,13 @@ int run_forward(moe_handle *h, const void *x, int T, float *out, bool accumulate
   return err == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
 }
 
-int check_call(moe_handle *h, const void *x, int T, const void *out) {
+// device: x and out are device pointers the kernels access directly.
+int check_call(moe_handle *h, const void *x, int T, const void *out, bool device = true) {
   if (!h || T < 0) return MOE_ERR_ARG;
   if (T > h->L.max_tokens) return MOE_ERR_NOMEM;
   if (T > 0 && (!x || !out)) return MOE_ERR_ARG;
+  // x is read and out written with 16-byte vector accesses.
+  if (device && T > 0 && (((uintptr_t)x | (uintptr_t)out) & 15)) return MOE_ERR_ARG;
   return MOE_OK;
 }
 
@@ -371,7 +374,7 @@ __attribute__((visibility("default"))) int moe_forward_residual(moe_handle *h, c
 __attribute__((visibility("default"))) int moe_forward_host(moe_handle *h, const void *x_host,
                                                             int T, float *out_host,
                                                             moe_stream_t stream) {
-  int rc = check_call(h, x_host, T, out_host);
+  int rc = check_call(h, x_host, T, out_host, false);
   if (rc || T == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t xb = (size_t)T * h->H * h->x_elem, ob = (size_t)T * h->H * sizeof(float);

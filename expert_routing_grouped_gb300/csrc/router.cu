@@ -733,33 +733,33 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
   else MOE_RS(32);
 #undef MOE_RS
 #undef MOE_RS2
-  return err != cudaSuccess ? err : cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t st) {
   const int E = h->E, H = h->H, k = h->k;
   const int xb = h->L.x_dtype == 1;
   const int splits = router_splits(T, E, H, h->num_sms);
+  cudaError_t err = cudaSuccess;
   if (T <= 4) {
     const int hps = H / splits;
     const dim3 grid((E + 7) / 8, splits);
     const size_t smem = (size_t)4 * hps * sizeof(float);
     if (smem > 48 * 1024) {
-      cudaError_t err = cudaFuncSetAttribute(router_gemv_kernel<4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      err = cudaFuncSetAttribute(router_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
       if (err != cudaSuccess) return err;
     }
-    router_gemv_kernel<4><<<grid, 256, smem, st>>>(x, xb, T, H, E, h->wr_t, hps, h->ws.z_part,
-                                                   kGemvTokens);
+    err = launch_k(false, router_gemv_kernel<4>, grid, dim3(256), smem, st, x, xb, T, H, E,
+                   h->wr_t, hps, h->ws.z_part, kGemvTokens);
   } else if (xb && tc_path_available()) {
     // bf16 activations: tensor cores on the three bf16 planes of the f32 weights.
-    cudaError_t err = launch_router_tc(h, x, T, h->ws.z_part, st);
-    if (err != cudaSuccess) return err;
+    err = launch_router_tc(h, x, T, h->ws.z_part, st);
   } else {
     const dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT);
-    router_gemm_kernel<<<grid, 256, 0, st>>>(x, xb, T, H, E, h->wr_t, h->ws.z_part);
+    err = launch_k(false, router_gemm_kernel, grid, dim3(256), 0, st, x, xb, T, H, E, h->wr_t,
+                   h->ws.z_part);
   }
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int zstride = (T <= 4) ? kGemvTokens : T;
   const int epl = (E + 31) / 32;
@@ -774,7 +774,7 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
   else if (epl <= 16) MOE_TOPK(16);
   else MOE_TOPK(32);
 #undef MOE_TOPK
-  return err != cudaSuccess ? err : cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe
@@ -836,6 +836,8 @@ extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
   if (router_mode == 1 && !router_bias) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !router_w_eh || !idx || !w) return MOE_ERR_ARG;
+  // x and the router rows are read with 16-byte vector loads.
+  if (((uintptr_t)x | (uintptr_t)router_w_eh) & 15) return MOE_ERR_ARG;
   const int E = num_experts, H = hidden;
   // Scratch needed: split partials [splits][4][E] for T <= 4, logits [T][E] above.
   if (T > 4 && (size_t)T * E > kRouteScratchFloats) return MOE_ERR_NOMEM;
@@ -854,22 +856,22 @@ extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
         cudaFuncSetAttribute(router_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return MOE_ERR_DEVICE;
-    router_gemv_kernel<4><<<dim3((E + 7) / 8, splits), 256, smem, st>>>(x, xb, T, H, E,
-                                                                        router_w_eh, hps, z,
-                                                                        kGemvTokens);
+    if (launch_k(false, router_gemv_kernel<4>, dim3((E + 7) / 8, splits), dim3(256), smem, st, x,
+                 xb, T, H, E, router_w_eh, hps, z, kGemvTokens) != cudaSuccess)
+      return MOE_ERR_DEVICE;
   } else {
-    router_gemm_kernel<<<dim3((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT), 256, 0, st>>>(
-        x, xb, T, H, E, router_w_eh, z);
+    if (launch_k(false, router_gemm_kernel, dim3((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT),
+                 dim3(256), 0, st, x, xb, T, H, E, router_w_eh, z) != cudaSuccess)
+      return MOE_ERR_DEVICE;
   }
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_DEVICE;
   const int zstride = (T <= 4) ? kGemvTokens : T;
   const int epl = (E + 31) / 32;
   const dim3 g2((T + 7) / 8);
+  cudaError_t err = cudaSuccess;
 #define MOE_TOPK_NA(N)                                                                      \
-  router_topk_kernel<N><<<g2, 256, 0, st>>>(z, splits, zstride, T, E, top_k,               \
-                                            RouteRule{router_mode, 0, 0, 0.f,               \
-                                                      routed_scaling_factor},               \
-                                            router_bias, idx, w)
+  err = launch_k(false, router_topk_kernel<N>, g2, dim3(256), 0, st, z, splits, zstride, T, E, \
+                 top_k, RouteRule{router_mode, 0, 0, 0.f, routed_scaling_factor}, router_bias, \
+                 idx, w)
   if (epl <= 1) MOE_TOPK_NA(1);
   else if (epl <= 2) MOE_TOPK_NA(2);
   else if (epl <= 4) MOE_TOPK_NA(4);
@@ -877,5 +879,5 @@ extern "C" __attribute__((visibility("default"))) int moe_route_noalloc(
   else if (epl <= 16) MOE_TOPK_NA(16);
   else MOE_TOPK_NA(32);
 #undef MOE_TOPK_NA
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_DEVICE;
 }

@@ -158,8 +158,11 @@ int moe_init(const moe_layout *layout, const moe_weights *weights, moe_handle **
  * out[T][H] (f32, device) = MoE(x), x [T][H] device (f32 or bf16 per layout).
  * Asynchronous on `stream`; no allocation, no host synchronisation.
  * T == 0 validates the arguments and launches nothing (dry run; x and out may
- * then be NULL).  T > max_tokens returns MOE_ERR_NOMEM.  A handle serves one
- * stream at a time and is not thread-safe.
+ * then be NULL).  T > max_tokens returns MOE_ERR_NOMEM.  x and out must be
+ * 16-byte aligned (the kernels use 16-byte vector accesses); a misaligned
+ * pointer returns MOE_ERR_ARG before anything is launched.  A handle serves
+ * one stream at a time and is not thread-safe.  moe_route and
+ * moe_forward_residual take the same checks.
  */
 int moe_forward(moe_handle *h, const void *x, int T, float *out, moe_stream_t stream);
 
@@ -236,10 +239,11 @@ int moe_debug_view(moe_handle *h, moe_debug *d);
  * kernels as moe_forward, and allocates nothing: the logit scratch is a fixed
  * 4 MiB array in the library's device image, which every GPU that loads the
  * library keeps until the process exits.
- *   x            [T][hidden] device, f32 (x_dtype 0) or bf16 (x_dtype 1)
- *   router_w_eh  [num_experts][hidden] f32 device: row e is expert e's router
- *                vector (the layout of a linear layer's weight; the transpose
- *                of moe_weights.router_w)
+ *   x            [T][hidden] device, f32 (x_dtype 0) or bf16 (x_dtype 1),
+ *                16-byte aligned
+ *   router_w_eh  [num_experts][hidden] f32 device, 16-byte aligned: row e is
+ *                expert e's router vector (the layout of a linear layer's
+ *                weight; the transpose of moe_weights.router_w)
  *   router_bias  [num_experts] f32 device, or NULL (softmax mode only)
  *   idx, w       [T][top_k] device outputs, as moe_debug.idx / moe_debug.w
  * router_mode 0, 1 or 2; the group and top-p variants need a handle.
@@ -253,6 +257,8 @@ int moe_debug_view(moe_handle *h, moe_debug *d);
  * value a call reads was written earlier in the same call.  Calls that
  * overlap on the GPU (different streams, or concurrent host threads) race on
  * the scratch and must be serialised by the caller.
+ * A misaligned x or router_w_eh returns MOE_ERR_ARG before any launch.
+ * MOE_ERR_DEVICE reports only errors of this call's own launches.
  * Returns MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_ARG or MOE_ERR_DEVICE.
  */
 int moe_route_noalloc(const void *x, int T, int hidden, int num_experts, int top_k, int x_dtype,

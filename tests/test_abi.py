@@ -106,3 +106,14 @@ def test_strerror():
     assert moe.lib.moe_strerror(-2) == b"invalid routing layout"
     assert b"usage-history" in moe.lib.moe_strerror(-5)
     assert b"another engine" in moe.lib.moe_strerror(-6)
+
+
+@pytest.mark.parametrize("x,w_eh", [(0x1008, 0x2000), (0x1000, 0x2004), (0x1001, 0x2001)])
+def test_route_noalloc_rejects_misaligned_pointers(x, w_eh):
+    """x and the router rows are read with 16-byte vector loads: a pointer off
+    a 16-byte boundary is refused on the host, before any CUDA call (the
+    pointers here are never dereferenced)."""
+    import expert_routing_grouped_gb300 as moe
+    rc = moe.lib.moe_route_noalloc(x, 4, 512, 8, 2, 0, 0, 1.0, w_eh, None, 0x3000, 0x4000,
+                                   None)
+    assert rc == moe.MOE_ERR_ARG
