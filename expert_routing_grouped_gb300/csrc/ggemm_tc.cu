@@ -10,23 +10,38 @@
 //   ggemm_w13:  D[128 weight rows][N tokens] = W13_tile . x_grouped^T, the 128
 //               rows being 64 features' W1 and W3 rows interleaved by 16, so
 //               SwiGLU h = silu(g) * u pairs lanes l and l+16 of one warp;
-//               h is written as bf16 in grouped order.
+//               h is written as fp16 in grouped order.
 //   ggemm_w2:   D[128 output rows][N tokens] = W2_tile . h^T; the epilogue
 //               scales each token's column by its routing weight and writes
 //               y[grouped row][o] in f32.
 //
+// Operands are fp16 (11 significant bits; the same tensor-core rate as bf16)
+// with f32 accumulation, and every quantity is brought into fp16's range by
+// exact powers of two that the epilogues take out again:
+//   x       per token: fp16(x * 2^ex) with |x * 2^ex| < 2^14 (exact for bf16 x);
+//   weights per row:   fp16(q * s * 2^pw) with the row's largest scale times
+//                      2^pw in [2^7, 2^8), so |w| < 2^11;
+//   h       per token: fp16(h * 2^fh) with 2^fh from a bound on |h| that
+//                      cannot be exceeded: |g_i| <= |W1_i| |x| (Cauchy-Schwarz,
+//                      Euclidean norms), |silu(g)| <= max(|g|, 0.279), so
+//                      |h| <= max(N1 |x|, 0.279) N3 |x| with N1, N3 the largest
+//                      W1 / W3 row norms -- then |h * 2^fh| < 2^14.
+// The bound may be loose by a few powers of two; that only moves small
+// elements of h toward fp16's subnormal range, where their absolute error
+// (2^-24 * 2^-fh) stays far below the rounding of the large ones.
+//
 // Per CTA (one per SM, 16 warps):
 //   warp 0      TMA producer of raw int4 weight tiles (128 rows x 256 K, 128-byte
 //               swizzled) and their gs64 scales, 4 stages deep;
-//   warp 2      TMA producer of bf16 token tiles (up to 192 rows x 64 K, 128-byte
+//   warp 2      TMA producer of fp16 token tiles (up to 192 rows x 64 K, 128-byte
 //               swizzled, several K blocks per 32 KB slot for small tiles); the
 //               two producers run independently.
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (fp16 in,
 //               f32 accumulate) M=128, N=16..160, K=16 by one elected lane
 //               (the warp runs the loop, so operands stay uniform), commits
 //               to mbarriers.  A is read from TMEM, B from shared memory.
 //   warps 4-7   epilogue: tcgen05.ld of their TMEM lane quadrant.
-//   warps 8-15  dequant: raw int4 -> bf16(q * s), written straight into TMEM
+//   warps 8-15  dequant: raw int4 -> fp16(q * s * 2^pw), written straight into TMEM
 //               as the MMA's A operand with tcgen05.st (a warp owns one lane
 //               quadrant and half of each 64-K block: one row, 32 K per thread).
 // TMEM (512 columns): two 160-column accumulators, so the epilogue of one tile
@@ -63,7 +78,7 @@ constexpr int NB = 3;            // token slots
 constexpr int NR = 4;            // raw stages
 constexpr int kSlotRows = 384;   // rows of 128 bytes per token slot (48 KB)
 constexpr uint32_t kACol0 = 2 * BN;            // first TMEM column of the A groups
-constexpr uint32_t kGroupCols = KPG * BK / 2;  // 64 columns: 2 bf16 per column
+constexpr uint32_t kGroupCols = KPG * BK / 2;  // 64 columns: 2 fp16 per column
 constexpr int kThreads = 512;
 constexpr int kEpiWarp0 = 4;
 constexpr int kDeqWarp0 = 8;
@@ -98,7 +113,7 @@ struct TcParams {
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
   CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
-  CUtensorMap map_b[4];    // bf16 token operand [R][K], boxes of 32/64/96/192 rows
+  CUtensorMap map_b[4];    // fp16 token operand [R][K], boxes of 32/64/96/192 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
   int K;                   // reduction length (H for W13, I for W2)
   int K_s;                 // the shared expert's reduction length (H, or Is for W2)
@@ -108,11 +123,15 @@ struct TcParams {
   const int32_t *blocks;   // token blocks (expert << 16 | block index)
   const int32_t *n_blocks;
   const int32_t *offsets;  // [E+1]
-  __nv_bfloat16 *hb;       // W13 output [R][h_stride]
+  const float *rexp;       // per weight row 2^pw of the routed experts [E * rows]
+  const float *rexp_s;     // per weight row 2^pw of the shared expert [rows_s]
+  __half *hb;              // W13 output [R][h_stride]: fp16(h * 2^fh)
   int h_stride;
   float *y;                // W2 output [R][H]
   int H;
-  const float *wperm;      // [R]
+  const float *wperm;      // [R] routing weight times 2^-fh (W2 epilogue)
+  const float *xcol;       // [R] 2^-ex of the row's token (W13 epilogue)
+  const float *hcol;       // [R] 2^fh of the row's token (W13 epilogue)
   int32_t *status;
 };
 
@@ -160,8 +179,8 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
 
 // --------------------------------------------------------------- kernel --
 //
-// A = bf16(q * s) per weight (the scale applied in the dequant), one
-// accumulator per tile, bf16 h out of W13.
+// A = fp16(q * s * 2^pw) per weight (the scale applied in the dequant), one
+// accumulator per tile, fp16 h * 2^fh out of W13.
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
@@ -294,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
         tc_fence_after();
         const int ncols = tl.nvalid;
-        const uint32_t idesc = idesc_bf16(BM, (ncols + 15) & ~15);
+        const uint32_t idesc = idesc_f16(BM, (ncols + 15) & ~15);
         const int bi = box_index(ncols);
         const int kps_m1 = box_kps(bi) - 1;                     // K blocks per slot - 1
         const uint32_t jj_desc = (uint32_t)(box_rows(bi) * 128) >> 4;
@@ -359,40 +378,56 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       Tile tl;
       if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
       const int fb = (tl.wrow0 - (tl.shared ? 0 : tl.e * p.rows)) / BM;
+      // 2^-pw of this lane's weight row (exact: a power of two).
+      const float rinv = __frcp_rn(__ldg((tl.shared ? p.rexp_s : p.rexp) + tl.wrow0 + row));
       const int buf = it & 1;
       if (!(ok = wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + lane_base + buf * BN;
       for (int c0 = 0; c0 < tl.nvalid; c0 += 32) {
+        // The chunk's per-column factors: lane j loads column c0 + j once and
+        // the loops below take them by shuffle (a load per column would wait
+        // behind the previous column's stores, which may alias it).
+        const bool lane_col = c0 + lane < tl.nvalid;
+        const float f0 = lane_col ? __ldcg((p.mode == 0 ? p.xcol : p.wperm) + tl.p0 + c0 + lane) : 0.f;
+        const float f1 = (p.mode == 0 && lane_col) ? __ldcg(p.hcol + tl.p0 + c0 + lane) : 0.f;
         float v[32];
         tmem_ld32(tbase + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= rinv;
         if (p.mode == 0) {
           // Rows: lanes 0-15 hold g of features fb*64 + 16q + (lane & 15),
           // lanes 16-31 u of the same.  One exchange per column pair: lanes
           // 0-15 finish token j (their g, the partner's u), lanes 16-31 token
-          // j + 1 (the partner's g, their u).  h is rounded to bf16, so the
-          // fast exponential and division are well inside its resolution.
+          // j + 1 (the partner's g, their u).  g and u carry the token's 2^ex,
+          // taken out before SwiGLU; h is rounded to fp16, so the fast
+          // exponential and division are well inside its resolution.
           const int feat = fb * 64 + q * 16 + (lane & 15);
           const bool lo_half = lane < 16;
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const float recv = __shfl_xor_sync(0xffffffffu, lo_half ? v[j + 1] : v[j], 16);
-            const float g = lo_half ? v[j] : recv;
-            const float u = lo_half ? recv : v[j + 1];
-            const int col = c0 + j + (lo_half ? 0 : 1);
+            const int jc = j + (lo_half ? 0 : 1);
+            const float xc = __shfl_sync(0xffffffffu, f0, jc);
+            const float hc = __shfl_sync(0xffffffffu, f1, jc);
+            const int col = c0 + jc;
             if (col < tl.nvalid) {
+              const int pr = tl.p0 + col;
+              const float g = (lo_half ? v[j] : recv) * xc;
+              const float u = (lo_half ? recv : v[j + 1]) * xc;
               const float e = __expf(fminf(-g, 80.0f));
-              const float hval = __fdividef(g, 1.0f + e) * u;
-              p.hb[(size_t)(tl.p0 + col) * p.h_stride + feat] = __float2bfloat16_rn(hval);
+              const float hval = __fdividef(g, 1.0f + e) * u * hc;
+              p.hb[(size_t)pr * p.h_stride + feat] = __float2half_rn(hval);
             }
           }
         } else {
           const int o = fb * BM + row;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
+            const float wt = __shfl_sync(0xffffffffu, f0, j);
             if (c0 + j < tl.nvalid) {
               const int pr = tl.p0 + c0 + j;
-              p.y[(size_t)pr * p.H + o] = v[j] * p.wperm[pr];
+              p.y[(size_t)pr * p.H + o] = v[j] * wt;
             }
           }
         }
@@ -406,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     // ------------------------------------------------------ dequant
     // Warp w owns TMEM lane quadrant w % 4 (tile rows 32 (w % 4) .. +31, one
     // per lane) and half (w - 8) / 4 of every 64-K block: per raw stage a
-    // thread turns 4 x 32 weights of its row into 4 x 16 bf16x2 columns of the
+    // thread turns 4 x 32 weights of its row into 4 x 16 fp16x2 columns of the
     // stage's A group.  The 32 lanes read 32 consecutive rows of the swizzled
     // raw tile, 8 distinct 16-byte bank groups per 8 lanes.
     const int dw = warp - kDeqWarp0;
@@ -418,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       Tile tl;
       if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
+      const float re = __ldg((tl.shared ? p.rexp_s : p.rexp) + tl.wrow0 + r);   // 2^pw
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
         if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
@@ -441,12 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
           for (int jj = 0; jj < KPG; ++jj) {
             const int j = gi * KPG + jj;
             const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-            const float sv = j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w;
-            const __nv_bfloat16 shi = __float2bfloat16_rn(sv);
-            const __nv_bfloat16 slo = __float2bfloat16_rn(sv - __bfloat162float(shi));
-            const uint32_t shi2 = bf16x2_splat(shi), slo2 = bf16x2_splat(slo);
+            const float sv = (j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w) * re;
+            const __half shi = __float2half_rn(sv);
+            const __half slo = __float2half_rn(sv - __half2float(shi));
+            const uint32_t shi2 = f16x2_splat(shi), slo2 = f16x2_splat(slo);
 #pragma unroll
-            for (int wv = 0; wv < 4; ++wv) dequant_word(words[wv], shi2, slo2, o[jj] + 4 * wv);
+            for (int wv = 0; wv < 4; ++wv) dequant_word_f16(words[wv], shi2, slo2, o[jj] + 4 * wv);
           }
           static_assert(KPG == 2, "two K blocks per A group");
           tmem_st16x2(acol, o[0], acol + BK / 2, o[1]);   // includes the wait
@@ -471,50 +507,110 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 
 // ---------------------------------------------------- gather and combine --
 
-// xp[p] = bf16(x[token of grouped row p]); wperm[p] = routing weight (shared 1).
+// Grouped row p of the tensor-core path, for the token t it carries:
+//   xp[p]    = fp16(x[t] * 2^ex), 2^ex the power of two that puts max |x[t]|
+//              just under 2^14 (exact for bf16 x: 8 significant bits of 11);
+//   xcol[p]  = 2^-ex (the W13 epilogue takes it out of g and u);
+//   hcol[p]  = 2^fh with max(N1 |x[t]|, 0.28) N3 |x[t]| * 2^fh < 2^14, a bound
+//              on |h| (Euclidean norms; N1, N3 = hnorm[0], hnorm[1], each
+//              factor widened by 2% for the fp16 weights' and f32 sums'
+//              rounding);
+//   wperm[p] = the routing weight (1 for the shared expert) times 2^-fh.
+// One warp per row; every row of a token reduces max |x| and |x|^2 in the same
+// order, so all of them get the same factors.
 __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x, int x_is_bf16,
                                                      int T, int H, int k, int n_shared,
                                                      const int32_t *__restrict__ perm,
                                                      const int32_t *__restrict__ n_assigned,
                                                      const float *__restrict__ w,
-                                                     __nv_bfloat16 *__restrict__ xp,
-                                                     float *__restrict__ wperm) {
+                                                     const float *__restrict__ hnorm,
+                                                     __half *__restrict__ xp,
+                                                     float *__restrict__ wperm,
+                                                     float *__restrict__ xcol,
+                                                     float *__restrict__ hcol) {
   pdl_enter();
   perm = after_wait(perm);
   n_assigned = after_wait(n_assigned);
   w = after_wait(w);
   xp = after_wait(xp);
   wperm = after_wait(wperm);
+  xcol = after_wait(xcol);
+  hcol = after_wait(hcol);
   const int A = T * k, R = A + n_shared * T;
   const int n_routed = __ldcg(n_assigned);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const float n1 = __ldg(hnorm) * 1.02f, n3 = __ldg(hnorm + 1) * 1.02f;
   for (int pr = warp; pr < R; pr += nwarps) {
     if (pr >= n_routed && pr < A) continue;   // rows of slots the top-p trim dropped
     int t;
     float wt;
     if (pr < A) {
-      const int a = perm[pr];
+      const int a = __ldcg(perm + pr);
       t = a / k;
-      wt = w[a];
+      wt = __ldcg(w + a);
     } else {
       t = pr - A;
       wt = 1.0f;
     }
-    if (lane == 0) wperm[pr] = wt;
+    const uint4 *src16 = reinterpret_cast<const uint4 *>(
+        reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H);
+    const float4 *src32 = reinterpret_cast<const float4 *>(
+        reinterpret_cast<const float *>(x) + (size_t)t * H);
+    float amax = 0.f, ss = 0.f;
     if (x_is_bf16) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H);
-      uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pr * H);
-      for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+      for (int i = lane; i < H / 8; i += 32) {
+        const uint4 v = __ldg(src16 + i);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float lo = __uint_as_float(wd[c] << 16), hi = __uint_as_float(wd[c] & 0xFFFF0000u);
+          amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+      }
     } else {
-      const float4 *src = reinterpret_cast<const float4 *>(
-          reinterpret_cast<const float *>(x) + (size_t)t * H);
-      __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(xp + (size_t)pr * H);
       for (int i = lane; i < H / 4; i += 32) {
-        const float4 f = __ldg(src + i);
-        dst[2 * i] = __floats2bfloat162_rn(f.x, f.y);
-        dst[2 * i + 1] = __floats2bfloat162_rn(f.z, f.w);
+        const float4 f = __ldg(src32 + i);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    }
+    const int ex = max(-126, min(126, 14 - pow2_above(amax)));
+    const float nrm = sqrtf(ss);
+    const float bound = fmaxf(n1 * nrm, 0.28f) * (n3 * nrm);
+    const int fh = max(-126, min(126, 14 - pow2_above(bound)));
+    if (lane == 0) {
+      wperm[pr] = wt * pow2f(-fh);
+      xcol[pr] = pow2f(-ex);
+      hcol[pr] = pow2f(fh);
+    }
+    const float xs = pow2f(ex);
+    if (x_is_bf16) {
+      uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pr * H);
+      for (int i = lane; i < H / 8; i += 32) {
+        const uint4 v = __ldg(src16 + i);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(wd[c] << 16) * xs,
+                                               __uint_as_float(wd[c] & 0xFFFF0000u) * xs);
+          o[c] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    } else {
+      __half2 *dst = reinterpret_cast<__half2 *>(xp + (size_t)pr * H);
+      for (int i = lane; i < H / 4; i += 32) {
+        const float4 f = __ldg(src32 + i);
+        dst[2 * i] = __floats2half2_rn(f.x * xs, f.y * xs);
+        dst[2 * i + 1] = __floats2half2_rn(f.z * xs, f.w * xs);
       }
     }
   }
@@ -915,7 +1011,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   cudaError_t err = set_tc_attrs();
   if (err != cudaSuccess) return err;
   err = launch_k(h->pdl, gather_kernel, dim3(h->num_sms * 4), dim3(256), 0, st, x,
-                 h->L.x_dtype == 1, T, H, k, S, w.perm, w.offsets + h->E, w.w, w.xp, w.wperm);
+                 h->L.x_dtype == 1, T, H, k, S, w.perm, w.offsets + h->E, w.w,
+                 (const float *)h->hnorm, w.xp, w.wperm, w.xcol, w.hcol);
   if (err != cudaSuccess) return err;
   moe_handle *hm = const_cast<moe_handle *>(h);
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
@@ -926,14 +1023,14 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
 
   TcParams p{};
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   // ---- W13
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, BM);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
                       (uint64_t)2 * (S ? Is : I), H / 2, 128, BM);
   for (int i = 0; i < 4; ++i)
-    ok = ok && make_map(&p.map_b[i], w.xp, BF, 2, H, (uint64_t)maxR, H, BK, kBoxRows[i]);
+    ok = ok && make_map(&p.map_b[i], w.xp, F16, 2, H, (uint64_t)maxR, H, BK, kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w13s, F32, 4, H / 64, (uint64_t)E * 2 * I, H / 64,
                       RK / 64, BM, false);
   ok = ok && make_map(&p.map_scs, S ? h->sh.w13s : h->ex.w13s, F32, 4, H / 64,
@@ -950,11 +1047,15 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.blocks = w.tiles;
   p.n_blocks = w.n_tiles;
   p.offsets = w.offsets;
+  p.rexp = h->ex.w13e;
+  p.rexp_s = S ? h->sh.w13e : h->ex.w13e;
   p.hb = w.hb;
   p.h_stride = h_stride;
   p.y = w.y;
   p.H = H;
   p.wperm = w.wperm;
+  p.xcol = w.xcol;
+  p.hcol = w.hcol;
   p.status = w.status;
   if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
       cudaSuccess)
@@ -969,7 +1070,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   ok = ok && make_map(&p.map_ws, S ? h->sh.w2q : h->ex.w2q, U8, 1, Is / 2, (uint64_t)H, Is / 2, 128,
                       BM);
   for (int i = 0; i < 4; ++i)
-    ok = ok && make_map(&p.map_b[i], w.hb, BF, 2, h_stride, (uint64_t)maxR, h_stride, BK,
+    ok = ok && make_map(&p.map_b[i], w.hb, F16, 2, h_stride, (uint64_t)maxR, h_stride, BK,
                         kBoxRows[i]);
   ok = ok && make_map(&p.map_sc, h->ex.w2s, F32, 4, I / 64, (uint64_t)E * H, I / 64, RK / 64, BM,
                       false);
@@ -981,6 +1082,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.K_s = Is;
   p.rows = H;
   p.rows_s = H;
+  p.rexp = h->ex.w2e;
+  p.rexp_s = S ? h->sh.w2e : h->ex.w2e;
   if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
       cudaSuccess)
     return err;

@@ -132,6 +132,63 @@ __global__ void repack_w13_scales_kernel(const float *__restrict__ s1, const flo
   }
 }
 
+// Per-row power-of-two factor of the tensor-core path's fp16 weights:
+// out[r] = 2^(8 - e) with max_g |s[r][g]| < 2^e, so every |q * s * out[r]| < 2^11
+// and the row's largest scale sits in [2^7, 2^8): well inside fp16's range
+// whatever the model's scale magnitudes.  One warp per row.
+__global__ void row_pow2_kernel(const float *__restrict__ s, long long n_rows, int groups,
+                                float *__restrict__ out) {
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  const int lane = threadIdx.x & 31;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < n_rows; r += nw) {
+    float m = 0.f;
+    for (int g = lane; g < groups; g += 32) m = fmaxf(m, fabsf(s[r * groups + g]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+      const int eb = (__float_as_int(m) >> 23) & 0xFF;
+      const int e = m > 0.f ? (eb > 0 ? eb : 1) - 126 : 8;
+      const int f = max(-126, min(126, 8 - e));
+      out[r] = __int_as_float((f + 127) << 23);
+    }
+  }
+}
+
+// Largest Euclidean row norm of W1 (norms[0]) and of W3 (norms[1]) over the
+// interleaved W13 rows [n_rows][kb] (offset-binary nibbles) and their scales
+// [n_rows][kb/32]; norms are raised with an integer max (non-negative floats
+// order as their bits), so the result does not depend on the order of rows.
+// One warp per row.
+__global__ void w13_norm_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
+                                long long n_rows, int kb, float *__restrict__ norms) {
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int groups = kb / 32;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < n_rows; r += nw) {
+    float acc = 0.f;
+    for (int g = lane; g < groups; g += 32) {
+      const uint32_t *wq = reinterpret_cast<const uint32_t *>(q + r * kb + (size_t)g * 32);
+      int sq = 0;
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w = wq[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int v = (int)((w >> (4 * j)) & 0xFu) - 8;
+          sq += v * v;
+        }
+      }
+      const float sc = s[r * groups + g];
+      acc = fmaf((float)sq * sc, sc, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      const int is_w3 = (r & 31) >= 16;   // the interleaved layout's quadrant halves
+      atomicMax(reinterpret_cast<int *>(norms) + is_w3, __float_as_int(sqrtf(acc)));
+    }
+  }
+}
+
 // In-place nibble repack of a plain [rows][kb] array (W2).
 __global__ void repack_words_kernel(uint32_t *__restrict__ w, long long n_words) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_words;
@@ -156,6 +213,16 @@ cudaError_t launch_repack_w13_scales(const float *s1, const float *s3, float *ds
 cudaError_t launch_repack_words(uint8_t *w, long long n_bytes, cudaStream_t s) {
   return launch_k(false, repack_words_kernel, dim3(152 * 8), dim3(256), 0, s,
                   reinterpret_cast<uint32_t *>(w), n_bytes / 4);
+}
+
+cudaError_t launch_row_pow2(const float *s, long long n_rows, int groups, float *out,
+                            cudaStream_t st) {
+  return launch_k(false, row_pow2_kernel, dim3(152 * 4), dim3(256), 0, st, s, n_rows, groups, out);
+}
+
+cudaError_t launch_w13_norm(const uint8_t *q, const float *s, long long n_rows, int kb,
+                            float *norms, cudaStream_t st) {
+  return launch_k(false, w13_norm_kernel, dim3(152 * 4), dim3(256), 0, st, q, s, n_rows, kb, norms);
 }
 
 cudaError_t launch_transpose_router(const float *src, float *dst, int H, int E, cudaStream_t s) {

@@ -79,15 +79,20 @@ void carve(moe_handle *h, Carver &c) {
   h->wr_t = c.take<float>(E * H);
   h->wr_planes = c.take<__nv_bfloat16>(3 * E * H);
   h->bias = c.take<float>(E);
+  h->hnorm = c.take<float>(2);
   h->ex.w13q = c.take<uint8_t>(E * 2 * I * H / 2);
   h->ex.w2q = c.take<uint8_t>(E * H * I / 2);
   h->ex.w13s = c.take<float>(E * 2 * I * H / 64);
   h->ex.w2s = c.take<float>(E * H * I / 64);
+  h->ex.w13e = c.take<float>(E * 2 * I);
+  h->ex.w2e = c.take<float>(E * H);
   if (S) {
     h->sh.w13q = c.take<uint8_t>(2 * Is * H / 2);
     h->sh.w2q = c.take<uint8_t>(H * Is / 2);
     h->sh.w13s = c.take<float>(2 * Is * H / 64);
     h->sh.w2s = c.take<float>(H * Is / 64);
+    h->sh.w13e = c.take<float>(2 * Is);
+    h->sh.w2e = c.take<float>(H);
   }
   moe::Workspace &w = h->ws;
   const size_t zrows = maxT > (size_t)moe::kRouterSplitMax * moe::kRouteTokens
@@ -109,10 +114,12 @@ void carve(moe_handle *h, Carver &c) {
   w.route_kv = c.take<float>(2 * (size_t)moe::kRouteTokens * E);
   w.usage = c.take<unsigned long long>(E);
   w.h = c.take<float>(rows * Imax);
-  w.hb = c.take<__nv_bfloat16>(rows * Imax);
+  w.hb = c.take<__half>(rows * Imax);
   w.y = c.take<float>(rows * H);
-  w.xp = c.take<__nv_bfloat16>(rows * H);
+  w.xp = c.take<__half>(rows * H);
   w.wperm = c.take<float>(rows);
+  w.xcol = c.take<float>(rows);
+  w.hcol = c.take<float>(rows);
   const size_t rows_x = (size_t)moe::kExactTokens * (h->k + S);
   w.xe = c.take<__nv_bfloat16>(2 * rows_x * H);
   w.he = c.take<__nv_bfloat16>(2 * rows_x * Imax);
@@ -171,6 +178,21 @@ int copy_expert_set(const moe::ExpertWeights &dst, const uint8_t *w1q, const flo
   return MOE_OK;
 }
 
+// The tensor-core path's fp16 range control, from the repacked weights: the
+// per-row power-of-two factors of W13 and W2, and the largest W1 / W3 row
+// norms (raised into hnorm, which the caller zeroes first).
+int tc_weight_factors(const moe::ExpertWeights &ew, size_t n_exp, size_t H, size_t I,
+                      float *hnorm) {
+  if (moe::launch_row_pow2(ew.w13s, (long long)(n_exp * 2 * I), (int)(H / 64),
+                           const_cast<float *>(ew.w13e), 0) != cudaSuccess ||
+      moe::launch_row_pow2(ew.w2s, (long long)(n_exp * H), (int)(I / 64),
+                           const_cast<float *>(ew.w2e), 0) != cudaSuccess ||
+      moe::launch_w13_norm(ew.w13q, ew.w13s, (long long)(n_exp * 2 * I), (int)(H / 2), hnorm,
+                           0) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
 int copy_weights(moe_handle *h, const moe_weights *W) {
   const size_t E = h->E, H = h->H, I = h->I, Is = h->Is;
   // One staging buffer: at least one expert's W1+W3, at most 512 MB.
@@ -189,6 +211,9 @@ int copy_weights(moe_handle *h, const moe_weights *W) {
   if (rc == MOE_OK && h->S)
     rc = copy_expert_set(h->sh, W->sw1_q, W->sw1_s, W->sw3_q, W->sw3_s, W->sw2_q, W->sw2_s, 1, H,
                          Is, stage, stage_bytes);
+  if (rc == MOE_OK && cudaMemset(h->hnorm, 0, 2 * sizeof(float)) != cudaSuccess) rc = MOE_ERR_DEVICE;
+  if (rc == MOE_OK) rc = tc_weight_factors(h->ex, E, H, I, h->hnorm);
+  if (rc == MOE_OK && h->S) rc = tc_weight_factors(h->sh, 1, H, Is, h->hnorm);
   if (rc == MOE_OK) {
     if (W->router_bias) {
       if (cudaMemcpy(h->bias, W->router_bias, E * 4, cudaMemcpyDefault) != cudaSuccess)

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -33,9 +34,12 @@ enum Status : int32_t {
 // interleaved [n_experts][2I][H/2] array (see misc.cu), W2 is [n_experts][H][I/2];
 // both with repacked offset-binary nibbles.  Scales are f32, gs64, in the same
 // row order: w13s [n_experts][2I][H/64], w2s [n_experts][H][I/64].
+// w13e / w2e: per-row power-of-two factors of the tensor-core path's fp16
+// weights (fp16(q * s * e) in the MMA, the accumulator times 1/e after it).
 struct ExpertWeights {
   const uint8_t *w13q, *w2q;
   const float *w13s, *w2s;
+  const float *w13e, *w2e;
 };
 
 struct Workspace {
@@ -59,10 +63,13 @@ struct Workspace {
   unsigned long long *usage;  // [E] assignments per expert over the counted forwards
   // expert activations
   float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
-  __nv_bfloat16 *hb;  // [max_tokens*k + S*max_tokens][I_max] bf16 (tensor-core path)
+  __half *hb;         // [max_tokens*k + S*max_tokens][I_max] fp16 h * 2^fh (tensor-core path)
   float *y;           // [max_tokens*k + S*max_tokens][H] f32 (tensor-core path)
-  __nv_bfloat16 *xp;  // [max_tokens*k + S*max_tokens][H] bf16 activations in grouped order
-  float *wperm;       // [max_tokens*k + S*max_tokens] routing weight per grouped row (shared 1)
+  __half *xp;         // [max_tokens*k + S*max_tokens][H] fp16 x * 2^ex in grouped order
+  float *wperm;       // [max_tokens*k + S*max_tokens] routing weight per grouped row (shared 1);
+                      // on the tensor-core path times 2^-fh of the row's token
+  float *xcol;        // [max_tokens*k + S*max_tokens] 2^-ex of the row's token (tensor-core path)
+  float *hcol;        // [max_tokens*k + S*max_tokens] 2^fh of the row's token (tensor-core path)
   // exact tensor-core mode (T <= kExactTokens): operands as bf16 (hi, lo) plane pairs
   __nv_bfloat16 *xe;  // [2 * kExactTokens*(k+S)][H] grouped x (one plane when x is bf16)
   __nv_bfloat16 *he;  // [2 * kExactTokens*(k+S)][I_max] h planes
@@ -129,6 +136,7 @@ struct moe_handle {
   float *wr_t;                   // [E][H] f32 router weights, transposed
   __nv_bfloat16 *wr_planes;      // [3][E][H] bf16 hi/mid/lo planes of wr_t (tensor-core router)
   float *bias;                   // [E] or nullptr
+  float *hnorm;                  // [2] largest W1 / W3 row norm over all experts (bounds |h|)
   moe::ExpertWeights ex;         // routed experts
   moe::ExpertWeights sh;         // shared expert (single)
   moe::Workspace ws;
@@ -198,6 +206,14 @@ cudaError_t launch_repack_w13(const uint8_t *w1, const uint8_t *w3, uint8_t *dst
 cudaError_t launch_repack_w13_scales(const float *s1, const float *s3, float *dst, long long n_exp,
                                      int I, int groups, cudaStream_t s);
 cudaError_t launch_repack_words(uint8_t *w, long long n_bytes, cudaStream_t s);
+// out[r] = the power of two that scales row r's gs64 scales [n_rows][groups]
+// into [2^7, 2^8) (fp16 weights of the tensor-core path).
+cudaError_t launch_row_pow2(const float *s, long long n_rows, int groups, float *out,
+                            cudaStream_t s_);
+// norms[0], norms[1] (raised, not reset) = the largest Euclidean norm of a W1
+// row and of a W3 row of an interleaved W13 array [n_rows][kb].
+cudaError_t launch_w13_norm(const uint8_t *q, const float *s, long long n_rows, int kb,
+                            float *norms, cudaStream_t st);
 
 // Row of W1 (is_w3 = 0) or W3 (1) feature f in the interleaved W13 layout.
 __host__ __device__ __forceinline__ size_t w13_row_of(int f, int is_w3) {

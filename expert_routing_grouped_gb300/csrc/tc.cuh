@@ -1,9 +1,11 @@
 // tc.cuh -- tcgen05 glue shared by the tensor-core kernels: shared-memory
 // matrix and instruction descriptors, MMA issue with A in tensor memory,
-// tensor-memory loads and stores, and the int4 -> bf16 decodes that feed A.
+// tensor-memory loads and stores, and the int4 -> bf16 / fp16 decodes that
+// feed A.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -34,6 +36,14 @@ static __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4)                          // D format f32
          | (1u << 7)                        // A format bf16
          | (1u << 10)                       // B format bf16
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), f32 accumulator
+// (format fields 0 = f16; A and B of one MMA always share a type).
+static __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4)                          // D format f32
          | ((uint32_t)(N >> 3) << 17)       // N / 8
          | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
@@ -160,34 +170,11 @@ static __device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-static __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-static __device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
 static __device__ __forceinline__ uint32_t lop_nib(uint32_t w) {
   uint32_t d;
   // (w & 0x000F000F) | 0x43004300: two offset-binary nibbles into bf16 128 + n.
   asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(d) : "r"(w));
   return d;
-}
-
-// 8 weights of one library-layout word -> 4 bf16x2 words of bf16(q * s), with
-// s = s_hi + s_lo split into two bf16 (q * s_hi is exact inside the fused
-// multiply-add, q * s_lo contributes below bf16 resolution).
-static __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_hi2, uint32_t s_lo2,
-                                             uint32_t out[4]) {
-  const uint32_t c136 = 0x43084308u;   // bf16x2 (136, 136)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t q = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
-    out[i] = hfma2_bf16(q, s_hi2, hmul2_bf16(q, s_lo2));
-  }
 }
 
 // 8 weights of one library-layout word -> 4 bf16x2 words of the exact codes q.
@@ -197,10 +184,59 @@ static __device__ __forceinline__ void dequant_word_q(uint32_t w, uint32_t out[4
   for (int i = 0; i < 4; ++i) out[i] = hsub2_bf16(lop_nib(w >> (4 * i)), c136);
 }
 
-static __device__ __forceinline__ uint32_t bf16x2_splat(__nv_bfloat16 v) {
-  const uint16_t b = __bfloat16_as_ushort(v);
+// fp16x2 arithmetic on raw 32-bit registers.
+static __device__ __forceinline__ uint32_t hsub2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+static __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+static __device__ __forceinline__ uint32_t hfma2_f16(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+static __device__ __forceinline__ uint32_t lop_nib16(uint32_t w) {
+  uint32_t d;
+  // (w & 0x000F000F) | 0x64006400: two offset-binary nibbles n into fp16
+  // 1024 + n (the unit in the last place of 1024 is 1 in fp16).
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(d) : "r"(w));
+  return d;
+}
+
+// 8 weights of one library-layout word -> 4 fp16x2 words of fp16(q * s), with
+// s = s_hi + s_lo split into two fp16: q = (1024 + n) - 1032 is exact, q * s_hi
+// is exact inside the fused multiply-add, q * s_lo adds the part below fp16
+// resolution, and the sum is rounded once.
+static __device__ __forceinline__ void dequant_word_f16(uint32_t w, uint32_t s_hi2, uint32_t s_lo2,
+                                                        uint32_t out[4]) {
+  const uint32_t c1032 = 0x64086408u;   // fp16x2 (1032, 1032)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = hsub2_f16(lop_nib16(w >> (4 * i)), c1032);
+    out[i] = hfma2_f16(q, s_hi2, hmul2_f16(q, s_lo2));
+  }
+}
+
+static __device__ __forceinline__ uint32_t f16x2_splat(__half v) {
+  const uint16_t b = __half_as_ushort(v);
   return (uint32_t)b | ((uint32_t)b << 16);
 }
+
+// 2^e as an f32, e in [-126, 127].
+static __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// The exponent e of a power of two with |v| < 2^e for a finite v >= 0 (v = 0
+// and subnormals give -125).
+static __device__ __forceinline__ int pow2_above(float v) {
+  const int eb = (__float_as_int(v) >> 23) & 0xFF;
+  return (eb > 0 ? eb : 1) - 126;
+}
+
 
 
 // Thread i of the warp writes 32 consecutive 32-bit columns of TMEM lane

@@ -271,19 +271,23 @@ def test_init_fault_injection_leaks_nothing(dev):
 
 # ------------------------------------------------------------ tensor cores --
 
-TC_TOL = 5e-3          # relative L2 on the bf16 tensor-core path
-# Largest element error of a token, in units of that token's output rms.  The
-# bf16 path's error scales with each token's own expert outputs (rounding of
-# its h and of the weights), and the largest of N near-Gaussian errors whose
-# rms is at most TC_TOL of the signal is about sqrt(2 ln N) * TC_TOL, 5.8 *
-# TC_TOL for N = T*H up to 25M elements.
-TC_MAXABS = 6 * TC_TOL
+# The tensor-core path's bar: relative L2 <= 5e-3 and the largest element
+# error <= 2e-2 of the reference's rms over the whole compared output.  The
+# same 2e-2 is also held per token against that token's own rms (stricter for
+# tokens whose outputs are small).  The fp16 operands give about 4e-4 relative
+# L2 and 2e-3 rms on these workloads (a CPU emulation of the kernel's
+# roundings), so both bars hold with a wide margin.
+TC_TOL = 5e-3
+TC_MAXABS = 2e-2
 
 
 def check_tc(got, ref_out):
-    assert rel_l2(got, ref_out) <= TC_TOL
-    rms_t = np.sqrt(np.mean(np.asarray(ref_out, np.float64) ** 2, axis=1))
-    assert np.all(np.max(np.abs(got - ref_out), axis=1) <= TC_MAXABS * rms_t)
+    ref = np.asarray(ref_out, np.float64)
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    assert rel_l2(got, ref) <= TC_TOL
+    assert err.max() <= TC_MAXABS * np.sqrt(np.mean(ref ** 2))
+    rms_t = np.sqrt(np.mean(ref ** 2, axis=1))
+    assert np.all(err.max(axis=1) <= TC_MAXABS * rms_t)
 
 
 def run_tc(wl, T, dev, rows=None):
@@ -337,6 +341,75 @@ def test_tc_path_parity_full_size(dev, name, T, n):
     h.forward(xd, T, out2)
     torch.cuda.synchronize()
     assert np.array_equal(out2.cpu().numpy(), got)
+
+
+def _host_layer(wl, T, dev, experts, Wr):
+    """A layer built from host weight arrays (routed experts only)."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    stack = [np.stack([experts[e][i] for e in range(wl.E)]) for i in range(6)]
+    t = {n: torch.from_numpy(np.ascontiguousarray(a)).to(dev) for n, a in zip(
+        ("w1_q", "w1_s", "w3_q", "w3_s", "w2_q", "w2_s"), stack)}
+    t["router_w"] = torch.from_numpy(np.ascontiguousarray(Wr)).to(dev)
+    return moe.MoELayer(moe.layout_for(wl, T), t)
+
+
+@pytest.mark.parametrize("x_mul,s_mul", [(2.0 ** 12, 2.0 ** -20), (2.0 ** -16, 2.0 ** 6),
+                                         (1.0, 2.0 ** -24)])
+def test_tc_fp16_range(dev, x_mul, s_mul):
+    """The tensor-core path keeps its fp16 operands in range with exact powers
+    of two: x per token, weights per row, h per token from its bound.  With
+    activations and gs64 scales far from 1 -- where unscaled fp16 weights,
+    activations or h would underflow or overflow -- the output keeps the same
+    accuracy.  Scaling x by a power of two scales every f32 logit exactly, so
+    the routing stays the margin-checked one."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["tiny"]
+    T = 16
+    Wr = synth.router_w(wl)
+    experts = {}
+    for e in range(wl.E):
+        w = list(synth.expert_weights(wl, 0, e))
+        for i in (1, 3, 5):
+            w[i] = (w[i] * np.float32(s_mul)).astype(np.float32)
+        experts[e] = tuple(w)
+    x0, _ = margin_x(wl, T, Wr, None)
+    x = (x0 * np.float32(x_mul)).astype(np.float32)
+    L = oracle.layout(wl)
+    ref, ref_idx, _ = oracle.moe_forward(L, oracle.weights(L, Wr, None, experts), x)
+    layer = _host_layer(wl, T, dev, experts, Wr)
+    try:
+        layer.set_option(moe.MOE_OPT_REGIME, moe.REGIME_TC)
+        out = torch.full((T, wl.H), float("nan"), device=dev)
+        layer.forward(torch.from_numpy(x).to(dev), T, out)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert np.array_equal(layer.debug_read(moe.MOE_DBG_IDX).reshape(T, wl.k), ref_idx)
+        got = out.cpu().numpy()
+        assert np.all(np.isfinite(got))
+        check_tc(got, ref)
+        assert rel_l2(got, ref) <= 1e-3      # fp16 accuracy, not merely the bar
+    finally:
+        layer.close()
+
+
+def test_forward_rejects_misaligned_pointers(dev):
+    """x and out are accessed with 16-byte vectors: a view 4 bytes off the
+    allocation is refused with MOE_ERR_ARG before any launch."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["tiny"]
+    h, Wr, bias = get_layer(wl, 16, dev)
+    x = torch.zeros(17 * wl.H, device=dev)
+    out = torch.zeros(17 * wl.H, device=dev)
+    good_x, good_o = x.data_ptr(), out.data_ptr()
+    for xp, op in ((good_x + 4, good_o), (good_x, good_o + 4)):
+        assert moe.lib.moe_forward(h.handle, xp, 4, op, None) == moe.MOE_ERR_ARG
+        assert moe.lib.moe_forward_residual(h.handle, xp, 4, op, None) == moe.MOE_ERR_ARG
+    assert moe.lib.moe_route(h.handle, good_x + 4, 4, None) == moe.MOE_ERR_ARG
+    assert moe.lib.moe_forward(h.handle, good_x, 4, good_o, None) == moe.MOE_OK
+    torch.cuda.synchronize()
 
 
 def test_tc_and_gemv_agree(dev):
@@ -463,7 +536,7 @@ def test_router_variant_noalloc_raw_softmax(dev):
 
 def test_auto_regime_choice(dev):
     """Automatic expert path: one token on the SIMT GEMV path, 2-8 on the exact
-    tensor-core decode path, more on the bf16 tensor-core path."""
+    tensor-core decode path, more on the fp16 tensor-core path."""
     import torch
     import expert_routing_grouped_gb300 as moe
     wl = synth.BY_NAME["glm_decode"]
