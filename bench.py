@@ -217,11 +217,13 @@ def distinct_active(idx_rows, n_shared):
     return len(np.unique(idx_rows)) + n_shared
 
 
-def layer_bytes(wl, n_active, T):
+def layer_bytes(wl, n_active, T, n_shared_active=None):
     """Algorithmic bytes of one layer: activated experts' packed int4 + gs64
-    scales, router, bias, x (bf16) and out (f32)."""
+    scales (n_active counts the shared expert), router, bias, x (bf16, or f32
+    for the f32-input workloads) and out (f32)."""
+    xb = 4 if wl.x_dtype == 0 else 2
     return (n_active * 3 * wl.H * wl.I * 9 // 16 + wl.H * wl.E * 4 + wl.E * 4
-            + T * wl.H * 2 + T * wl.H * 4)
+            + T * wl.H * xb + T * wl.H * 4)
 
 
 def layer_flops(wl, T):
@@ -392,35 +394,171 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     return res
 
 
+# -------------------------------------------------------------- configs --
+
+# Every seeded configuration (workload, T) besides the prefill headline: the
+# tiny layer, the OLMoE- and Mixtral-shaped layers at their batch sizes and
+# one GLM-shaped decode layer at the MTP-verify sizes.
+CONFIG_CASES = (("tiny", (16,)), ("olmoe", (1, 64)), ("mixtral", (1, 4, 512)),
+                ("glm_decode", (1, 2, 4)))
+FLUSH_BYTES = 384 << 20       # > the 129 MB L2
+
+
+def bench_configs(dev, stream, steps, warmup, pk, src):
+    """One layer per call (layer 0 of the workload), CUDA events around each
+    moe_forward on its stream, the L2 flushed (a 384 MB write) before every
+    timed call and outside the events; median and p90 over `steps` calls.
+    Bytes and FLOPs are the algorithmic ones of the call's own routing, and
+    the roofline is max(bytes / HBM peak, FLOPs / tensor peak)."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    import synth
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    cases = []
+    for name, Ts in CONFIG_CASES:
+        wl = synth.BY_NAME[name]
+        layer, _, _ = make_layer(wl, 0, max(Ts), dev)
+        for T in Ts:
+            x = torch.from_numpy(synth.x_rows(wl, T)).to(dev)
+            out = torch.empty(T, wl.H, device=dev)
+            cases.append((wl, T, layer, x, out))
+    torch.cuda.synchronize()
+
+    def region():
+        res = []
+        with torch.cuda.stream(stream):
+            for wl, T, layer, x, out in cases:
+                for _ in range(warmup):
+                    layer.forward(x, T, out, stream)
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(steps)]
+                for i in range(steps):
+                    flush.fill_(float(i))
+                    evs[i][0].record(stream)
+                    layer.forward(x, T, out, stream)
+                    evs[i][1].record(stream)
+                torch.cuda.synchronize()
+                # this case's own routing and expert path (the layer serves several T)
+                idx = layer.debug_read(moe.MOE_DBG_IDX)
+                res.append(([a.elapsed_time(b) for a, b in evs],
+                            distinct_active(idx[idx >= 0], wl.n_shared),
+                            layer.debug_view().regime))
+        return res
+
+    times, clocks = timed_region(dev, region)
+    tpk, tsrc = tensor_peak(pk, src, clocks)
+    out = []
+    for (wl, T, layer, x, _), (ms, na, regime) in zip(cases, times):
+        by = layer_bytes(wl, na, T)
+        fl = layer_flops(wl, T)
+        med = statistics.median(ms)
+        p90 = sorted(ms)[min(len(ms) - 1, int(0.9 * len(ms)))]
+        t_hbm = by / (pk["hbm_gbs"] * 1e9)
+        t_tc = fl / (tpk * 1e12)
+        out.append({"workload": wl.name, "T": T, "regime": regime,
+                    "us_per_layer": round(1e3 * med, 2), "us_p90": round(1e3 * p90, 2),
+                    "tokens_per_s": round(T / (med * 1e-3), 1),
+                    "activated_experts": int(na), "bytes": int(by), "flops": int(fl),
+                    "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                    "hbm_gbs": round(by / (med * 1e-3) / 1e9, 1),
+                    "tflops": round(fl / (med * 1e-3) / 1e12, 2),
+                    "roofline_us": round(1e6 * max(t_hbm, t_tc), 2),
+                    "frac": round(max(t_hbm, t_tc) / (med * 1e-3), 4)})
+    for c in {id(c[2]): c[2] for c in cases}.values():
+        c.close()
+    del flush, cases
+    torch.cuda.empty_cache()
+    return {"protocol": "one layer per call, CUDA events on the launching stream, L2 flushed "
+                        "(384 MB write) before each timed call, median of %d calls after %d "
+                        "warm-up calls; roofline = max(bytes / HBM peak, FLOPs / tensor peak)"
+                        % (steps, warmup),
+            "peaks": {"hbm_gbs": pk["hbm_gbs"], "tensor_tflops": tpk, "tensor_peak_source": tsrc},
+            "clocks": clocks, "cases": out}
+
+
 # ---------------------------------------------------------- cpu baseline --
 
-def oracle_sample(wl, rows, x):
-    """Time the oracle as it stands on x[rows] of the workload (layer 0)."""
-    import oracle
-    import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from inputs import oracle_weights_for
-    Wr = synth.router_w(wl)
-    bias = synth.router_bias(wl)
-    t0 = time.perf_counter()
-    L = oracle.layout(wl)
-    idx, _, _, _ = oracle.route(L, oracle.weights(L, Wr, bias), x[rows])
-    L, W, _, _ = oracle_weights_for(wl, 0, Wr, bias, np.unique(idx))
-    oracle.moe_forward(L, W, x[rows])
-    return time.perf_counter() - t0
+def host_cpu():
+    """The host's CPU model and its physical core count (lscpu, else
+    /proc/cpuinfo and os.cpu_count)."""
+    model, cores = None, None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        kv = {}
+        for ln in out.splitlines():
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                kv[k.strip()] = v.strip()
+        model = kv.get("Model name")
+        cps, sockets = kv.get("Core(s) per socket"), kv.get("Socket(s)")
+        if cps and sockets and cps.isdigit() and sockets.isdigit():
+            cores = int(cps) * int(sockets)
+        elif cps and cps.isdigit():
+            cores = int(cps)
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not cores:
+        cores = os.cpu_count() or 1
+    return {"model": model or "unknown", "physical_cores": cores, "logical_cpus": os.cpu_count()}
+
+
+class OracleSample:
+    """The oracle on a bounded sample of a workload's tokens, with everything
+    that is not the oracle done beforehand: the sample's routing decides which
+    experts it needs, and their int4 weights are generated before any timing.
+    run(threads) then times oracle.moe_forward alone -- on the whole sample
+    (threads = 1), or on `threads` disjoint token chunks from as many host
+    threads at once (the same C, unmodified: a token's output depends only on
+    its own row, and the library call releases the interpreter lock)."""
+
+    def __init__(self, wl, rows, x):
+        import oracle
+        import synth
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from inputs import oracle_weights_for
+        self.wl = wl
+        Wr = synth.router_w(wl)
+        bias = synth.router_bias(wl)
+        self.x = np.ascontiguousarray(x[rows])
+        L = oracle.layout(wl)
+        idx, _, _, _ = oracle.route(L, oracle.weights(L, Wr, bias), self.x)
+        need = np.unique(idx)
+        self.L, self.W, self._ex, self._sh = oracle_weights_for(wl, 0, Wr, bias, need[need >= 0])
+
+    def run(self, threads=1):
+        import concurrent.futures as cf
+        import oracle
+        chunks = [c for c in np.array_split(np.arange(len(self.x)), threads) if len(c)]
+        t0 = time.perf_counter()
+        if len(chunks) == 1:
+            oracle.moe_forward(self.L, self.W, self.x)
+        else:
+            with cf.ThreadPoolExecutor(len(chunks)) as ex:
+                list(ex.map(lambda c: oracle.moe_forward(self.L, self.W, self.x[c]), chunks))
+        return time.perf_counter() - t0
 
 
 def cpu_baseline(wl, T, n_tokens, layers_per_step=1):
+    """The oracle timed on the host: all physical cores (one thread per core,
+    the headline) and one core, each on a bounded sample of the batch."""
     import synth
+    cpu = host_cpu()
+    n = cpu["physical_cores"]
     x = synth.x_rows(wl, T)
-    rows = np.arange(n_tokens)
-    dt = oracle_sample(wl, rows, x)
-    return {"value": n_tokens / (dt * layers_per_step), "unit": "tokens/s", "cores": 1,
-            "kind": "oracle",
-            "sample": "oracle f64 (plain C, 1 thread) on tokens 0..%d of the %s batch through "
-                      "one layer (routing, dispatch, expert FFNs incl. host weight generation, "
-                      "combine): %.1f s, scaled to %d layer(s) per step"
-                      % (n_tokens - 1, wl.name, dt, layers_per_step)}
+    one = OracleSample(wl, np.arange(n_tokens), x)
+    dt1 = one.run(1)
+    many = OracleSample(wl, np.arange(min(T, n_tokens * n)), x)
+    dtn = many.run(n)
+    n_many = len(many.x)
+    return {"value": n_many / (dtn * layers_per_step), "unit": "tokens/s", "cores": n,
+            "kind": "oracle", "cpu": cpu,
+            "sample": "oracle f64 (plain C, unmodified) on tokens 0..%d of the %s batch through "
+                      "one layer (routing, dispatch, expert FFNs, combine), %d threads on disjoint "
+                      "token chunks, weights generated before timing: %.1f s, scaled to %d "
+                      "layer(s) per step" % (n_many - 1, wl.name, n, dtn, layers_per_step),
+            "one_core": {"value": n_tokens / (dt1 * layers_per_step), "unit": "tokens/s",
+                         "cores": 1,
+                         "sample": "tokens 0..%d, one thread: %.1f s" % (n_tokens - 1, dt1)}}
 
 
 # ------------------------------------------------------------------ main --
@@ -454,20 +592,47 @@ def traffic(kernel):
     return e.get("bytes_per_launch")
 
 
+def tensor_peak(pk, src, clocks):
+    """The dense fp16/bf16 tensor peak that applies to a timed region.  The
+    path's operands are fp16, whose nominal dense rate equals bf16's, so the
+    measured bf16 figure applies at ratio 1.  A region that ran at the maximum
+    SM clock with no power cap takes the burst peak (the denominators were
+    measured as a burst and as a seconds-long power-capped loop); otherwise
+    the sustained one."""
+    c = clocks or {}
+    sm, mx = c.get("sm_mhz"), c.get("sm_max_mhz")
+    capped = "sw_power_cap" in (c.get("reasons") or [])
+    at_max = bool(sm and mx and sm >= 0.97 * mx)
+    if at_max and not capped:
+        return pk["bf16_tflops"], "%s bf16_tflops (burst) x 1.0 for fp16; timed at %s of %s MHz, " \
+            "no power cap" % (src, sm, mx)
+    return pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), \
+        "%s bf16_tflops_sustained x 1.0 for fp16; timed at %s of %s MHz%s" % (
+            src, sm, mx, ", power-capped" if capped else "")
+
+
 def roofline_tc(res, pk, src):
+    """The dominant kernel (W13 grouped GEMM) against the tensor peak, with
+    the W2 pass beside it."""
     wl, T = res["wl"], res["T"]
     rows = T * wl.k + wl.n_shared * T
-    fl = 2 * rows * wl.H * 2 * wl.I
-    ms = res["stage"].get("w13")
-    if not ms:
+    fl13 = 2 * rows * wl.H * 2 * wl.I
+    fl2 = 2 * rows * wl.I * wl.H
+    ms13, ms2 = res["stage"].get("w13"), res["stage"].get("w2")
+    if not ms13:
         return None
-    ach = fl / (ms * 1e-3) / 1e12
-    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    return {"kernel": "ggemm_w13_tc", "bound": "tensor", "achieved": round(ach, 1),
-            "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-            "traffic": traffic("ggemm_w13_tc") if wl.name == "glm_prefill" else None,
-            "peak_source": "%s bf16_tflops_sustained" % src,
-            "per_launch": "2*(T*k+T)*H*2I = %.3g FLOP" % fl}
+    peak, psrc = tensor_peak(pk, src, res.get("clocks"))
+    ach = fl13 / (ms13 * 1e-3) / 1e12
+    out = {"kernel": "ggemm_w13_tc", "bound": "tensor", "achieved": round(ach, 1),
+           "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+           "traffic": traffic("ggemm_w13_tc") if wl.name == "glm_prefill" else None,
+           "peak_source": psrc,
+           "per_launch": "2*(T*k+T)*H*2I = %.3g FLOP" % fl13}
+    if ms2:
+        a2 = fl2 / (ms2 * 1e-3) / 1e12
+        out["w2"] = {"kernel": "ggemm_w2_tc", "achieved": round(a2, 1), "frac": round(a2 / peak, 4),
+                     "per_launch": "2*(T*k+T)*I*H = %.3g FLOP" % fl2}
+    return out
 
 
 def roofline_gemv(res, pk, src):
@@ -498,7 +663,7 @@ def make_line(pre, dec, world, reduce_max, pk, src, steps, warmup):
     line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if head is pre else "f32", "data": "synthetic",
+            "dtype": "f16" if head is pre else "f32", "data": "synthetic",
             "config": {"workload": head["wl"].name, "T": head["T"],
                        "layers_per_step": 1 if head is pre else head["layers"],
                        "parallelism": "replicas" if world > 1 else "single",
@@ -547,6 +712,8 @@ def main():
                     choices=["both", "prefill", "decode", "prefill_small", "decode_small"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config measurements (every seeded configuration)")
     ap.add_argument("--decode-tokens", type=int, default=1, choices=range(1, 9),
                     help="tokens per decode step (1: the GEMV path; 2-8: the decode "
                          "tensor-core kernel, as for MTP verification)")
@@ -563,18 +730,26 @@ def main():
         wl = synth.BY_NAME["glm_prefill" if args.workload != "decode" else "glm_decode"]
         T = 4096 if wl.name == "glm_prefill" else args.decode_tokens
         x = synth.x_rows(wl, T)
+        cpu = host_cpu()
+        n = cpu["physical_cores"]
+        # each step: one token per physical core, one thread per core
+        smp = OracleSample(wl, np.arange(min(T, n)), x)
+        per_step = len(smp.x)
         for _ in range(min(args.warmup, 1)):
-            oracle_sample(wl, np.arange(1), x)
-        times = [oracle_sample(wl, np.arange(1), x) for _ in range(args.steps)]
-        v = 1.0 / statistics.mean(times)
+            smp.run(n)
+        times = [smp.run(n) for _ in range(args.steps)]
+        v = per_step / statistics.mean(times)
         line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": v,
                 "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl.name, "sample_tokens_per_step": 1},
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                 "sample": "1 token of the %s batch per step" % wl.name},
+                "config": {"workload": wl.name, "sample_tokens_per_step": per_step},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                                 "cpu": cpu,
+                                 "sample": "%d tokens of the %s batch per step, one per host "
+                                           "thread, weights generated before timing"
+                                           % (per_step, wl.name)},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -623,6 +798,26 @@ def main():
 
     line = make_line(pre, dec, world, reduce_max, pk, src, args.steps, args.warmup)
     head = pre if pre is not None else dec
+    if world == 1 and not args.no_configs and args.workload == "both":
+        cfg = bench_configs(dev, stream, args.steps, args.warmup, pk, src)
+        if pre is not None:     # the headline, in the same table
+            rows = pre["T"] * pre["wl"].k + pre["wl"].n_shared * pre["T"]
+            fl = layer_flops(pre["wl"], pre["T"])
+            by = layer_bytes(pre["wl"], pre["wl"].E + 1, pre["T"])
+            med = statistics.median(pre["step_ms"])
+            tpk, _ = tensor_peak(pk, src, pre["clocks"])
+            t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), fl / (tpk * 1e12)
+            cfg["cases"].append({"workload": pre["wl"].name, "T": pre["T"], "regime": pre["regime"],
+                                 "us_per_layer": round(1e3 * med, 2),
+                                 "tokens_per_s": round(pre["T"] / (med * 1e-3), 1),
+                                 "activated_experts": pre["wl"].E + 1, "bytes": int(by),
+                                 "flops": int(fl), "bound": "tensor" if t_tc > t_hbm else "hbm",
+                                 "tflops": round(fl / (med * 1e-3) / 1e12, 2),
+                                 "roofline_us": round(1e6 * max(t_hbm, t_tc), 2),
+                                 "frac": round(max(t_hbm, t_tc) / (med * 1e-3), 4),
+                                 "note": "the headline step (CUDA events, inputs larger than L2)"})
+            del rows
+        line["configs"] = cfg
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the host baseline: N = 1 only
         line["cpu_baseline"] = cpu_baseline(head["wl"], head["T"], 8 if head is pre else 1,
                                             1 if head is pre else head["layers"])

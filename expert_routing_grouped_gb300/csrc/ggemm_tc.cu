@@ -19,8 +19,8 @@
 // with f32 accumulation, and every quantity is brought into fp16's range by
 // exact powers of two that the epilogues take out again:
 //   x       per token: fp16(x * 2^ex) with |x * 2^ex| < 2^14 (exact for bf16 x);
-//   weights per row:   fp16(q * s * 2^pw) with the row's largest scale times
-//                      2^pw in [2^7, 2^8), so |w| < 2^11;
+//   weights per row:   fp16(q * fp16(s * 2^pw)) with the row's largest scale
+//                      times 2^pw in [2^7, 2^8), so |w| < 2^11;
 //   h       per token: fp16(h * 2^fh) with 2^fh from a bound on |h| that
 //                      cannot be exceeded: |g_i| <= |W1_i| |x| (Cauchy-Schwarz,
 //                      Euclidean norms), |silu(g)| <= max(|g|, 0.279), so
@@ -33,9 +33,9 @@
 // Per CTA (one per SM, 16 warps):
 //   warp 0      TMA producer of raw int4 weight tiles (128 rows x 256 K, 128-byte
 //               swizzled) and their gs64 scales, 4 stages deep;
-//   warp 2      TMA producer of fp16 token tiles (up to 192 rows x 64 K, 128-byte
-//               swizzled, several K blocks per 32 KB slot for small tiles); the
-//               two producers run independently.
+//   warp 2      TMA producer of fp16 token tiles (up to 160 rows x 64 K, 128-byte
+//               swizzled, several K blocks per 40 KB slot); the two producers
+//               run independently.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (fp16 in,
 //               f32 accumulate) M=128, N=16..160, K=16 by one elected lane
 //               (the warp runs the loop, so operands stay uniform), commits
@@ -47,9 +47,12 @@
 // TMEM (512 columns): two 160-column accumulators, so the epilogue of one tile
 // overlaps the main loop of the next, and two 64-column A groups (2 K blocks
 // of 64 each), so the dequant of one group overlaps the MMAs of the other.
-// An issuing thread pays ~110 clocks per MMA for any N up to 192, so the tile
-// is as wide as TMEM allows while both accumulators fit; 192-token tiles
-// (A groups then in columns 384-511) were not bitwise repeatable and are not used.
+// One issuing thread keeps the tensor pipe full for N >= 128 (an M=128, K=16
+// MMA takes N/2 clocks there; below N = 128 about 59 clocks whatever N), so
+// the tile is as wide as TMEM allows while both accumulators fit.  The MMAs
+// are not what sets this kernel's pace: the dequant warps and the weight
+// stream are (a 128 x 64 weight block takes ~350 clocks to arrive and
+// decode against ~320 clocks of MMAs at N = 160).
 // Keeping A out of shared memory leaves shared-memory bandwidth to the token
 // operand: per 64-K block the MMA reads N x 128 bytes of tokens that TMA wrote,
 // and nothing else but the 4.5 KB raw stage passes through it.
@@ -76,7 +79,7 @@ constexpr int GPS = RK / BK / KPG;  // A groups per raw stage
 constexpr int NG = 2;            // A groups in TMEM
 constexpr int NB = 3;            // token slots
 constexpr int NR = 4;            // raw stages
-constexpr int kSlotRows = 384;   // rows of 128 bytes per token slot (48 KB)
+constexpr int kSlotRows = 320;   // rows of 128 bytes per token slot (40 KB)
 constexpr uint32_t kACol0 = 2 * BN;            // first TMEM column of the A groups
 constexpr uint32_t kGroupCols = KPG * BK / 2;  // 64 columns: 2 fp16 per column
 constexpr int kThreads = 512;
@@ -87,7 +90,7 @@ static_assert(kACol0 + NG * kGroupCols <= 512, "TMEM columns");
 
 struct __align__(1024) SmemTC {
   uint8_t raw[NR][BM * 128];     // 4 x 16 KB
-  uint8_t b[NB][kSlotRows * 128];  // 3 x 48 KB
+  uint8_t b[NB][kSlotRows * 128];  // 3 x 40 KB
   float sc[NR][BM * (RK / 64)];  // 4 x 2 KB: the raw stage's gs64 scales, [row][4]
   uint64_t raw_full[NR], raw_empty[NR];
   uint64_t a_full[NG], a_empty[NG];
@@ -97,23 +100,24 @@ struct __align__(1024) SmemTC {
   int abort;
 };
 
-// Token boxes of 32, 64, 96 or 192 rows (the smallest that covers the tile's
-// operand rows); a 48 KB slot carries 8, 4, 4 or 2 K blocks of one box, so
-// small tiles keep as many K blocks in flight as large ones keep bytes (the
-// counts are powers of two: K / 64 is a multiple of 8).
-constexpr int kBoxRows[4] = {32, 64, 96, 192};
+// Token boxes of 32, 64, 96 or 160 rows (the smallest that covers the tile's
+// operand rows); a 40 KB slot carries 8, 4, 2 or 2 K blocks of one box, so
+// small tiles keep more K blocks in flight (the counts are powers of two: K / 64
+// is a multiple of 8).
+constexpr int kBoxRows[4] = {32, 64, 96, BN};
+static_assert(BN == 160, "the largest token box is one tile");
 __device__ __forceinline__ int box_index(int nvalid) {
   return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 96 ? 2 : 3;
 }
-__device__ __forceinline__ int box_rows(int bi) { return bi == 0 ? 32 : bi == 1 ? 64 : bi == 2 ? 96 : 192; }
-__device__ __forceinline__ int box_kps(int bi) { return bi == 0 ? 8 : bi <= 2 ? 4 : 2; }
+__device__ __forceinline__ int box_rows(int bi) { return bi == 0 ? 32 : bi == 1 ? 64 : bi == 2 ? 96 : BN; }
+__device__ __forceinline__ int box_kps(int bi) { return bi == 0 ? 8 : bi == 1 ? 4 : 2; }
 
 struct TcParams {
   CUtensorMap map_w;       // raw weights of the routed experts [E * rows][K/2] u8
   CUtensorMap map_ws;      // raw weights of the shared expert [rows_s][K/2] u8
   CUtensorMap map_sc;      // scales of the routed experts [E * rows][K/64] f32
   CUtensorMap map_scs;     // scales of the shared expert [rows_s][K/64] f32
-  CUtensorMap map_b[4];    // fp16 token operand [R][K], boxes of 32/64/96/192 rows
+  CUtensorMap map_b[4];    // fp16 token operand [R][K], boxes of 32/64/96/160 rows
   int mode;                // 0: W13 + SwiGLU, 1: W2 + routing weight
   int K;                   // reduction length (H for W13, I for W2)
   int K_s;                 // the shared expert's reduction length (H, or Is for W2)
@@ -478,11 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
             const int j = gi * KPG + jj;
             const uint32_t words[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
             const float sv = (j == 0 ? sc4.x : j == 1 ? sc4.y : j == 2 ? sc4.z : sc4.w) * re;
-            const __half shi = __float2half_rn(sv);
-            const __half slo = __float2half_rn(sv - __half2float(shi));
-            const uint32_t shi2 = f16x2_splat(shi), slo2 = f16x2_splat(slo);
+            const __half sh = __float2half_rn(sv);
+            const uint32_t s2 = f16x2_splat(sh);
+            const uint32_t s16_2 = f16x2_splat(__float2half_rn(__half2float(sh) * 0.0625f));
 #pragma unroll
-            for (int wv = 0; wv < 4; ++wv) dequant_word_f16(words[wv], shi2, slo2, o[jj] + 4 * wv);
+            for (int wv = 0; wv < 4; ++wv) dequant_word_f16(words[wv], s2, s16_2, o[jj] + 4 * wv);
           }
           static_assert(KPG == 2, "two K blocks per A group");
           tmem_st16x2(acol, o[0], acol + BK / 2, o[1]);   // includes the wait

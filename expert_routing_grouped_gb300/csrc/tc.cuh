@@ -195,31 +195,35 @@ static __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-static __device__ __forceinline__ uint32_t hfma2_f16(uint32_t a, uint32_t b, uint32_t c) {
+// (w & mask) | 0x64006400 with mask 0x000F000F: two offset-binary nibbles n in
+// bits 0-3 / 16-19 into fp16 1024 + n (the unit in the last place of 1024 is
+// 1); with mask 0x00F000F0 the nibbles in bits 4-7 / 20-23 become 1024 + 16 n.
+static __device__ __forceinline__ uint32_t lop_nib16_lo(uint32_t w) {
   uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-static __device__ __forceinline__ uint32_t lop_nib16(uint32_t w) {
-  uint32_t d;
-  // (w & 0x000F000F) | 0x64006400: two offset-binary nibbles n into fp16
-  // 1024 + n (the unit in the last place of 1024 is 1 in fp16).
   asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(d) : "r"(w));
   return d;
 }
+static __device__ __forceinline__ uint32_t lop_nib16_hi(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(d) : "r"(w));
+  return d;
+}
 
-// 8 weights of one library-layout word -> 4 fp16x2 words of fp16(q * s), with
-// s = s_hi + s_lo split into two fp16: q = (1024 + n) - 1032 is exact, q * s_hi
-// is exact inside the fused multiply-add, q * s_lo adds the part below fp16
-// resolution, and the sum is rounded once.
-static __device__ __forceinline__ void dequant_word_f16(uint32_t w, uint32_t s_hi2, uint32_t s_lo2,
+// 8 weights of one library-layout word -> 4 fp16x2 words of fp16(q * s), s
+// given as fp16 (s2) and as fp16 s / 16 (s16_2, exact).  The pairs in nibble
+// positions 0 and 2 decode as q = (1024 + n) - 1032, those in positions 1 and 3
+// in place as 16 q = (1024 + 16 n) - 1152 (both exact), so one shift serves
+// the word; 16 q * (s / 16) is the same product as q * s.  13 instructions
+// per 8 weights.
+static __device__ __forceinline__ void dequant_word_f16(uint32_t w, uint32_t s2, uint32_t s16_2,
                                                         uint32_t out[4]) {
   const uint32_t c1032 = 0x64086408u;   // fp16x2 (1032, 1032)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t q = hsub2_f16(lop_nib16(w >> (4 * i)), c1032);
-    out[i] = hfma2_f16(q, s_hi2, hmul2_f16(q, s_lo2));
-  }
+  const uint32_t c1152 = 0x64806480u;   // fp16x2 (1152, 1152)
+  const uint32_t w8 = w >> 8;
+  out[0] = hmul2_f16(hsub2_f16(lop_nib16_lo(w), c1032), s2);
+  out[1] = hmul2_f16(hsub2_f16(lop_nib16_hi(w), c1152), s16_2);
+  out[2] = hmul2_f16(hsub2_f16(lop_nib16_lo(w8), c1032), s2);
+  out[3] = hmul2_f16(hsub2_f16(lop_nib16_hi(w8), c1152), s16_2);
 }
 
 static __device__ __forceinline__ uint32_t f16x2_splat(__half v) {

@@ -274,9 +274,9 @@ def test_init_fault_injection_leaks_nothing(dev):
 # The tensor-core path's bar: relative L2 <= 5e-3 and the largest element
 # error <= 2e-2 of the reference's rms over the whole compared output.  The
 # same 2e-2 is also held per token against that token's own rms (stricter for
-# tokens whose outputs are small).  The fp16 operands give about 4e-4 relative
-# L2 and 2e-3 rms on these workloads (a CPU emulation of the kernel's
-# roundings), so both bars hold with a wide margin.
+# tokens whose outputs are small).  The fp16 operands give about 5e-4 relative
+# L2 and at most 3.2e-3 rms on these workloads (a CPU emulation of the
+# kernel's roundings), so both bars hold with a wide margin.
 TC_TOL = 5e-3
 TC_MAXABS = 2e-2
 
