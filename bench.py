@@ -347,7 +347,15 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
                     stage.setdefault(nm, []).append(ms)
     for lay in built:
         lay.set_option(moe.MOE_OPT_PROFILE, 0)
-    # capture the stack once, replay it for the timed steps
+    # The stack as captured without next-layer links (for the comparison
+    # below), then with them: each layer's W2 pass prefetches the next layer's
+    # router and shared expert into L2 (moe_set_next_layer).  The linked graph
+    # is the one timed.
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain):
+        step(torch.cuda.current_stream())
+    for a, b in zip(built[:-1], built[1:]):
+        a.set_next_layer(b)
     launches0 = sum(l.debug_view().launches for l in built)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -355,7 +363,16 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     per_replay = sum(l.debug_view().launches for l in built) - launches0 + n_layers
     for _ in range(warmup):
         g.replay()
+        g_plain.replay()
     torch.cuda.synchronize()
+    plain_ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g_plain.replay()
+        b.record()
+        torch.cuda.synchronize()
+        plain_ms.append(a.elapsed_time(b))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     cur = torch.cuda.current_stream()
@@ -386,8 +403,11 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     res = dict(wl=wl, T=T, step_ms=step_ms, layers=n_layers, regime=regime,
                stage={k: statistics.mean(v) for k, v in stage.items()},
                launches=per_replay * steps, n_active=n_active, clocks=clocks,
-               e2e_s=statistics.median(e2e), h2d=T * wl.H * 4, d2h=T * wl.H * 4)
-    del g
+               e2e_s=statistics.median(e2e), h2d=T * wl.H * 4, d2h=T * wl.H * 4,
+               no_prefetch_ms=statistics.median(plain_ms))
+    del g, g_plain
+    for lay in built:
+        lay.set_next_layer(None)
     for lay in built:
         lay.close()
     torch.cuda.empty_cache()
@@ -691,6 +711,10 @@ def make_line(pre, dec, world, reduce_max, pk, src, steps, warmup):
                           "hbm_gbs": byts * world / (dms * 1e-3) / 1e9,
                           "hbm_frac": byts / (dms * 1e-3) / 1e9 / pk["hbm_gbs"],
                           "stage_ms": {k: round(v, 4) for k, v in dec["stage"].items()},
+                          "without_next_layer_prefetch": {
+                              "ms_per_step": dec.get("no_prefetch_ms"),
+                              "note": "the same stack captured without moe_set_next_layer links, "
+                                      "median of the same number of replays"},
                           "e2e": {"value": dec["T"] * world / reduce_max(dec["e2e_s"]),
                                   "unit": "tokens/s", "h2d_bytes_per_step": dec["h2d"],
                                   "d2h_bytes_per_step": dec["d2h"]},

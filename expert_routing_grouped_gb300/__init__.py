@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 MOE_OK, MOE_ERR_NOMEM, MOE_ERR_ROUTING, MOE_ERR_DEVICE, MOE_ERR_ARG = 0, -1, -2, -3, -4
 MOE_ERR_IO, MOE_ERR_ENGINE = -5, -6
 MOE_OPT_REGIME, MOE_OPT_SMALL_T_MAX, MOE_OPT_PROFILE, MOE_OPT_USAGE, MOE_OPT_PDL = 1, 2, 3, 4, 5
+MOE_OPT_WAIT_LIMIT_US = 6
 REGIME_AUTO, REGIME_GEMV, REGIME_TC, REGIME_TC_EXACT = 0, 1, 2, 3
 ROUTER_SOFTMAX, ROUTER_SIGMOID, ROUTER_SOFTMAX_RAW = 0, 1, 2
 X_F32, X_BF16 = 0, 1
@@ -24,7 +25,7 @@ EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual", "moe_
            "moe_rmsnorm_bf16", "moe_set_option", "moe_debug_view", "moe_debug_read",
            "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror",
            "moe_route_noalloc", "moe_usage_read", "moe_usage_reset", "moe_engine_id",
-           "moe_route_trace_write", "moe_route_trace_read")
+           "moe_route_trace_write", "moe_route_trace_read", "moe_set_next_layer")
 
 
 class MoeLayout(ctypes.Structure):
@@ -75,6 +76,7 @@ def _load():
         "moe_route_noalloc": (i, [P, i, i, i, i, i, i, f, P, P, P, P, P]),
         "moe_usage_read": (i, [P, P, i]),
         "moe_usage_reset": (i, [P]),
+        "moe_set_next_layer": (i, [P, P]),
         "moe_engine_id": (ctypes.c_uint32, [ctypes.c_char_p]),
         "moe_route_trace_write": (i, [ctypes.c_char_p, i, i, ctypes.c_uint32, P]),
         "moe_route_trace_read": (i, [ctypes.c_char_p, i, i, ctypes.c_uint32, P, P]),
@@ -148,6 +150,13 @@ class MoELayer:
 
     def set_option(self, option, value):
         return _check(lib.moe_set_option(self._handle, option, value), "moe_set_option")
+
+    def set_next_layer(self, nxt):
+        """moe_set_next_layer: prefetch nxt's router and shared expert into L2
+        during this layer's forwards (None clears the link)."""
+        self._next = nxt
+        return _check(lib.moe_set_next_layer(self._handle, nxt.handle if nxt is not None else None),
+                      "moe_set_next_layer")
 
     def debug_view(self):
         d = MoeDebug()

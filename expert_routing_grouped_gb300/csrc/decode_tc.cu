@@ -106,6 +106,8 @@ struct DecParams {
   int H;
   const float *wperm;      // [R]
   int32_t *status;
+  L2Prefetch pf;           // W2: the next layer's router and shared expert
+  unsigned long long wait_ns;   // limit of each role wait (MOE_OPT_WAIT_LIMIT_US)
 };
 
 // The grid's flat SU range: routed experts (slot a < n_r) first, then the
@@ -273,8 +275,11 @@ __device__ void finish_rb(const DecParams &p, const Geo &q, int pp, const Cur &c
 
 // NT: tokens per expert handled (a power of two >= T); PL: operand planes per
 // token (1: bf16 x; 2: hi/lo planes of f32 x or of h).
-template <int NT, int PL>
+// kShortWaits: the instantiation launched when the caller set a wait limit
+// below the default (MOE_OPT_WAIT_LIMIT_US); the ordinary one never tests it.
+template <int NT, int PL, bool kShortWaits>
 __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant__ DecParams p) {
+  if (p.mode == 1) l2_prefetch_share(p.pf);   // init-time weights: no wait needed
   pdl_enter();
   constexpr int NC = NT * PL;                 // accumulator columns read back
   static_assert(NC <= 16, "16 MMA columns");
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
       // SU jp goes into the stage SU jp - NS used, once all decode warps released it.
       const int stage = (int)(jp % NS);
       if (jp >= (uint32_t)NS &&
-          !wait_bar(&sm->empty[stage], ((jp / NS) & 1) ^ 1, &sm->abort, p.status)) {
+          !wait_role<kShortWaits>(&sm->empty[stage], ((jp / NS) & 1) ^ 1, &sm->abort, p.status, p.wait_ns)) {
         fail = true;
         break;
       }
@@ -353,8 +358,8 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
     uint32_t j = 0;
     for (; j < n; ++j) {
       const int stage = (int)(j % NS);
-      if (!wait_bar(&sm->afull[pp][j & 1], (j >> 1) & 1, &sm->abort, p.status) ||
-          !wait_bar(&sm->full[stage], (j / NS) & 1, &sm->abort, p.status)) {
+      if (!wait_role<kShortWaits>(&sm->afull[pp][j & 1], (j >> 1) & 1, &sm->abort, p.status, p.wait_ns) ||
+          !wait_role<kShortWaits>(&sm->full[stage], (j / NS) & 1, &sm->abort, p.status, p.wait_ns)) {
         fail = true;
         break;
       }
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
         // that read that buffer two SUs ago are complete (the epilogue of SU
         // j - 2 waited for them).
         const int stage = (int)(j % NS);
-        bool go = wait_bar(&sm->full[stage], (j / NS) & 1, &sm->abort, p.status);
+        bool go = wait_role<kShortWaits>(&sm->full[stage], (j / NS) & 1, &sm->abort, p.status, p.wait_ns);
         go = __all_sync(0xffffffffu, go);     // tcgen05.st is warp-collective
         if (!go) {
           fail = true;
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(DT, 1) decode_tc_kernel(const __grid_constant_
         // Epilogue of SU j - 1.
         const uint32_t jm = j - 1;
         const int stage = (int)(jm % NS);
-        bool ok = wait_bar(&sm->done[pp][jm & 1], (jm >> 1) & 1, &sm->abort, p.status);
+        bool ok = wait_role<kShortWaits>(&sm->done[pp][jm & 1], (jm >> 1) & 1, &sm->abort, p.status, p.wait_ns);
         ok = __all_sync(0xffffffffu, ok);     // tcgen05.ld is warp-collective
         if (!ok) {
           fail = true;
@@ -477,13 +482,18 @@ cudaError_t launch_pass(const DecParams &p, int T, int grid, bool pdl, cudaStrea
   do {                                                                                       \
     static bool attr = false;                                                                \
     if (!attr) {                                                                             \
-      cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NT, PL>,                         \
+      cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NT, PL, false>,                  \
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,      \
                                            (int)kDecSmem);                                   \
+      if (e == cudaSuccess)                                                                  \
+        e = cudaFuncSetAttribute(decode_tc_kernel<NT, PL, true>,                             \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmem); \
       if (e != cudaSuccess) return e;                                                        \
       attr = true;                                                                           \
     }                                                                                        \
-    err = launch_k(pdl, decode_tc_kernel<NT, PL>, dim3(grid), dim3(DT), kDecSmem, st, p);     \
+    err = launch_k(pdl, p.wait_ns < kWaitNs ? decode_tc_kernel<NT, PL, true>                  \
+                                            : decode_tc_kernel<NT, PL, false>,               \
+                   dim3(grid), dim3(DT), kDecSmem, st, p);                                   \
   } while (0)
   if (T <= 1) MOE_DEC(1);
   else if (T <= 2) MOE_DEC(2);
@@ -530,6 +540,7 @@ cudaError_t launch_decode_tc(const moe_handle *h, const void *x, int T, float *o
   p.H = H;
   p.wperm = w.wperm;
   p.status = w.status;
+  p.wait_ns = h->wait_ns;
   // ---- W13 over the x planes
   bool ok = make_map(&p.map_w, h->ex.w13q, U8, 1, H / 2, (uint64_t)E * 2 * I, H / 2, 128, 128);
   ok = ok && make_map(&p.map_ws, S ? h->sh.w13q : h->ex.w13q, U8, 1, H / 2,
@@ -572,6 +583,7 @@ cudaError_t launch_decode_tc(const moe_handle *h, const void *x, int T, float *o
   p.K_s = Is;
   p.ticket = w.dec_ticket + h->dec_rb_max;
   p.ticket_other = w.dec_ticket;
+  p.pf = next_layer_prefetch(h);
   err = launch_pass<2>(p, T, h->num_sms, h->pdl, st);
   if (err != cudaSuccess) return err;
   hm->launches += 1;

@@ -1,5 +1,5 @@
 // gemv.cu -- steps 4-5 of the layer for small T (decode and MTP-verify
-// batches): int4 gs64 dequant GEMV, f32 throughout.
+// batches): int4 gs64 dequant GEMV with exact products and f32 accumulation.
 //
 // At small T the layer is bound by streaming the activated experts' packed
 // weights from HBM (the pages' expert tier moves ~19 MB per expert: colibrì
@@ -14,16 +14,20 @@
 //         token's rows in slot order, then the shared expert (tutorial §3.3
 //         Step 5), one owner per output element, no atomics.
 //
-// One kernel serves both matrices.  An item is 32 consecutive weight rows of
-// one active expert (W13: 16 features' W1 and W3 rows, interleaved; W2: 32
-// output rows); each of the 8 warps streams 4 of those rows over the full K
-// with 128-bit non-allocating loads (a lane's 16 bytes = 32 weights inside one
-// 64-wide scale group).  The expert's activation rows sit in shared memory as
-// f32 (staged when the expert changes, XOR-swizzled against bank conflicts)
-// and are reused across the 4 rows.
-// Dequant and FMAs use packed f32x2 arithmetic.  CTAs take contiguous item
-// ranges, so one activation stage serves many items.
+// An item is 32 consecutive weight rows of one active expert (W13: 16
+// features' W1 and W3 rows, interleaved; W2: 32 output rows); each of the 8
+// warps streams 4 of those rows over the full K with 128-bit non-allocating
+// loads (a lane's 16 bytes = 32 weights inside one 64-wide scale group).  The
+// expert's activation rows sit in shared memory (staged when the expert
+// changes, XOR-swizzled against bank conflicts) and are reused across the 4
+// rows.  CTAs take contiguous item ranges, so one activation stage serves
+// many items.
+// Two kernels: the bf16-pair kernel (W13 on bf16 x, and W2 on h, which W13
+// leaves as two exact bf16 planes) multiplies bf16 codes by bf16 activations
+// with fma.rn.f32.bf16; W13 on f32 x decodes the codes to f32 and uses packed
+// f32x2 arithmetic.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -33,11 +37,14 @@ constexpr int kWarps = 8;
 constexpr int kRowsPerWarp = kRowsPerItem / kWarps;   // 4
 constexpr int kActSmemBytes = 96 * 1024;
 
-__device__ __forceinline__ uint4 ld_stream(const void *p) {
+// Weights are read once per call: no L1 allocation, and an evict-first L2
+// policy (pol) so that they do not push out what is worth keeping there (the
+// workspace, and the next layer's router and shared expert when prefetched).
+__device__ __forceinline__ uint4 ld_stream(const void *p, uint64_t pol) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return r;
 }
 
@@ -61,6 +68,15 @@ __device__ __forceinline__ void dequant8(uint32_t w, float2 q[4]) {
   q[3] = __fadd2_rn(make_float2(__uint_as_float((w & 0x0000F000u) | 0x45000000u),
                                 __uint_as_float((v & 0x000F0000u) | 0x43000000u)),
                     make_float2(-2056.0f, -136.0f));
+}
+
+// h as two exact bf16 planes: row p's hi plane at planes + 2p * stride, its lo
+// plane at (2p + 1) * stride.
+__device__ __forceinline__ void store_h_planes(__nv_bfloat16 *planes, int stride, int p, int f,
+                                               float h) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+  planes[(size_t)(2 * p) * stride + f] = hi;
+  planes[(size_t)(2 * p + 1) * stride + f] = __float2bfloat16_rn(h - __bfloat162float(hi));
 }
 
 // One item: 32 consecutive weight rows (group g) of one active expert e.
@@ -97,40 +113,40 @@ __device__ __forceinline__ Item item_at(int item, int n_routed, int items_r, int
 
 // The weights and scales of chunk c of an item's four rows for this warp.
 __device__ __forceinline__ void load_chunk(const Item &it, const int rr[kRowsPerWarp], int c,
-                                           uint4 wv[kRowsPerWarp], float sc[kRowsPerWarp]) {
+                                           uint4 wv[kRowsPerWarp], float sc[kRowsPerWarp],
+                                           uint64_t pol) {
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
     const size_t row = (size_t)it.g * kRowsPerItem + rr[i];
-    wv[i] = ld_stream(it.wq + row * (it.K / 2) + (size_t)c * 16);
+    wv[i] = ld_stream(it.wq + row * (it.K / 2) + (size_t)c * 16, pol);
     sc[i] = __ldg(it.ws + row * (it.K / 64) + (c >> 1));
   }
 }
 
-// mode 0: W13 + SwiGLU -> out = h;  mode 1: W2 times routing weight -> out = y.
+// W13 + SwiGLU for f32 activations (x of an f32-input layer): h is written as
+// the exact bf16 planes hi = bf16(h), lo = bf16(h - hi) that W2 reads.
 // Each lane keeps the next chunk's weights in flight while it works on the
 // current one; the last chunk of an item prefetches the first chunk of the
-// next item (when the item has one token batch), so short rows (W2) do not pay
-// a memory round trip per item.
+// next item (when the item has one token batch).
 template <int NT>
 __global__ void __launch_bounds__(256) gemv_kernel(
-    int mode, const void *__restrict__ act, int act_is_bf16, int act_stride, int T, int k, int E,
+    const void *__restrict__ act, int act_is_bf16, int act_stride, int T, int k, int E,
     int K_r, int K_s, int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
     const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
     const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
-    const float *__restrict__ wts, float *__restrict__ out, int out_stride) {
+    __nv_bfloat16 *__restrict__ out_h, int out_stride) {
   pdl_enter();
   act = after_wait(act);
   active = after_wait(active);
   n_active_p = after_wait(n_active_p);
   offsets = after_wait(offsets);
   perm = after_wait(perm);
-  wts = after_wait(wts);
-  out = after_wait(out);
+  out_h = after_wait(out_h);
   extern __shared__ float act_s[];   // [NT][K] activations of the current expert pass
-  __shared__ float wt_s[NT];         // W2: routing weights of the staged tokens
   const int n_active = *n_active_p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t pol = l2_evict_first_policy();
   const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
   const int n_routed = n_active - has_shared;
   const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
@@ -141,18 +157,9 @@ __global__ void __launch_bounds__(256) gemv_kernel(
   int staged_e = -1, staged_b = -1;
   const int sw = lane & 7;             // swizzle of every chunk this lane reads
 
-  // Rows of this warp inside an item: W13 -> W1 of features 2w, 2w+1 and W3 of
-  // the same (rows 2w, 2w+1, 16+2w, 17+2w of the 32-row group); W2 -> 4w..4w+3.
-  int rr[kRowsPerWarp];
-  if (mode == 0) {
-    rr[0] = 2 * warp;
-    rr[1] = 2 * warp + 1;
-    rr[2] = 16 + 2 * warp;
-    rr[3] = 17 + 2 * warp;
-  } else {
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) rr[i] = kRowsPerWarp * warp + i;
-  }
+  // Rows of this warp inside an item: W1 of features 2w, 2w+1 and W3 of the
+  // same (rows 2w, 2w+1, 16+2w, 17+2w of the 32-row group).
+  const int rr[kRowsPerWarp] = {2 * warp, 2 * warp + 1, 16 + 2 * warp, 17 + 2 * warp};
 
   bool pre = false;                    // wv/sc already hold this item's first chunk
   uint4 wv[kRowsPerWarp];
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
     for (int b0 = 0; b0 < cnt; b0 += NT) {
       const int nb = min(NT, cnt - b0);
       if (!pre || b0 > 0) {
-        if (lane < chunks) load_chunk(it, rr, lane, wv, sc);
+        if (lane < chunks) load_chunk(it, rr, lane, wv, sc, pol);
       }
       pre = false;
       if (e != staged_e || b0 != staged_b) {
@@ -175,8 +182,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
           if (tkn < nb) {
             const int p = p0 + b0 + tkn;
-            // W13 reads the token's x row; W2 reads the grouped position's h row.
-            const int src = (mode == 0) ? ((e < E) ? perm[p] / k : p - A) : p;
+            const int src = (e < E) ? perm[p] / k : p - A;   // the token's x row
             if (act_is_bf16) {
               const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(
                                         reinterpret_cast<const __nv_bfloat16 *>(act) +
@@ -195,9 +201,6 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           const int cc = c4 >> 3, jj = c4 & 7;
           reinterpret_cast<float4 *>(act_s + (size_t)tkn * K)[cc * 8 + (jj ^ (cc & 7))] = v;
         }
-        if (mode == 1 && threadIdx.x < NT)
-          wt_s[threadIdx.x] =
-              (threadIdx.x < nb && e < E) ? wts[perm[p0 + b0 + threadIdx.x]] : 1.0f;
         __syncthreads();
         staged_e = e;
         staged_b = b0;
@@ -217,12 +220,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(
           sn[i] = 0.f;
         }
         if (cn < chunks) {
-          load_chunk(it, rr, cn, wn, sn);
+          load_chunk(it, rr, cn, wn, sn, pol);
         } else if (b0 + NT >= cnt && item + 1 < i1) {
           const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r,
                                   ws_r, wq_s, ws_s, active, offsets);
           if (lane < nx.K / 32) {
-            load_chunk(nx, rr, lane, wn, sn);
+            load_chunk(nx, rr, lane, wn, sn, pol);
             pre = true;
           }
         }
@@ -273,20 +276,13 @@ __global__ void __launch_bounds__(256) gemv_kernel(
         for (int t = 0; t < NT; ++t) {
           if (t < nb) {
             const int p = p0 + b0 + t;
-            if (mode == 0) {
-              // 32-row group g = 128-row block g/4, quadrant g%4: features
-              // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
-              const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
+            // 32-row group g = 128-row block g/4, quadrant g%4: features
+            // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
+            const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
 #pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const float gg = acc[j][t], uu = acc[2 + j][t];
-                out[(size_t)p * out_stride + f0 + j] = gg / (1.0f + expf(-gg)) * uu;
-              }
-            } else {
-              const float wt = wt_s[t];
-#pragma unroll
-              for (int i = 0; i < kRowsPerWarp; ++i)
-                out[(size_t)p * out_stride + g * kRowsPerItem + rr[i]] = wt * acc[i][t];
+            for (int j = 0; j < 2; ++j) {
+              const float gg = acc[j][t], uu = acc[2 + j][t];
+              store_h_planes(out_h, out_stride, p, f0 + j, gg / (1.0f + expf(-gg)) * uu);
             }
           }
         }
@@ -296,14 +292,21 @@ __global__ void __launch_bounds__(256) gemv_kernel(
 }
 
 // ----------------------------------------------------------------------------
-// W13 with bf16 activations.  A pair of int4 codes becomes a bf16 pair
-// (136 + q_even, 136 + q_odd) in one lop3; fma.rn.f32.bf16 multiplies it by the
-// bf16 activations exactly and accumulates in f32.  136 times the chunk's
-// activation sum (f32, computed once per token when the expert's activations
-// are staged) is taken off per 32-weight chunk, before the gs64 scale:
-//   W1[n] . x = sum_chunks s_chunk * (sum_i (136 + q_i) x_i - 136 * sum_i x_i).
+// The bf16-pair GEMV.  A pair of int4 codes becomes a bf16 pair (136 + q_even,
+// 136 + q_odd) in one lop3; fma.rn.f32.bf16 multiplies it by bf16 activations
+// exactly and accumulates in f32.  136 times the chunk's activation sum (f32,
+// computed once per token when the expert's activations are staged) is taken
+// off per 32-weight chunk, before the gs64 scale:
+//   W[n] . a = sum_chunks s_chunk * (sum_i (136 + q_i) a_i - 136 * sum_i a_i).
+// The activations come in PL bf16 planes whose sum is the operand: W13 reads
+// x itself (one plane; bf16 x is exact), W2 reads h as the exact split
+// h = hi + lo, hi = bf16(h), lo = bf16(h - hi) (16 significant bits, about
+// 8e-6 relative), which the W13 epilogue writes.
+//   MODE 0 (W13): rows 2w, 2w+1, 16+2w, 17+2w of a 32-row group are W1 / W3
+//                 of features 2w, 2w+1; h = silu(g) * u, written as planes.
+//   MODE 1 (W2):  rows 4w..4w+3; y[p][o] = routing weight * (W2[o] . h[p]).
 // Each lane prefetches the next chunk's weights and scales before it uses the
-// current ones.
+// current ones (at an item's last chunk, the next item's first).
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w) {
   uint32_t d;
   // (w & 0x000F000F) | 0x43004300: two offset-binary nibbles into bf16 128 + n.
@@ -321,78 +324,133 @@ __device__ __forceinline__ void mfma_pair(float &acc0, float &acc1, uint32_t q2,
       : "r"(q2), "r"(x2));
 }
 
-template <int NT>
-__global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
-    const __nv_bfloat16 *__restrict__ act, int act_stride, int T, int k, int E, int K,
+template <int NT, int PL, int MODE>
+__global__ void __launch_bounds__(256) gemv_bf16_kernel(
+    const __nv_bfloat16 *__restrict__ act, int act_stride, int T, int k, int E, int K_r, int K_s,
     int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
     const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
     const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
-    float *__restrict__ out, int out_stride) {
-  pdl_enter();
-  act = after_wait(act);
-  active = after_wait(active);
-  n_active_p = after_wait(n_active_p);
-  offsets = after_wait(offsets);
-  perm = after_wait(perm);
-  out = after_wait(out);
+    const float *__restrict__ wts, float *__restrict__ out_y, __nv_bfloat16 *__restrict__ out_h,
+    int out_stride, const __grid_constant__ L2Prefetch pf) {
+  static_assert(PL == 1 || PL == 2, "one or two activation planes");
+  if (MODE == 1) l2_prefetch_share(pf);   // init-time weights: no wait needed
+  // W13 runs the shared expert's items before it waits for the routing kernel
+  // it is chained to: they need only x, which was complete before that kernel
+  // (the first of the call, launched plainly) started, and they write only the
+  // shared expert's rows of h, which nothing reads before W2.  So the shared
+  // expert's weights stream while the routing kernel runs; the routed items
+  // follow the wait.  W2 waits first.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint4 smem_v[];
-  // [NT][K/8] 16-byte groups of bf16 activations: group j of 32-wide chunk c at
-  // slot j ^ ((c >> 1) & 3), so 8 lanes reading the same j of chunks c..c+7
-  // hit 8 different 16-byte bank groups; then [NT][K/32] f32 chunk sums.
+  // [PL][NT][K/8] 16-byte groups of bf16 activations: group j of 32-wide chunk
+  // c at slot j ^ ((c >> 1) & 3), so 8 lanes reading the same j of chunks
+  // c..c+7 hit 8 different 16-byte bank groups; then [NT][K/32] f32 chunk sums
+  // over the planes.  K is the larger of the routed and shared lengths.
+  const int Kmax = K_r > K_s ? K_r : K_s;
   uint4 *xs = smem_v;
-  float *xsum = reinterpret_cast<float *>(smem_v + (size_t)NT * (K / 8));
-  const int n_active = *n_active_p;
+  float *xsum = reinterpret_cast<float *>(smem_v + (size_t)PL * NT * (Kmax / 8));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
-  const int n_routed = n_active - has_shared;
+  const uint64_t pol = l2_evict_first_policy();
   const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
-  const int items = n_routed * items_r + has_shared * items_s;
   const int A = T * k;
-  const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
-  const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
-  const int chunks = K / 32;
+  const bool early = MODE == 0 && items_s > 0;
   int staged_e = -1, staged_b = -1;
-  const int rr[kRowsPerWarp] = {2 * warp, 2 * warp + 1, 16 + 2 * warp, 17 + 2 * warp};
+  int rr[kRowsPerWarp];
+  if (MODE == 0) {
+    rr[0] = 2 * warp;
+    rr[1] = 2 * warp + 1;
+    rr[2] = 16 + 2 * warp;
+    rr[3] = 17 + 2 * warp;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) rr[i] = kRowsPerWarp * warp + i;
+  }
 
   bool pre = false;                    // wv/sc already hold this item's first chunk
   uint4 wv[kRowsPerWarp];
   float sc[kRowsPerWarp];
+  // The work is dealt as contiguous ranges of [routed items, shared items].
+  // Before the wait the routed count is not known; the deal assumes the
+  // usual one, min(E, T k) distinct experts, so phase 0 takes this CTA's
+  // share of the shared items from that deal and phase 1 its routed share.
+  // When the routing turns out otherwise (repeated experts, a top-p trim)
+  // phase 1 deals the routed items evenly instead.
+  const long long r_guess = (long long)min(E, T * k) * items_r;
+  const long long n_guess = r_guess + items_s;
+  const long long g_lo = n_guess * blockIdx.x / gridDim.x;
+  const long long g_hi = n_guess * (blockIdx.x + 1) / gridDim.x;
+  for (int phase = early ? 0 : 1; phase < 2; ++phase) {
+  // Phase 0: the shared expert's items (item_at with no routed experts maps
+  // item i to the shared expert's 32-row group i).  Phase 1: after the wait,
+  // the routed items (and, in W2, the shared expert's after them).
+  int n_routed = 0, items = items_s;
+  int i0 = (int)(max(g_lo, r_guess) - r_guess), i1 = (int)(max(g_hi, r_guess) - r_guess);
+  if (phase == 1) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    act = after_wait(act);
+    active = after_wait(active);
+    n_active_p = after_wait(n_active_p);
+    offsets = after_wait(offsets);
+    perm = after_wait(perm);
+    wts = after_wait(wts);
+    out_y = after_wait(out_y);
+    out_h = after_wait(out_h);
+    const int n_active = *n_active_p;
+    const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
+    n_routed = n_active - has_shared;
+    items = n_routed * items_r + (early ? 0 : has_shared * items_s);
+    if (early && items == r_guess) {
+      i0 = (int)min(g_lo, r_guess);
+      i1 = (int)min(g_hi, r_guess);
+    } else {
+      i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+      i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+    }
+  }
+  pre = false;
   for (int item = i0; item < i1; ++item) {
-    const Item it = item_at(item, n_routed, items_r, E, A, T, K, K, rows_r, wq_r, ws_r, wq_s,
+    const Item it = item_at(item, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r, ws_r, wq_s,
                             ws_s, active, offsets);
-    const int e = it.e, g = it.g, p0 = it.p0, cnt = it.cnt;
+    const int e = it.e, g = it.g, p0 = it.p0, cnt = it.cnt, K = it.K;
+    const int chunks = K / 32;
     for (int b0 = 0; b0 < cnt; b0 += NT) {
       const int nb = min(NT, cnt - b0);
       if (!pre || b0 > 0) {
-        if (lane < chunks) load_chunk(it, rr, lane, wv, sc);
+        if (lane < chunks) load_chunk(it, rr, lane, wv, sc, pol);
       }
       pre = false;
       if (e != staged_e || b0 != staged_b) {
         __syncthreads();   // previous readers are done
-        // One thread per (token, chunk): 64 bytes in, swizzled out, chunk sum.
+        // One thread per (token, chunk): 64 bytes per plane in, swizzled out,
+        // the chunk sum over the planes.
         for (int i = threadIdx.x; i < NT * chunks; i += blockDim.x) {
           const int tkn = i / chunks, c = i - tkn * chunks;
-          uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                        make_uint4(0, 0, 0, 0)};
           float sum = 0.f;
-          if (tkn < nb) {
-            const int p = p0 + b0 + tkn;
-            const int src = (e < E) ? perm[p] / k : p - A;
-            const uint4 *row = reinterpret_cast<const uint4 *>(act + (size_t)src * act_stride) + c * 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __ldcg(row + j);
+          for (int pl = 0; pl < PL; ++pl) {
+            uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                          make_uint4(0, 0, 0, 0)};
+            if (tkn < nb) {
+              const int p = p0 + b0 + tkn;
+              // W13 reads the token's x row; W2 reads the grouped position's planes.
+              const size_t row = MODE == 0 ? (size_t)((e < E) ? perm[p] / k : p - A)
+                                           : (size_t)(2 * p + pl);
+              const uint4 *src = reinterpret_cast<const uint4 *>(act + row * act_stride) + c * 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+              for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + j);
 #pragma unroll
-              for (int m = 0; m < 4; ++m)
-                sum += __uint_as_float(u[m] << 16) + __uint_as_float(u[m] & 0xFFFF0000u);
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                  sum += __uint_as_float(u[m] << 16) + __uint_as_float(u[m] & 0xFFFF0000u);
+              }
             }
-          }
-          uint4 *dst = xs + (size_t)tkn * (K / 8) + c * 4;
+            uint4 *dst = xs + ((size_t)pl * NT + tkn) * (K / 8) + c * 4;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j ^ ((c >> 1) & 3)] = v[j];
+            for (int j = 0; j < 4; ++j) dst[j ^ ((c >> 1) & 3)] = v[j];
+          }
           xsum[tkn * chunks + c] = sum;
         }
         __syncthreads();
@@ -415,28 +473,33 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
         }
         const int cn = c + 32;
         if (cn < chunks) {
-          load_chunk(it, rr, cn, wn, sn);
+          load_chunk(it, rr, cn, wn, sn, pol);
         } else if (b0 + NT >= cnt && item + 1 < i1) {
-          const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K, K, rows_r, wq_r, ws_r,
-                                  wq_s, ws_s, active, offsets);
-          load_chunk(nx, rr, lane, wn, sn);
-          pre = true;
+          const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r,
+                                  ws_r, wq_s, ws_s, active, offsets);
+          if (lane < nx.K / 32) {
+            load_chunk(nx, rr, lane, wn, sn, pol);
+            pre = true;
+          }
         }
-        uint32_t xw[NT][16];
+        uint32_t xw[PL][NT][16];
         float xc[NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const uint4 *src = xs + (size_t)t * (K / 8) + c * 4;
+        for (int pl = 0; pl < PL; ++pl)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 u = src[j ^ ((c >> 1) & 3)];
-            xw[t][4 * j] = u.x;
-            xw[t][4 * j + 1] = u.y;
-            xw[t][4 * j + 2] = u.z;
-            xw[t][4 * j + 3] = u.w;
+          for (int t = 0; t < NT; ++t) {
+            const uint4 *src = xs + ((size_t)pl * NT + t) * (K / 8) + c * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 u = src[j ^ ((c >> 1) & 3)];
+              xw[pl][t][4 * j] = u.x;
+              xw[pl][t][4 * j + 1] = u.y;
+              xw[pl][t][4 * j + 2] = u.z;
+              xw[pl][t][4 * j + 3] = u.w;
+            }
           }
-          xc[t] = 136.0f * xsum[t * chunks + c];
-        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) xc[t] = 136.0f * xsum[t * chunks + c];
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
           const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
@@ -449,7 +512,9 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
             for (int pp = 0; pp < 4; ++pp) {
               const uint32_t q2 = nib_pair_bf16(words[wi] >> (4 * pp));
 #pragma unroll
-              for (int t = 0; t < NT; ++t) mfma_pair(pe[t], po[t], q2, xw[t][4 * wi + pp]);
+              for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int pl = 0; pl < PL; ++pl) mfma_pair(pe[t], po[t], q2, xw[pl][t][4 * wi + pp]);
             }
           }
 #pragma unroll
@@ -468,55 +533,65 @@ __global__ void __launch_bounds__(256) gemv_w13_bf16_kernel(
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) acc[i][t] += __shfl_xor_sync(0xffffffffu, acc[i][t], o);
       if (lane == 0) {
-        // 32-row group g = 128-row block g/4, quadrant g%4: features
-        // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
-        const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (t < nb) {
             const int p = p0 + b0 + t;
+            if (MODE == 0) {
+              // 32-row group g = 128-row block g/4, quadrant g%4: features
+              // 64 (g/4) + 16 (g%4) + 2w + {0, 1}
+              const int f0 = (g >> 2) * 64 + (g & 3) * 16 + 2 * warp;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const float gg = acc[j][t], uu = acc[2 + j][t];
-              out[(size_t)p * out_stride + f0 + j] = gg / (1.0f + expf(-gg)) * uu;
+              for (int j = 0; j < 2; ++j) {
+                const float gg = acc[j][t], uu = acc[2 + j][t];
+                store_h_planes(out_h, out_stride, p, f0 + j, gg / (1.0f + expf(-gg)) * uu);
+              }
+            } else {
+              const float wt = (e < E) ? __ldcg(wts + __ldcg(perm + p)) : 1.0f;
+#pragma unroll
+              for (int i = 0; i < kRowsPerWarp; ++i)
+                out_y[(size_t)p * out_stride + g * kRowsPerItem + rr[i]] = wt * acc[i][t];
             }
           }
         }
       }
     }
   }
+  }   // phase
 }
 
-template <int NT>
-cudaError_t launch_w13_bf16(const moe_handle *h, const __nv_bfloat16 *x, int T, cudaStream_t st) {
-  const int K = h->H;
-  const size_t smem = (size_t)NT * (K / 8) * 16 + (size_t)NT * (K / 32) * 4;
+template <int NT, int PL, int MODE>
+cudaError_t launch_bf16(const moe_handle *h, const __nv_bfloat16 *act, int act_stride, int T,
+                        int K_r, int K_s, int rows_r, int rows_s, const uint8_t *wq_r,
+                        const float *ws_r, const uint8_t *wq_s, const float *ws_s, float *out_y,
+                        __nv_bfloat16 *out_h, int out_stride, cudaStream_t st) {
+  const int Kmax = K_r > K_s ? K_r : K_s;
+  const size_t smem = (size_t)PL * NT * (Kmax / 8) * 16 + (size_t)NT * (Kmax / 32) * 4;
   static bool attr = false;
   if (!attr) {
-    cudaError_t err = cudaFuncSetAttribute(gemv_w13_bf16_kernel<NT>,
+    cudaError_t err = cudaFuncSetAttribute(gemv_bf16_kernel<NT, PL, MODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kActSmemBytes);
     if (err != cudaSuccess) return err;
     attr = true;
   }
   int per_sm = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w13_bf16_kernel<NT>, kWarps * 32,
-                                                    smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_bf16_kernel<NT, PL, MODE>,
+                                                    kWarps * 32, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int h_stride = h->I > h->Is ? h->I : h->Is;
-  return launch_k(h->pdl, gemv_w13_bf16_kernel<NT>, dim3(h->num_sms * per_sm), dim3(kWarps * 32),
-                  smem, st, x, h->H, T, h->k, h->E, K, 2 * h->I, h->S ? 2 * h->Is : 0,
-                  h->ex.w13q, h->ex.w13s, h->sh.w13q, h->sh.w13s, h->ws.active, h->ws.n_active,
-                  h->ws.offsets, h->ws.perm, h->ws.h, h_stride);
+  return launch_k(h->pdl, gemv_bf16_kernel<NT, PL, MODE>, dim3(h->num_sms * per_sm),
+                  dim3(kWarps * 32), smem, st, act, act_stride, T, h->k, h->E, K_r, K_s, rows_r,
+                  rows_s, wq_r, ws_r, wq_s, ws_s, h->ws.active, h->ws.n_active, h->ws.offsets,
+                  h->ws.perm, h->ws.w, out_y, out_h, out_stride,
+                  MODE == 1 ? next_layer_prefetch(h) : L2Prefetch{});
 }
 
 template <int NT>
-cudaError_t launch_nt(int mode, const moe_handle *h, const void *act, int act_bf16, int act_stride,
-                      int T, int K, int K_s, int rows_r, int rows_s, const uint8_t *wq_r, const float *ws_r,
-                      const uint8_t *wq_s, const float *ws_s, float *out, int out_stride,
+cudaError_t launch_nt(const moe_handle *h, const void *act, int act_bf16, int T,
                       cudaStream_t st) {
-  const size_t smem = (size_t)NT * (K > K_s ? K : K_s) * sizeof(float);
+  const int K = h->H;
+  const size_t smem = (size_t)NT * K * sizeof(float);
   static bool attr = false;
   if (!attr) {
     cudaError_t err = cudaFuncSetAttribute(
@@ -531,49 +606,50 @@ cudaError_t launch_nt(int mode, const moe_handle *h, const void *act, int act_bf
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int blocks = h->num_sms * per_sm;
-  return launch_k(h->pdl, gemv_kernel<NT>, dim3(blocks), dim3(kWarps * 32), smem, st, mode, act,
-                  act_bf16, act_stride, T, h->k, h->E, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
-                  ws_s, h->ws.active, h->ws.n_active, h->ws.offsets, h->ws.perm, h->ws.w, out,
-                  out_stride);
-}
-
-// Tokens per pass: up to 4, as many as fit 96 KB of f32 activations.
-cudaError_t launch_gemv(int mode, const moe_handle *h, const void *act, int act_bf16,
-                        int act_stride, int T, int K, int K_s, int rows_r, int rows_s, const uint8_t *wq_r,
-                        const float *ws_r, const uint8_t *wq_s, const float *ws_s, float *out,
-                        int out_stride, cudaStream_t st) {
-  const int fit = kActSmemBytes / ((K > K_s ? K : K_s) * 4);
-  if (fit >= 4 && T >= 3)
-    return launch_nt<4>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
-                        ws_s, out, out_stride, st);
-  if (fit >= 2 && T >= 2)
-    return launch_nt<2>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
-                        ws_s, out, out_stride, st);
-  return launch_nt<1>(mode, h, act, act_bf16, act_stride, T, K, K_s, rows_r, rows_s, wq_r, ws_r, wq_s,
-                      ws_s, out, out_stride, st);
+  const int h_stride = h->I > h->Is ? h->I : h->Is;
+  return launch_k(h->pdl, gemv_kernel<NT>, dim3(h->num_sms * per_sm), dim3(kWarps * 32), smem, st,
+                  act, act_bf16, h->H, T, h->k, h->E, K, K, 2 * h->I, h->S ? 2 * h->Is : 0,
+                  h->ex.w13q, h->ex.w13s, h->sh.w13q, h->sh.w13s, h->ws.active, h->ws.n_active,
+                  h->ws.offsets, h->ws.perm, h->ws.hpl, h_stride);
 }
 
 }  // namespace
 
+// Shared memory of the bf16-pair kernel: PL planes of NT tokens' activations
+// and their chunk sums.
+static size_t bf16_smem(int NT, int PL, int K) {
+  return (size_t)PL * NT * (K / 8) * 16 + (size_t)NT * (K / 32) * 4;
+}
+
 cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStream_t st) {
-  if (h->L.x_dtype == 1 && (size_t)4 * (h->H / 8) * 16 + (size_t)4 * (h->H / 32) * 4 <= (size_t)kActSmemBytes) {
+  const int H = h->H, h_stride = h->I > h->Is ? h->I : h->Is;
+  if (h->L.x_dtype == 1 && bf16_smem(4, 1, H) <= (size_t)kActSmemBytes) {
     const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
-    if (T >= 3) return launch_w13_bf16<4>(h, xb, T, st);
-    if (T == 2) return launch_w13_bf16<2>(h, xb, T, st);
-    return launch_w13_bf16<1>(h, xb, T, st);
+#define MOE_W13(NT)                                                                             \
+  return launch_bf16<NT, 1, 0>(h, xb, H, T, H, H, 2 * h->I, h->S ? 2 * h->Is : 0, h->ex.w13q,   \
+                               h->ex.w13s, h->sh.w13q, h->sh.w13s, nullptr, h->ws.hpl, h_stride, \
+                               st)
+    if (T >= 3) MOE_W13(4);
+    if (T == 2) MOE_W13(2);
+    MOE_W13(1);
+#undef MOE_W13
   }
-  const int h_stride = h->I > h->Is ? h->I : h->Is;
-  return launch_gemv(0, h, x, h->L.x_dtype == 1, h->H, T, h->H, h->H, 2 * h->I,
-                     h->S ? 2 * h->Is : 0,
-                     h->ex.w13q, h->ex.w13s, h->sh.w13q, h->sh.w13s, h->ws.h, h_stride, st);
+  // f32 activations: tokens per pass up to 4, as many as fit 96 KB.
+  const int fit = kActSmemBytes / (H * 4);
+  if (fit >= 4 && T >= 3) return launch_nt<4>(h, x, h->L.x_dtype == 1, T, st);
+  if (fit >= 2 && T >= 2) return launch_nt<2>(h, x, h->L.x_dtype == 1, T, st);
+  return launch_nt<1>(h, x, h->L.x_dtype == 1, T, st);
 }
 
 cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  return launch_gemv(1, h, h->ws.h, 0, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,
-                     h->S ? h->H : 0, h->ex.w2q,
-                     h->ex.w2s, h->sh.w2q, h->sh.w2s, h->ws.y, h->H, st);
+#define MOE_W2(NT)                                                                             \
+  return launch_bf16<NT, 2, 1>(h, h->ws.hpl, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,     \
+                               h->S ? h->H : 0, h->ex.w2q, h->ex.w2s, h->sh.w2q, h->sh.w2s,     \
+                               h->ws.y, nullptr, h->H, st)
+  if (T >= 2 && bf16_smem(2, 2, h_stride) <= (size_t)kActSmemBytes) MOE_W2(2);
+  MOE_W2(1);
+#undef MOE_W2
 }
 
 }  // namespace moe

@@ -96,6 +96,7 @@ struct __align__(1024) SmemTC {
   uint64_t a_full[NG], a_empty[NG];
   uint64_t b_full[NB], b_empty[NB];
   uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;                // the MMA warp's last commit, before TMEM is freed
   uint32_t tmem_base;
   int abort;
 };
@@ -137,15 +138,17 @@ struct TcParams {
   const float *xcol;       // [R] 2^-ex of the row's token (W13 epilogue)
   const float *hcol;       // [R] 2^fh of the row's token (W13 epilogue)
   int32_t *status;
+  unsigned long long wait_ns;   // limit of each role wait (MOE_OPT_WAIT_LIMIT_US)
 };
 
 // --------------------------------------------------------------- PTX glue --
 // (mbarrier, TMA and elect helpers: ptx.cuh; tcgen05 descriptors, MMA issue,
 // tensor-memory loads and stores and the int4 decodes: tc.cuh)
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, SmemTC *sm,
-                                         int32_t *status) {
-  return moe::wait_bar(bar, parity, &sm->abort, status);
+template <bool kShortWaits>
+__device__ __forceinline__ bool wait_tc(uint64_t *bar, uint32_t parity, SmemTC *sm,
+                                        const TcParams &p) {
+  return moe::wait_role<kShortWaits>(bar, parity, &sm->abort, p.status, p.wait_ns);
 }
 
 // --------------------------------------------------------------- tiles --
@@ -185,6 +188,9 @@ __device__ __forceinline__ bool tile_at(const TcParams &p, int t, int n_fb, int 
 //
 // A = fp16(q * s * 2^pw) per weight (the scale applied in the dequant), one
 // accumulator per tile, fp16 h * 2^fh out of W13.
+// kShortWaits: the instantiation launched when the caller set a wait limit
+// below the default (MOE_OPT_WAIT_LIMIT_US); the ordinary one never tests it.
+template <bool kShortWaits>
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ TcParams p) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
@@ -213,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       mbar_init(&sm->acc_full[i], 1);
       mbar_init(&sm->acc_empty[i], 4);
     }
+    mbar_init(&sm->drain, 1);
     sm->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         for (int r = 0; r < tl.K / RK; ++r) {
           const int s = rk % NR;
           const uint32_t ph = (rk / NR) & 1;
-          if (!(ok = wait_bar(&sm->raw_empty[s], ph ^ 1, sm, p.status))) break;
+          if (!(ok = wait_tc<kShortWaits>(&sm->raw_empty[s], ph ^ 1, sm, p))) break;
           fence_proxy_async();
           if (elect_one()) {
             mbar_expect_tx(&sm->raw_full[s], BM * 128 + BM * (RK / 64) * 4);
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         for (int k0 = 0; k0 < tl.K / BK; k0 += kps) {
           const int s2 = sb % NB;
           const uint32_t ph2 = (sb / NB) & 1;
-          if (!(ok = wait_bar(&sm->b_empty[s2], ph2 ^ 1, sm, p.status))) break;
+          if (!(ok = wait_tc<kShortWaits>(&sm->b_empty[s2], ph2 ^ 1, sm, p))) break;
           if (elect_one()) {
             mbar_expect_tx(&sm->b_full[s2], kps * rows * 128);
             for (int j = 0; j < kps; ++j)
@@ -305,8 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       uint32_t it = 0;
       uint32_t ga = 0, gpar = 0;          // A group and its phase
       uint32_t bs = 0, bpar = 0;          // token slot and its phase
-      int last_acc = -1;
-      uint32_t last_acc_par = 0;
       constexpr uint32_t kSlotDesc = (kSlotRows * 128) >> 4;   // descriptor units per slot
       const uint64_t db0 = sw128_desc(smem_u32(sm->b[0]));
       bool ok = true;
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         Tile tl;
         if (!tile_at(p, t, n_fb, n_blocks, tl) || tl.nvalid <= 0) continue;
         const int buf = it & 1;
-        if (!(ok = wait_bar(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p.status))) break;
+        if (!(ok = wait_tc<kShortWaits>(&sm->acc_empty[buf], ((it >> 1) & 1) ^ 1, sm, p))) break;
         tc_fence_after();
         const int ncols = tl.nvalid;
         const uint32_t idesc = idesc_f16(BM, (ncols + 15) & ~15);
@@ -327,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         uint32_t first = 1;
         uint64_t db_slot = db0;
         for (int k0 = 0; ok && k0 < nkb; k0 += KPG) {
-          if (!(ok = wait_bar(&sm->a_full[ga], gpar, sm, p.status))) break;
+          if (!(ok = wait_tc<kShortWaits>(&sm->a_full[ga], gpar, sm, p))) break;
           tc_fence_after();
           const uint32_t acol = tmem + kACol0 + ga * kGroupCols;
 #pragma unroll
           for (int j = 0; j < KPG; ++j) {
             if (jj == 0) {
-              if (!(ok = wait_bar(&sm->b_full[bs], bpar, sm, p.status))) break;
+              if (!(ok = wait_tc<kShortWaits>(&sm->b_full[bs], bpar, sm, p))) break;
               db_slot = db0 + (uint64_t)(bs * kSlotDesc);
             }
             const bool slot_done = (jj == kps_m1);
@@ -359,15 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         if (!ok) break;
         if (elect_one()) mma_commit(&sm->acc_full[buf]);
         __syncwarp();
-        last_acc = buf;
-        last_acc_par = (it >> 1) & 1;
         ++it;
       }
-      // Drain: the last commit covers every MMA issued before it.
-      if (last_acc >= 0) {
+      // Drain: one more commit covers every MMA this thread issued -- also
+      // those of a tile it stopped in the middle of -- and TMEM is freed only
+      // once it has arrived (bounded by the full limit, whatever wait_ns is).
+      if (elect_one()) mma_commit(&sm->drain);
+      __syncwarp();
+      {
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(&sm->acc_full[last_acc], last_acc_par) &&
-               globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try_wait(&sm->drain, 0) && globaltimer() - t0 < kWaitNs) {
         }
       }
     }
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       // 2^-pw of this lane's weight row (exact: a power of two).
       const float rinv = __frcp_rn(__ldg((tl.shared ? p.rexp_s : p.rexp) + tl.wrow0 + row));
       const int buf = it & 1;
-      if (!(ok = wait_bar(&sm->acc_full[buf], (it >> 1) & 1, sm, p.status))) break;
+      if (!(ok = wait_tc<kShortWaits>(&sm->acc_full[buf], (it >> 1) & 1, sm, p))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + lane_base + buf * BN;
       for (int c0 = 0; c0 < tl.nvalid; c0 += 32) {
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
       const float re = __ldg((tl.shared ? p.rexp_s : p.rexp) + tl.wrow0 + r);   // 2^pw
       for (int rr = 0; rr < tl.K / RK; ++rr) {
         const int s = rk % NR;
-        if (!(ok = wait_bar(&sm->raw_full[s], (rk / NR) & 1, sm, p.status))) break;
+        if (!(ok = wait_tc<kShortWaits>(&sm->raw_full[s], (rk / NR) & 1, sm, p))) break;
         const float4 sc4 = *reinterpret_cast<const float4 *>(&sm->sc[s][r * (RK / 64)]);
         const uint8_t *rrow = sm->raw[s] + r * 128;
         uint4 c[RK / BK];
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 #pragma unroll
         for (int gi = 0; gi < GPS; ++gi) {
           const int ga = ag % NG;
-          if (!(ok = wait_bar(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p.status))) break;
+          if (!(ok = wait_tc<kShortWaits>(&sm->a_empty[ga], ((ag / NG) & 1) ^ 1, sm, p))) break;
           tc_fence_after();
           const uint32_t acol = tmem + lane_base + kACol0 + ga * kGroupCols + hh * 16;
           uint32_t o[KPG][16];
@@ -768,9 +774,10 @@ __device__ __noinline__ bool rt_wait_slow(uint64_t *bar, uint32_t parity, SmemRT
   }
 }
 
+// Called by whole warps; the same result in every lane (see moe::wait_bar).
 __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, SmemRT *sm,
                                         int32_t *status) {
-  return mbar_try_wait(bar, parity) || rt_wait_slow(bar, parity, sm, status);
+  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity) || rt_wait_slow(bar, parity, sm, status));
 }
 
 __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant__ RtParams p) {
@@ -987,9 +994,12 @@ namespace {
 cudaError_t set_tc_attrs() {
   static bool attr = false;   // per process; the attribute is per function
   if (!attr) {
-    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel,
+    cudaError_t err = cudaFuncSetAttribute(ggemm_kernel<false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(ggemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     attr = true;
   }
@@ -1014,6 +1024,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   const int h_stride = I > Is ? I : Is;
   cudaError_t err = set_tc_attrs();
   if (err != cudaSuccess) return err;
+  const bool short_waits = h->wait_ns < kWaitNs;
   err = launch_k(h->pdl, gather_kernel, dim3(h->num_sms * 4), dim3(256), 0, st, x,
                  h->L.x_dtype == 1, T, H, k, S, w.perm, w.offsets + h->E, w.w,
                  (const float *)h->hnorm, w.xp, w.wperm, w.xcol, w.hcol);
@@ -1061,7 +1072,9 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.xcol = w.xcol;
   p.hcol = w.hcol;
   p.status = w.status;
-  if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
+  p.wait_ns = h->wait_ns;
+  if ((err = launch_k(h->pdl, short_waits ? ggemm_kernel<true> : ggemm_kernel<false>, dim3(h->num_sms),
+                      dim3(kThreads), kSmemBytes, st, p)) !=
       cudaSuccess)
     return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {
@@ -1088,7 +1101,8 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   p.rows_s = H;
   p.rexp = h->ex.w2e;
   p.rexp_s = S ? h->sh.w2e : h->ex.w2e;
-  if ((err = launch_k(h->pdl, ggemm_kernel, dim3(h->num_sms), dim3(kThreads), kSmemBytes, st, p)) !=
+  if ((err = launch_k(h->pdl, short_waits ? ggemm_kernel<true> : ggemm_kernel<false>, dim3(h->num_sms),
+                      dim3(kThreads), kSmemBytes, st, p)) !=
       cudaSuccess)
     return err;
   if (h->profile && hm->n_ev <= moe_handle::kMaxStages) {

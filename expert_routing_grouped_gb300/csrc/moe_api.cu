@@ -113,7 +113,7 @@ void carve(moe_handle *h, Carver &c) {
   w.ticket = c.take<int32_t>(1 + (E + 7) / 8);
   w.route_kv = c.take<float>(2 * (size_t)moe::kRouteTokens * E);
   w.usage = c.take<unsigned long long>(E);
-  w.h = c.take<float>(rows * Imax);
+  w.hpl = c.take<__nv_bfloat16>(2 * rows * Imax);
   w.hb = c.take<__half>(rows * Imax);
   w.y = c.take<float>(rows * H);
   w.xp = c.take<__half>(rows * H);
@@ -239,6 +239,34 @@ int copy_weights(moe_handle *h, const moe_weights *W) {
   return rc;
 }
 
+}  // namespace
+
+namespace moe {
+L2Prefetch next_layer_prefetch(const moe_handle *h) {
+  L2Prefetch pf{};
+  const moe_handle *nx = h->next;
+  if (!nx) return pf;
+  auto add = [&pf](const void *p, size_t bytes) {
+    if (p && bytes >= 16 && pf.n < L2Prefetch::kMax) {
+      pf.ptr[pf.n] = static_cast<const char *>(p);
+      pf.bytes[pf.n] = bytes & ~static_cast<size_t>(15);
+      ++pf.n;
+    }
+  };
+  const size_t E = nx->E, H = nx->H, Is = nx->Is;
+  add(nx->wr_t, E * H * 4);
+  if (nx->S) {
+    add(nx->sh.w13q, 2 * Is * H / 2);
+    add(nx->sh.w13s, 2 * Is * (H / 64) * 4);
+    add(nx->sh.w2q, H * Is / 2);
+    add(nx->sh.w2s, H * (Is / 64) * 4);
+  }
+  return pf;
+}
+}  // namespace moe
+
+namespace {
+
 int choose_regime(const moe_handle *h, int T) {
   if (h->regime_opt == 1) return 1;
   if (h->regime_opt == 2) return 2;
@@ -334,6 +362,7 @@ __attribute__((visibility("default"))) int moe_init(const moe_layout *layout,
   h->regime_opt = 0;
   h->small_t_max = 1;
   h->pdl = 1;
+  h->wait_ns = 2000000000ull;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -452,6 +481,11 @@ __attribute__((visibility("default"))) int moe_set_option(moe_handle *h, int opt
     h->pdl = value;
     return MOE_OK;
   }
+  if (option == MOE_OPT_WAIT_LIMIT_US) {
+    if (value < 0) return MOE_ERR_ARG;
+    h->wait_ns = value == 0 ? 0ull : (unsigned long long)value * 1000ull;
+    return MOE_OK;
+  }
   if (option == MOE_OPT_USAGE) {
     if (value != 0 && value != 1) return MOE_ERR_ARG;
     h->count_usage = value;
@@ -475,6 +509,13 @@ __attribute__((visibility("default"))) int moe_usage_reset(moe_handle *h) {
       cudaMemset(h->ws.usage, 0, (size_t)h->E * 8) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
     return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+__attribute__((visibility("default"))) int moe_set_next_layer(moe_handle *h,
+                                                              const moe_handle *next) {
+  if (!h || next == h) return MOE_ERR_ARG;
+  h->next = next;
   return MOE_OK;
 }
 

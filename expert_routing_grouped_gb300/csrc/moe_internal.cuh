@@ -62,7 +62,8 @@ struct Workspace {
   float *route_kv;    // [2][kRouteTokens][E] fused small-T routing: keys, then scores
   unsigned long long *usage;  // [E] assignments per expert over the counted forwards
   // expert activations
-  float *h;           // [max_tokens*k + S*max_tokens][I_max] f32 (GEMV path)
+  __nv_bfloat16 *hpl; // [max_tokens*k + S*max_tokens][2][I_max] GEMV path: h as exact bf16
+                      // planes, hi = bf16(h) then lo = bf16(h - hi)
   __half *hb;         // [max_tokens*k + S*max_tokens][I_max] fp16 h * 2^fh (tensor-core path)
   float *y;           // [max_tokens*k + S*max_tokens][H] f32 (tensor-core path)
   __half *xp;         // [max_tokens*k + S*max_tokens][H] fp16 x * 2^ex in grouped order
@@ -110,6 +111,36 @@ static __device__ __forceinline__ T *after_wait(T *p) {
   return reinterpret_cast<T *>(v);
 }
 
+// Address ranges to pull into L2 ahead of their use: the next layer's router
+// and shared expert, which that layer reads whatever it routes to.  Every
+// range starts on a 16-byte boundary and its length is a multiple of 16.
+struct L2Prefetch {
+  static constexpr int kMax = 5;
+  const char *ptr[kMax];
+  unsigned long long bytes[kMax];
+  int n;
+};
+
+// Thread 0 of each CTA prefetches the CTA's 1/gridDim share of every range
+// with cp.async.bulk.prefetch.L2 (a hint: nothing waits for it, and the data
+// read from these addresses is the same with or without it).
+static __device__ __forceinline__ void l2_prefetch_share(const L2Prefetch &pf) {
+  if (threadIdx.x != 0) return;
+  constexpr unsigned long long kPiece = 32768;
+  for (int r = 0; r < pf.n; ++r) {
+    const unsigned long long b = pf.bytes[r];
+    const unsigned long long share = ((b + gridDim.x - 1) / gridDim.x + 15) & ~15ull;
+    const unsigned long long lo = share * blockIdx.x;
+    const unsigned long long hi = lo + share < b ? lo + share : b;
+    for (unsigned long long off = lo; off < hi; off += kPiece) {
+      const unsigned long long len = hi - off < kPiece ? hi - off : kPiece;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pf.ptr[r] + off),
+                   "r"((uint32_t)len)
+                   : "memory");
+    }
+  }
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                      cudaStream_t st, Args &&...args) {
@@ -137,6 +168,8 @@ struct moe_handle {
   __nv_bfloat16 *wr_planes;      // [3][E][H] bf16 hi/mid/lo planes of wr_t (tensor-core router)
   float *bias;                   // [E] or nullptr
   float *hnorm;                  // [2] largest W1 / W3 row norm over all experts (bounds |h|)
+  const moe_handle *next;        // moe_set_next_layer: the layer whose router and shared expert
+                                 // this one's W2 pass prefetches into L2 (or nullptr)
   moe::ExpertWeights ex;         // routed experts
   moe::ExpertWeights sh;         // shared expert (single)
   moe::Workspace ws;
@@ -146,6 +179,7 @@ struct moe_handle {
   int small_t_max;               // MOE_OPT_SMALL_T_MAX
   int pdl;                       // MOE_OPT_PDL
   int count_usage;               // MOE_OPT_USAGE
+  unsigned long long wait_ns;    // MOE_OPT_WAIT_LIMIT_US, in ns (default 2 s)
   int last_T;
   int last_regime;
   cudaStream_t last_stream;
@@ -162,6 +196,9 @@ struct moe_handle {
 
 namespace moe {
 
+// The next layer's router and shared expert as L2 prefetch ranges (none when
+// no next layer is set).
+L2Prefetch next_layer_prefetch(const moe_handle *h);
 // router.cu
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t s);
 // T <= kRouteTokens: router, top-k and dispatch in one launch (also clears the

@@ -43,6 +43,20 @@ static __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t par
   return ok != 0;
 }
 
+// The non-blocking test (try_wait may hold the thread for a while before it
+// reports an incomplete phase; test_wait answers at once).
+static __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The same test, letting the thread sleep until the phase completes (or
 // kSuspendNs passes): a polling warp then takes no issue slots from the
 // warps that share its scheduler.
@@ -65,9 +79,10 @@ static __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-// Bounded wait: false if the CTA is stopping (*abort set) or the wait timed
-// out (then *status and *abort are set).  The first test is inlined; only a
-// wait that has to poll calls the out-of-line loop.
+// Bounded wait: false if the CTA is stopping (*abort set) or the wait ran
+// past kWaitNs (then *status and *abort are set).  The first test is
+// inlined; only a wait that has to poll calls the out-of-line loop, which
+// sleeps in the mbarrier between polls.
 static __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, int *abort,
                                                   int32_t *status) {
   const unsigned long long t0 = globaltimer();
@@ -84,9 +99,47 @@ static __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity
   }
 }
 
+// Called by a whole warp.  Its lanes decide alike: they test the barrier
+// together, and the phase cannot move on while they wait (the warp that
+// releases it next is held by this warp's own next __syncwarp), so under a
+// 2 s limit no lane can give up where another saw completion.
 static __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *abort,
                                                 int32_t *status) {
   return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort, status);
+}
+
+// The same wait under a limit shorter than the default, for the kernels'
+// short-wait instantiations (the limit test in the hot wait costs time, so
+// the ordinary kernels never carry it): non-blocking tests -- try_wait may
+// hold a thread past a short limit -- with the clock read after every one.
+// A limit of 0 gives up at the first incomplete test.
+static __device__ __noinline__ bool wait_bar_short_loop(uint64_t *bar, uint32_t parity, int *abort,
+                                                        int32_t *status,
+                                                        unsigned long long limit_ns) {
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int *>(abort)) return false;
+    if (globaltimer() - t0 >= limit_ns) {
+      atomicExch(abort, 1);
+      atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// The role wait of a kernel instantiated with or without short waits.  Under
+// a short limit a lane may give up within nanoseconds of another seeing the
+// phase complete, so there the warp votes: every lane gets the same answer
+// and the warp-collective instructions that follow (elect.sync, tcgen05.ld /
+// st) are never reached by part of a warp.
+template <bool kShortWaits>
+static __device__ __forceinline__ bool wait_role(uint64_t *bar, uint32_t parity, int *abort,
+                                                 int32_t *status, unsigned long long limit_ns) {
+  if constexpr (kShortWaits)
+    return __all_sync(0xffffffffu, wait_bar_short_loop(bar, parity, abort, status, limit_ns));
+  else
+    return wait_bar(bar, parity, abort, status);
 }
 
 // Spins (bounded) until the phase of `parity` completes; for draining copies

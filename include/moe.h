@@ -220,7 +220,32 @@ int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
  * wait covers kernels, not the caller's copies or memsets before it).  The
  * same results bit for bit; 0: plain launches. */
 #define MOE_OPT_PDL 5
+/* The time limit, in microseconds, of each wait between the roles of the
+ * pipelined tensor-core kernels (a copy or an MMA that a role waits for);
+ * default 2000000 (2 s).  A wait that runs out sets the status word to 2 and
+ * the kernel stops its roles, waits (with the full 2 s limit) for its own
+ * copies and MMAs in flight, frees its tensor memory and returns, so the next
+ * forward runs normally; moe_status reports the 2 and moe_forward returns
+ * MOE_OK (the launch succeeded).  0 makes every wait that is not complete
+ * when first tested give up at once: a way to exercise that recovery path
+ * without a fault or a hang.  Negative values return MOE_ERR_ARG. */
+#define MOE_OPT_WAIT_LIMIT_US 6
 int moe_set_option(moe_handle *h, int option, int value);
+
+/*
+ * Next-layer prefetch (the colibri tuning guide's PILOT, gitcode.com knob
+ * table and "PILOT" paragraph: while one layer runs, the engine fetches what
+ * the next layer will read, ahead of its routing).  With every weight resident
+ * in HBM, the GPU form of that read-ahead is an L2 prefetch of what the next
+ * layer reads whatever it routes to: its router weights and its shared
+ * expert.  After moe_set_next_layer(h, next), every forward on h issues
+ * cp.async.bulk.prefetch.L2 for next's router and shared expert from the W2
+ * pass of the GEMV and exact decode paths (T <= 8), spread over its CTAs; it
+ * is a hint and changes no result.  next == NULL clears the link; a handle
+ * cannot name itself (MOE_ERR_ARG).  next is not owned: clear the link (or
+ * free h) before moe_free(next).  Returns MOE_OK or MOE_ERR_ARG.
+ */
+int moe_set_next_layer(moe_handle *h, const moe_handle *next);
 
 /* Fills *d with device pointers describing the last forward call. */
 int moe_debug_view(moe_handle *h, moe_debug *d);

@@ -81,3 +81,59 @@ def test_decode_stack_teacher_forced_and_free_running():
     got = resid.cpu().numpy()
     assert np.all(np.isfinite(got))
     assert rel_l2(got, ox) <= FREE_TOL, (rel_l2(got, ox), near_ties)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_stack_graph_replay_and_prefetch_bitwise(T):
+    """The decode bench times the 8-layer stack as one captured CUDA graph with
+    next-layer L2 prefetch links (moe_set_next_layer).  Both must leave the
+    results untouched: the eager stack without links, the eager stack with
+    links, and two replays of the captured stack with links agree bit for bit
+    (the eager stack itself is checked against the oracle above).  T = 1 runs
+    the GEMV path, whose W13 pass streams the shared expert before it waits
+    for the routing kernel; T = 4 the exact decode tensor-core kernel."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    dev = torch.device("cuda:0")
+    wl = synth.BY_NAME["glm_decode"]
+    H = wl.H
+    layers = [make_layer(wl, l, 4, dev)[0] for l in range(wl.layers)]
+    x0 = torch.from_numpy(synth.bf16_to_f32(synth.x_rows(wl, T))).to(dev)
+    resid = torch.empty(T, H, device=dev)
+    xn = torch.empty(T, H, dtype=torch.int16, device=dev)
+    stream = torch.cuda.Stream()
+
+    def stack():
+        resid.copy_(x0)
+        for lay in layers:
+            moe.rmsnorm_bf16(resid, T, H, 1e-6, xn, stream)
+            lay.forward_residual(xn, T, resid, stream)
+
+    try:
+        with torch.cuda.stream(stream):
+            stack()
+        torch.cuda.synchronize()
+        plain = resid.cpu().numpy()
+        assert np.all(np.isfinite(plain))
+        assert all(lay.status() == 0 for lay in layers)
+        for a, b in zip(layers[:-1], layers[1:]):
+            a.set_next_layer(b)
+        with torch.cuda.stream(stream):
+            stack()
+        torch.cuda.synchronize()
+        assert np.array_equal(resid.cpu().numpy(), plain)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            stack()
+        for _ in range(2):
+            resid.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(resid.cpu().numpy(), plain)
+        assert all(lay.status() == 0 for lay in layers)
+        del g
+    finally:
+        for lay in layers:
+            lay.set_next_layer(None)
+        for lay in layers:
+            lay.close()
