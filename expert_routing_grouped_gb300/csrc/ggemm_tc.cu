@@ -787,7 +787,11 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.x * BM, t0 = blockIdx.y * RT_N;
-  const int nk = p.H / BK;
+  // Split-K over gridDim.z: this CTA's K blocks [kb0, kb0 + nk), its partial
+  // logits written to z[blockIdx.z][T][E] (the top-k sums the splits in order).
+  const int nk_all = p.H / BK;
+  const int kb0 = (int)((long long)nk_all * blockIdx.z / gridDim.z);
+  const int nk = (int)((long long)nk_all * (blockIdx.z + 1) / gridDim.z) - kb0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < RT_S; ++i) {
       mbar_init(&sm->full[i], 1);
@@ -818,8 +822,8 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
         mbar_expect_tx(&sm->full[s], RT_STAGE_TX);
 #pragma unroll
         for (int pl = 0; pl < 3; ++pl)
-          tma_load_2d(sm->a[s][pl], &p.map_a, kb * BK, pl * p.E + e0, &sm->full[s]);
-        tma_load_2d(sm->b[s], &p.map_x, kb * BK, t0, &sm->full[s]);
+          tma_load_2d(sm->a[s][pl], &p.map_a, (kb0 + kb) * BK, pl * p.E + e0, &sm->full[s]);
+        tma_load_2d(sm->b[s], &p.map_x, (kb0 + kb) * BK, t0, &sm->full[s]);
       }
       __syncwarp();
       armed |= 1u << s;
@@ -838,8 +842,12 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
       if (!(ok = rt_wait(&sm->full[s], (kb / RT_S) & 1, sm, p.status))) break;
       tc_fence_after();
       const uint64_t db = sw128_desc(smem_u32(sm->b[s]));
-      const int acc = kb * RT_ACC / nk;                       // accumulator of this k-block
-      const bool first = (kb == 0) || ((kb - 1) * RT_ACC / nk != acc);
+      // accumulator of this k-block: the n_acc accumulators take equal runs of
+      // the CTA's k-blocks (one each when there are no more k-blocks than
+      // accumulators)
+      const int n_acc = nk < RT_ACC ? nk : RT_ACC;
+      const int acc = kb * n_acc / nk;
+      const bool first = (kb == 0) || ((kb - 1) * n_acc / nk != acc);
       const uint32_t d = tmem + acc * RT_N;
       if (elect_one()) {
 #pragma unroll
@@ -882,7 +890,7 @@ __global__ void __launch_bounds__(256, 1) router_tc_kernel(const __grid_constant
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int t = t0 + c0 + j;
-            if (t < p.T) p.z[(size_t)t * p.E + e] = v[j];
+            if (t < p.T) p.z[((size_t)blockIdx.z * p.T + t) * p.E + e] = v[j];
           }
         }
       }
@@ -956,7 +964,8 @@ cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long l
   return launch_k(false, split_planes_kernel, dim3(152 * 4), dim3(256), 0, st, wr_t, planes, n);
 }
 
-cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t st) {
+cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, int splits,
+                             cudaStream_t st) {
   const int E = h->E, H = h->H;
   static bool attr = false;
   const size_t smem = sizeof(SmemRT) + 1024;
@@ -976,8 +985,8 @@ cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z
   p.H = H;
   p.z = z;
   p.status = h->ws.status;
-  return launch_k(false, router_tc_kernel, dim3((E + BM - 1) / BM, (T + RT_N - 1) / RT_N),
-                  dim3(256), smem, st, p);
+  return launch_k(false, router_tc_kernel,
+                  dim3((E + BM - 1) / BM, (T + RT_N - 1) / RT_N, splits), dim3(256), smem, st, p);
 }
 
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,

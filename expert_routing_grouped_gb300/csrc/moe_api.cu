@@ -95,9 +95,11 @@ void carve(moe_handle *h, Carver &c) {
     h->sh.w2e = c.take<float>(H);
   }
   moe::Workspace &w = h->ws;
-  const size_t zrows = maxT > (size_t)moe::kRouterSplitMax * moe::kRouteTokens
-                           ? maxT
-                           : (size_t)moe::kRouterSplitMax * moe::kRouteTokens;
+  // router partial logits: up to kRouterSplitMax splits of the small-T GEMV
+  // router, and of the batched routers up to kRouterSplitTokens tokens
+  const size_t zrows = std::max({maxT, (size_t)moe::kRouterSplitMax * moe::kRouteTokens,
+                                 (size_t)moe::kRouterSplitMax *
+                                     std::min(maxT, (size_t)moe::kRouterSplitTokens)});
   w.z_part = c.take<float>(zrows * E);
   w.idx = c.take<int32_t>(A);
   w.w = c.take<float>(A);

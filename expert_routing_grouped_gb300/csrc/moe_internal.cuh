@@ -14,7 +14,8 @@ namespace moe {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kRouterSplitMax = 16;   // split-K partitions of the decode router
+constexpr int kRouterSplitMax = 16;   // split-K partitions of the router
+constexpr int kRouterSplitTokens = 1024;   // largest T whose router is split above 4 tokens
 constexpr int kGemvTokens = 4;        // tokens one GEMV pass carries in registers
 constexpr int kRouteTokens = 8;       // largest T of the fused routing launch
 constexpr int kTileTokens = 160;      // tokens per tensor-core tile (the MMA's N)
@@ -218,7 +219,9 @@ cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumula
                            cudaStream_t s);
 cudaError_t launch_split_planes(const float *wr_t, __nv_bfloat16 *planes, long long n,
                                 cudaStream_t s);
-cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, cudaStream_t s);
+// splits: split-K partitions (gridDim.z); z receives [splits][T][E] partials.
+cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z, int splits,
+                             cudaStream_t s);
 // 2D tensor map over a row-major [rows][cols] array (row stride in elements),
 // box [box_rows][box_cols], 128-byte swizzle or none.  False if the driver
 // entry point is missing or the encoder rejects the arguments.

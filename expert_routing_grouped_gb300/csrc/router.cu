@@ -200,8 +200,14 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(
   __shared__ float ws[RG_BK][RG_BE + 4];
   const int t0 = blockIdx.y * RG_BT, e0 = blockIdx.x * RG_BE;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  // Split-K: this CTA's share of the H / RG_BK steps (gridDim.z splits), its
+  // partial logits written to z[blockIdx.z][T][E].
+  const int steps = H / RG_BK;
+  const int ks0 = (int)((long long)steps * blockIdx.z / gridDim.z);
+  const int ks1 = (int)((long long)steps * (blockIdx.z + 1) / gridDim.z);
+  z += (size_t)blockIdx.z * T * E;
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += RG_BK) {
+  for (int k0 = ks0 * RG_BK; k0 < ks1 * RG_BK; k0 += RG_BK) {
     // 64 x 16 elements of each operand, 4 per thread.
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -692,6 +698,17 @@ int router_splits(int T, int E, int H, int num_sms) {
   return T > 4 ? 1 : gemv_splits(E, H, num_sms);
 }
 
+// Split-K partitions of the batched routers (T > 4): a grid of `base` CTAs
+// (expert tiles x token tiles) is split over K until it covers the SMs, for
+// batches of up to kRouterSplitTokens tokens (the partials' buffer holds
+// kRouterSplitMax of those), each split keeping at least `min_steps` K steps.
+int batched_router_splits(int T, int base, int k_steps, int min_steps, int num_sms) {
+  int s = 1;
+  if (T > kRouterSplitTokens) return 1;
+  while (s < kRouterSplitMax && base * s < num_sms && k_steps / (2 * s) >= min_steps) s *= 2;
+  return s;
+}
+
 }  // namespace
 
 cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
@@ -739,7 +756,7 @@ cudaError_t launch_route_small(const moe_handle *h, const void *x, int T,
 cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_t st) {
   const int E = h->E, H = h->H, k = h->k;
   const int xb = h->L.x_dtype == 1;
-  const int splits = router_splits(T, E, H, h->num_sms);
+  int splits = router_splits(T, E, H, h->num_sms);
   cudaError_t err = cudaSuccess;
   if (T <= 4) {
     const int hps = H / splits;
@@ -753,12 +770,15 @@ cudaError_t launch_router(const moe_handle *h, const void *x, int T, cudaStream_
     err = launch_k(false, router_gemv_kernel<4>, grid, dim3(256), smem, st, x, xb, T, H, E,
                    h->wr_t, hps, h->ws.z_part, kGemvTokens);
   } else if (xb && tc_path_available()) {
-    // bf16 activations: tensor cores on the three bf16 planes of the f32 weights.
-    err = launch_router_tc(h, x, T, h->ws.z_part, st);
+    // bf16 activations: tensor cores on the three bf16 planes of the f32 weights
+    // (tiles of 128 experts x 64 tokens, 64-K blocks, at least 2 per split).
+    splits = batched_router_splits(T, ((E + 127) / 128) * ((T + 63) / 64), H / 64, 2, h->num_sms);
+    err = launch_router_tc(h, x, T, h->ws.z_part, splits, st);
   } else {
     const dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT);
-    err = launch_k(false, router_gemm_kernel, grid, dim3(256), 0, st, x, xb, T, H, E, h->wr_t,
-                   h->ws.z_part);
+    splits = batched_router_splits(T, (int)(grid.x * grid.y), H / RG_BK, 4, h->num_sms);
+    err = launch_k(false, router_gemm_kernel, dim3(grid.x, grid.y, splits), dim3(256), 0, st, x,
+                   xb, T, H, E, h->wr_t, h->ws.z_part);
   }
   if (err != cudaSuccess) return err;
   const int zstride = (T <= 4) ? kGemvTokens : T;
