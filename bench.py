@@ -586,7 +586,7 @@ def cpu_baseline(wl, T, n_tokens, layers_per_step=1):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 CSRC = os.path.join(ROOT, "expert_routing_grouped_gb300", "csrc")
 KERNEL_SOURCES = {"ggemm_w13_tc": ("ggemm_tc.cu", "tc.cuh", "ptx.cuh", "moe_internal.cuh"),
-                  "gemv_w13": ("gemv.cu", "moe_internal.cuh")}
+                  "gemv_w13": ("gemv.cu", "ptx.cuh", "moe_internal.cuh")}
 
 
 def source_digest(kernel):
