@@ -168,33 +168,41 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_scan_kernel(
     if (n_shared) active[na++] = E;
     *n_active = na;
   }
-  // Tensor-core token blocks, (expert << 16 | block index) in one int32,
-  // ordered by cost so that a round-robin deal of tiles over the CTAs gives
-  // each a similar mix: every full block (routed experts in expert order, then
-  // the shared expert's), then the partial last blocks by size class
-  // (> 128 tokens, > 64, > 32, the rest).
+  // Tensor-core token blocks, (expert << 16 | block index) in one int32.
+  // Two lists: every full block (routed experts in expert order, then the
+  // shared expert's), and the partial last blocks by size class (> 128
+  // tokens, > 64, > 32, the rest).  They are dealt alternately (full,
+  // partial, full, ...; the longer list's rest at the end), so that the
+  // tensor-bound full tiles and the weight-stream-bound small ones run side by
+  // side instead of one phase after the other; with the round-robin deal of
+  // tiles over the CTAs each CTA gets a similar mix.
   const int nfull = (tid < E) ? c / tile_m : 0;
   const int rem = (tid < E) ? c - nfull * tile_m : 0;
-  const int base_pos = block_exclusive_scan(nfull, warp_sums, &total);
-  for (int i = 0; i < nfull; ++i) tiles[base_pos + i] = (tid << 16) | i;
-  int ntot = total;
   const int s_full = n_shared ? T / tile_m : 0, s_rem = n_shared ? T - s_full * tile_m : 0;
+  const int base_pos = block_exclusive_scan(nfull, warp_sums, &total);
+  const int n_f = total + s_full;                       // full blocks
+  block_exclusive_scan(rem > 0 ? 1 : 0, warp_sums, &total);
+  const int n_p = total + (s_rem > 0 ? 1 : 0);         // partial blocks
+  // position of full block f and of partial block q in the dealt list
+  auto pos_f = [n_f, n_p](int f) { return f < n_p ? 2 * f : n_p + f; };
+  auto pos_q = [n_f, n_p](int q) { return q < n_f ? 2 * q + 1 : n_f + q; };
+  for (int i = 0; i < nfull; ++i) tiles[pos_f(base_pos + i)] = (tid << 16) | i;
   if (tid == 0)
-    for (int i = 0; i < s_full; ++i) tiles[ntot + i] = (E << 16) | i;
-  ntot += s_full;
+    for (int i = 0; i < s_full; ++i) tiles[pos_f(n_f - s_full + i)] = (E << 16) | i;
+  int nq = 0;
   for (int cls = 0; cls < 4; ++cls) {
     const int lo = cls == 0 ? 128 : cls == 1 ? 64 : cls == 2 ? 32 : 0;
     const int hi = cls == 0 ? tile_m : cls == 1 ? 128 : cls == 2 ? 64 : 32;
     const int f = (rem > lo && rem <= hi) ? 1 : 0;
     const int pos = block_exclusive_scan(f, warp_sums, &total);
-    if (f) tiles[ntot + pos] = (tid << 16) | nfull;
-    ntot += total;
+    if (f) tiles[pos_q(nq + pos)] = (tid << 16) | nfull;
+    nq += total;
     if (s_rem > lo && s_rem <= hi) {
-      if (tid == 0) tiles[ntot] = (E << 16) | s_full;
-      ntot += 1;
+      if (tid == 0) tiles[pos_q(nq)] = (E << 16) | s_full;
+      nq += 1;
     }
   }
-  if (tid == 0) n_tiles[0] = ntot;
+  if (tid == 0) n_tiles[0] = n_f + n_p;
 }
 
 // Phase 3, the ranges of phase 1: assignment a of range c and expert e goes to
