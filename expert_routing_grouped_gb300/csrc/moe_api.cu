@@ -436,11 +436,21 @@ __attribute__((visibility("default"))) int moe_forward_host(moe_handle *h, const
   const size_t xb = (size_t)T * h->H * h->x_elem, ob = (size_t)T * h->H * sizeof(float);
   if (cudaMemcpyAsync(h->ws.x_stage, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MOE_ERR_DEVICE;
-  rc = run_forward(h, h->ws.x_stage, T, h->ws.out_stage, false, st);
+  // A pinned, 16-byte aligned output buffer that the GPU can address (on a
+  // Grace host, over NVLink-C2C) is written by the combine kernel itself: its
+  // stores carry the device-to-host transfer, and no copy follows the layer.
+  // Any other buffer gets the result through the staging copy.
+  float *out_dev = h->ws.out_stage;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, out_host) == cudaSuccess && at.type == cudaMemoryTypeHost &&
+      at.devicePointer && (reinterpret_cast<uintptr_t>(at.devicePointer) & 15) == 0)
+    out_dev = static_cast<float *>(at.devicePointer);
+  rc = run_forward(h, h->ws.x_stage, T, out_dev, false, st);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, h->ws.out_stage, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaStreamSynchronize(st) != cudaSuccess)
+  if (out_dev == h->ws.out_stage &&
+      cudaMemcpyAsync(out_host, h->ws.out_stage, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_DEVICE;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_DEVICE;
   return MOE_OK;
 }
 

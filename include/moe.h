@@ -179,8 +179,13 @@ int moe_forward_residual(moe_handle *h, const void *x, int T, float *resid,
 
 /*
  * End-to-end call with HOST buffers: copies x (host) into the handle's
- * workspace, runs the layer, copies the result to out (host), and waits for
- * the stream.  Pinned host memory gives the fastest copies.
+ * workspace, runs the layer, delivers the result to out (host), and waits for
+ * the stream.  When out is pinned host memory with a device address and
+ * 16-byte aligned (cudaPointerGetAttributes reports it as host memory), the
+ * combine step writes the result into it directly (on a Grace host, over
+ * NVLink-C2C) and no copy follows; any other out buffer receives a copy from
+ * the workspace.  The results are the same either way.  Pinned x gives the
+ * fastest input copy.
  */
 int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
                      moe_stream_t stream);
@@ -197,8 +202,8 @@ int moe_rmsnorm_bf16(const float *x, int T, int H, float eps, uint16_t *out,
 
 /* Chooses the expert path: 0 automatic (T <= small_t_max -> the SIMT GEMV
  * path, T <= 8 -> the exact tensor-core path, else tensor cores), 1 always
- * the SIMT GEMV path, 2 always the tensor-core path (bf16 weights, bf16
- * operands), 3 the exact tensor-core path (T <= 8 only, else the GEMV path:
+ * the SIMT GEMV path, 2 always the tensor-core path (fp16 weights and
+ * operands with exact power-of-two range control), 3 the exact tensor-core path (T <= 8 only, else the GEMV path:
  * exact int4 codes, f32 operands as bf16 hi/lo pairs, f32 group scales and
  * accumulation -- the GEMV path's numerics, on four MMA pipelines per SM). */
 #define MOE_OPT_REGIME 1

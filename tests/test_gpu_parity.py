@@ -190,6 +190,33 @@ def test_dry_run_and_limits(dev):
     assert moe.lib.moe_set_option(h.handle, 99, 0) == -4
 
 
+@pytest.mark.parametrize("T", [1, 3, 16])
+def test_forward_host_pinned_and_pageable_outputs_agree(dev, T):
+    """moe_forward_host on all three expert paths (GEMV, exact decode TC,
+    tensor cores): a pinned 16-byte aligned output buffer, which the combine
+    step writes directly, a pinned buffer offset by 4 bytes and a pageable
+    numpy buffer, which both receive the staging copy, all get the device
+    forward's result bit for bit."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    wl = synth.BY_NAME["glm_decode"]
+    got, _, h, xd = run_and_compare(wl, T, dev, regime=moe.REGIME_AUTO)
+    assert h.debug_view().regime == (1 if T == 1 else 3 if T <= 8 else 2)
+    x_pin = xd.cpu().pin_memory()
+    out_pin = torch.full((T, wl.H), float("nan")).pin_memory()
+    h.forward_host(x_pin, T, out_pin)
+    assert np.array_equal(out_pin.numpy(), got)
+    buf = torch.full((T * wl.H + 1,), float("nan")).pin_memory()
+    off = buf[1:]                                   # 4 bytes past a pinned base
+    assert off.data_ptr() % 16 != 0
+    h.forward_host(x_pin, T, off)
+    assert np.array_equal(off.numpy().reshape(T, wl.H), got)
+    out_np = np.full((T, wl.H), np.nan, np.float32)
+    h.forward_host(x_pin.numpy(), T, out_np)
+    assert np.array_equal(out_np, got)
+    assert h.status() == 0
+
+
 def test_forward_host_and_residual(dev):
     import torch
     wl = synth.BY_NAME["glm_decode"]
