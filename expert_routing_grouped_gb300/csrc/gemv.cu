@@ -560,6 +560,255 @@ __global__ void __launch_bounds__(256) gemv_bf16_kernel(
   }   // phase
 }
 
+// ----------------------------------------------------------------------------
+// The single-token W2 GEMV on warp-level MMAs (T = 1: the decode regime).
+// The weights stream exactly as in the bf16-pair kernel (32-row items, 16-byte
+// non-allocating loads, one chunk prefetched ahead), and its exactness is
+// kept: bf16 (136 + q) codes times h's exact bf16 planes, f32 accumulation
+// inside each 64-wide group, 136 x (the group's sum of h) taken off and the
+// group scale applied per group.  Each iteration stores its 32 rows x 1024 K
+// and their scales into a shared tile; after one CTA barrier every warp
+// multiplies its 128-K slice of both 16-row tiles with mma.sync.m16n8k16
+// (bf16 in, f32 accumulate): one instruction covers 16 x 16 weights and both
+// planes, which are its B columns 0 (hi) and 1 (lo), so the sum of the two
+// accumulator columns is the product with h.  The eight warps' partial tiles
+// of an item are summed in warp order (the same sum every run).  (The same
+// scheme on W13, K = H = 6144, was slower than the SIMT kernel: six CTA
+// barriers per item tie every warp to the slowest load; W2 has two.)
+// Fragment layout (PTX ISA, mma.m16n8k16 for 16-bit types), lane = 4 g + q:
+// A rows g and g + 8, B column g, accumulator rows g, g + 8 and columns 2q,
+// 2q + 1.  Inside a 64-wide group the K order is permuted alike for A and B:
+// in step s, slots 2q, 2q + 1 hold K = 16q + 2s, +1 and slots 2q + 8, 2q + 9
+// hold K = 16q + 8 + 2s, +1.  A lane's A values are then the 32-bit words 2q
+// and 2q + 1 of its rows' 32-byte group (pair s = the nibbles at bits 4s and
+// 16 + 4s), and its B values the 16 activations K = 16q .. 16q + 15.
+constexpr int kTileK = 1024;                   // K per iteration (32 chunks)
+constexpr int kWPitch = kTileK / 2 + 32;       // bytes per staged weight row (an odd multiple of 32)
+constexpr int kSPitch = kTileK / 64 + 1;       // floats per staged scale row
+
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared memory of the MMA kernel: h's two planes and their chunk sums, two
+// weight tiles, two scale tiles, the partial tiles.
+size_t w2_mma_smem(int K) {
+  return (size_t)2 * K * 2 + (size_t)K / 8 + 2 * kRowsPerItem * kWPitch +
+         2 * kRowsPerItem * kSPitch * 4 + kWarps * 2 * 32 * 8;
+}
+
+__global__ void __launch_bounds__(256, 2) gemv_w2_mma_kernel(
+    const __nv_bfloat16 *__restrict__ act, int act_stride, int k, int E, int K_r, int K_s,
+    int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
+    const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
+    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    const float *__restrict__ wts, float *__restrict__ out_y, int out_stride,
+    const __grid_constant__ L2Prefetch pf) {
+  constexpr int PL = 2;   // h's planes = B columns 0 and 1
+  constexpr int T = 1;
+  l2_prefetch_share(pf);  // init-time weights: no wait needed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint4 smem_v[];
+  const int Kmax = K_r > K_s ? K_r : K_s;
+  uint4 *xs = smem_v;                                                      // [PL][K/8], swizzled
+  float *xsum = reinterpret_cast<float *>(smem_v + (size_t)PL * (Kmax / 8));  // [K/32]
+  uint8_t *wbuf = reinterpret_cast<uint8_t *>(xsum + Kmax / 32);          // [2][32][kWPitch]
+  float *sbuf = reinterpret_cast<float *>(wbuf + 2 * kRowsPerItem * kWPitch);  // [2][32][kSPitch]
+  float2 *part = reinterpret_cast<float2 *>(sbuf + 2 * kRowsPerItem * kSPitch);  // [8][2][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const uint64_t pol = l2_evict_first_policy();
+  const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
+  const int A = T * k;
+  int staged_e = -1;
+  int rr[kRowsPerWarp];   // this warp's rows of an item in the tile
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) rr[i] = kRowsPerWarp * warp + i;
+  bool pre = false;                    // wv/sc already hold this item's first chunk
+  uint4 wv[kRowsPerWarp];
+  float sc[kRowsPerWarp];
+  uint32_t tile = 0;                   // tiles written so far (buffer = tile & 1)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  act = after_wait(act);
+  active = after_wait(active);
+  n_active_p = after_wait(n_active_p);
+  offsets = after_wait(offsets);
+  perm = after_wait(perm);
+  wts = after_wait(wts);
+  out_y = after_wait(out_y);
+  // [routed items, the shared expert's], contiguous ranges per CTA
+  const int n_active = *n_active_p;
+  const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
+  const int n_routed = n_active - has_shared;
+  const int items = n_routed * items_r + has_shared * items_s;
+  const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+  const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+  for (int item = i0; item < i1; ++item) {
+    const Item it = item_at(item, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r, ws_r, wq_s,
+                            ws_s, active, offsets);
+    const int e = it.e, gi = it.g, p0 = it.p0, K = it.K;
+    const int chunks = K / 32;
+    if (!pre) {
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        wv[i] = make_uint4(0, 0, 0, 0);
+        sc[i] = 0.f;
+      }
+      if (lane < chunks) load_chunk(it, rr, lane, wv, sc, pol);
+    }
+    pre = false;
+    if (e != staged_e) {
+      __syncthreads();   // previous readers are done
+      // One thread per chunk: 64 bytes per plane in, swizzled out, the
+      // chunk sum over the planes.
+      for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        float sum = 0.f;
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) {
+          const size_t row = (size_t)(2 * p0 + pl);   // the position's plane pl
+          const uint4 *src = reinterpret_cast<const uint4 *>(act + row * act_stride) + c * 4;
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + j);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              sum += __uint_as_float(u[m] << 16) + __uint_as_float(u[m] & 0xFFFF0000u);
+          }
+          uint4 *dst = xs + (size_t)pl * (K / 8) + c * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j ^ ((c >> 1) & 3)] = v[j];
+        }
+        xsum[c] = sum;
+      }
+      __syncthreads();
+      staged_e = e;
+    }
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    const int niter = (K + kTileK - 1) / kTileK;
+    for (int itn = 0; itn < niter; ++itn, ++tile) {
+      // prefetch the next iteration's chunk of the same rows, or the next
+      // item's first
+      uint4 wn[kRowsPerWarp];
+      float sn[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        wn[i] = make_uint4(0, 0, 0, 0);
+        sn[i] = 0.f;
+      }
+      const int cn = (itn + 1) * 32 + lane;
+      if (itn + 1 < niter) {
+        if (cn < chunks) load_chunk(it, rr, cn, wn, sn, pol);
+      } else if (item + 1 < i1) {
+        const Item nx = item_at(item + 1, n_routed, items_r, E, A, T, K_r, K_s, rows_r, wq_r,
+                                ws_r, wq_s, ws_s, active, offsets);
+        if (lane < nx.K / 32) load_chunk(nx, rr, lane, wn, sn, pol);
+        pre = true;
+      }
+      // this iteration's rows and scales into tile buffer tile & 1 (its
+      // readers two tiles ago passed the barrier of the tile in between)
+      uint8_t *wt = wbuf + (size_t)(tile & 1) * kRowsPerItem * kWPitch;
+      float *st = sbuf + (size_t)(tile & 1) * kRowsPerItem * kSPitch;
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i)
+        *reinterpret_cast<uint4 *>(wt + rr[i] * kWPitch + lane * 16) = wv[i];
+      if ((lane & 1) == 0) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) st[rr[i] * kSPitch + (lane >> 1)] = sc[i];
+      }
+      __syncthreads();
+      // this warp's groups 2w, 2w + 1 of the iteration, both tiles
+      const int G = min(kTileK, K - itn * kTileK) / 64;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int gl = 2 * warp + j;
+        if (gl >= G) break;
+        const int gk = itn * (kTileK / 64) + gl;   // group index in K
+        uint32_t b0[4] = {0u, 0u, 0u, 0u}, b1[4] = {0u, 0u, 0u, 0u};
+        if (g < PL) {
+          const int c = 2 * gk + (q >> 1), j0 = 2 * (q & 1), sw = (c >> 1) & 3;
+          const uint4 *src = xs + (size_t)g * (K / 8) + c * 4;
+          const uint4 u0 = src[j0 ^ sw], u1 = src[(j0 + 1) ^ sw];
+          b0[0] = u0.x; b0[1] = u0.y; b0[2] = u0.z; b0[3] = u0.w;
+          b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
+        }
+        __syncwarp();   // the MMAs below are warp-collective
+        const float xc = 136.0f * (xsum[2 * gk] + xsum[2 * gk + 1]);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          // tile t: item rows 16t + g and 16t + g + 8
+          const int rl = 16 * t + g, rh = rl + 8;
+          const uint2 wl = *reinterpret_cast<const uint2 *>(wt + rl * kWPitch + gl * 32 + q * 8);
+          const uint2 wh = *reinterpret_cast<const uint2 *>(wt + rh * kWPitch + gl * 32 + q * 8);
+          const float sl = st[rl * kSPitch + gl], sh = st[rh * kSPitch + gl];
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4)
+            mma16816(d, nib_pair_bf16(wl.x >> (4 * s4)), nib_pair_bf16(wh.x >> (4 * s4)),
+                     nib_pair_bf16(wl.y >> (4 * s4)), nib_pair_bf16(wh.y >> (4 * s4)), b0[s4],
+                     b1[s4]);
+          // columns 0 and 1 (lanes q = 0): h's two planes
+          acc[t][0] = fmaf(sl, (d[0] + d[1]) - xc, acc[t][0]);
+          acc[t][1] = fmaf(sh, (d[2] + d[3]) - xc, acc[t][1]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        wv[i] = wn[i];
+        sc[i] = sn[i];
+      }
+    }
+    // The item's partial tiles; warp t sums tile t over the warps and
+    // writes it (lanes q = 0 hold columns 0 and 1).
+#pragma unroll
+    for (int t = 0; t < 2; ++t) part[(warp * 2 + t) * 32 + lane] = make_float2(acc[t][0], acc[t][1]);
+    __syncthreads();
+    if (warp < 2 && q == 0) {
+      const int t = warp;
+      float r0 = 0.f, r1 = 0.f;
+      for (int v = 0; v < kWarps; ++v) {   // warp order: the same sum every run
+        const float2 pv = part[(v * 2 + t) * 32 + lane];
+        r0 += pv.x;
+        r1 += pv.y;
+      }
+      const int p = p0;
+      const float w8 = (e < E) ? __ldcg(wts + __ldcg(perm + p)) : 1.0f;
+      out_y[(size_t)p * out_stride + gi * kRowsPerItem + 16 * t + g] = w8 * r0;
+      out_y[(size_t)p * out_stride + gi * kRowsPerItem + 16 * t + g + 8] = w8 * r1;
+    }
+  }
+}
+
+cudaError_t launch_w2_mma(const moe_handle *h, cudaStream_t st) {
+  const int h_stride = h->I > h->Is ? h->I : h->Is;
+  const int K_s = h->S ? h->Is : h->I;
+  const size_t smem = w2_mma_smem(h_stride);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(gemv_w2_mma_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  // Exactly the resident CTAs: items are dealt as contiguous per-CTA ranges.
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_w2_mma_kernel, kWarps * 32,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  return launch_k(h->pdl, gemv_w2_mma_kernel, dim3(h->num_sms * per_sm), dim3(kWarps * 32), smem,
+                  st, h->ws.hpl, h_stride, h->k, h->E, h->I, K_s, h->H, h->S ? h->H : 0, h->ex.w2q,
+                  h->ex.w2s, h->sh.w2q, h->sh.w2s, h->ws.active, h->ws.n_active, h->ws.offsets,
+                  h->ws.perm, h->ws.w, h->ws.y, h->H, next_layer_prefetch(h));
+}
+
 template <int NT, int PL, int MODE>
 cudaError_t launch_bf16(const moe_handle *h, const __nv_bfloat16 *act, int act_stride, int T,
                         int K_r, int K_s, int rows_r, int rows_s, const uint8_t *wq_r,
@@ -643,6 +892,7 @@ cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStrea
 
 cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
+  if (T == 1 && w2_mma_smem(h_stride) <= 113 * 1024) return launch_w2_mma(h, st);
 #define MOE_W2(NT)                                                                             \
   return launch_bf16<NT, 2, 1>(h, h->ws.hpl, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,     \
                                h->S ? h->H : 0, h->ex.w2q, h->ex.w2s, h->sh.w2q, h->sh.w2s,     \
