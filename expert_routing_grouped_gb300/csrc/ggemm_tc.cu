@@ -526,12 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 //              factor widened by 2% for the fp16 weights' and f32 sums'
 //              rounding);
 //   wperm[p] = the routing weight (1 for the shared expert) times 2^-fh.
-// One warp per row; every row of a token reduces max |x| and |x|^2 in the same
-// order, so all of them get the same factors.
+// One warp per token: it reduces max |x[t]| and |x[t]|^2 once, then converts
+// each 16-byte piece of x[t] once and stores it into every grouped row of the
+// token (its kept routed slots, inv[a] >= 0, and its shared-expert row A + t),
+// so x is read twice per token rather than twice per grouped row.
 __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x, int x_is_bf16,
                                                      int T, int H, int k, int n_shared,
-                                                     const int32_t *__restrict__ perm,
-                                                     const int32_t *__restrict__ n_assigned,
+                                                     const int32_t *__restrict__ inv,
                                                      const float *__restrict__ w,
                                                      const float *__restrict__ hnorm,
                                                      __half *__restrict__ xp,
@@ -539,30 +540,17 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
                                                      float *__restrict__ xcol,
                                                      float *__restrict__ hcol) {
   pdl_enter();
-  perm = after_wait(perm);
-  n_assigned = after_wait(n_assigned);
+  inv = after_wait(inv);
   w = after_wait(w);
   xp = after_wait(xp);
   wperm = after_wait(wperm);
   xcol = after_wait(xcol);
   hcol = after_wait(hcol);
-  const int A = T * k, R = A + n_shared * T;
-  const int n_routed = __ldcg(n_assigned);
+  const int A = T * k, nrows = k + n_shared;   // nrows <= 33
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const float n1 = __ldg(hnorm) * 1.02f, n3 = __ldg(hnorm + 1) * 1.02f;
-  for (int pr = warp; pr < R; pr += nwarps) {
-    if (pr >= n_routed && pr < A) continue;   // rows of slots the top-p trim dropped
-    int t;
-    float wt;
-    if (pr < A) {
-      const int a = __ldcg(perm + pr);
-      t = a / k;
-      wt = __ldcg(w + a);
-    } else {
-      t = pr - A;
-      wt = 1.0f;
-    }
+  for (int t = warp; t < T; t += nwarps) {
     const uint4 *src16 = reinterpret_cast<const uint4 *>(
         reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H);
     const float4 *src32 = reinterpret_cast<const float4 *>(
@@ -595,14 +583,24 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
     const float nrm = sqrtf(ss);
     const float bound = fmaxf(n1 * nrm, 0.28f) * (n3 * nrm);
     const int fh = max(-126, min(126, 14 - pow2_above(bound)));
-    if (lane == 0) {
+    // The token's grouped rows: row j < k is slot j (-1 when the top-p trim
+    // dropped it), row k the shared expert's.  Lane j holds row j; row 32
+    // (k = 32 with a shared expert) is the same in every lane.
+    const int a0 = t * k;
+    const int row_lane = lane < k ? __ldcg(inv + a0 + lane) : (lane < nrows ? A + t : -1);
+    const int row_32 = nrows > 32 ? A + t : -1;
+    for (int j = lane; j < nrows; j += 32) {
+      const int pr = j < 32 ? row_lane : row_32;
+      if (pr < 0) continue;
+      const float wt = j < k ? __ldcg(w + a0 + j) : 1.0f;
       wperm[pr] = wt * pow2f(-fh);
       xcol[pr] = pow2f(-ex);
       hcol[pr] = pow2f(fh);
     }
     const float xs = pow2f(ex);
+    // H is a multiple of 256, so every lane runs the same number of pieces
+    // and the shuffles below see the whole warp.
     if (x_is_bf16) {
-      uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pr * H);
       for (int i = lane; i < H / 8; i += 32) {
         const uint4 v = __ldg(src16 + i);
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
@@ -613,14 +611,23 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ x,
                                                __uint_as_float(wd[c] & 0xFFFF0000u) * xs);
           o[c] = *reinterpret_cast<const uint32_t *>(&hh);
         }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < nrows; ++j) {
+          const int pr = j < 32 ? __shfl_sync(0xffffffffu, row_lane, j) : row_32;
+          if (pr >= 0) reinterpret_cast<uint4 *>(xp + (size_t)pr * H)[i] = ov;
+        }
       }
     } else {
-      __half2 *dst = reinterpret_cast<__half2 *>(xp + (size_t)pr * H);
       for (int i = lane; i < H / 4; i += 32) {
         const float4 f = __ldg(src32 + i);
-        dst[2 * i] = __floats2half2_rn(f.x * xs, f.y * xs);
-        dst[2 * i + 1] = __floats2half2_rn(f.z * xs, f.w * xs);
+        const __half2 h0 = __floats2half2_rn(f.x * xs, f.y * xs);
+        const __half2 h1 = __floats2half2_rn(f.z * xs, f.w * xs);
+        const uint2 ov = make_uint2(*reinterpret_cast<const uint32_t *>(&h0),
+                                    *reinterpret_cast<const uint32_t *>(&h1));
+        for (int j = 0; j < nrows; ++j) {
+          const int pr = j < 32 ? __shfl_sync(0xffffffffu, row_lane, j) : row_32;
+          if (pr >= 0) reinterpret_cast<uint2 *>(xp + (size_t)pr * H)[i] = ov;
+        }
       }
     }
   }
@@ -1035,7 +1042,7 @@ cudaError_t launch_tc_path(const moe_handle *h, const void *x, int T, float *out
   if (err != cudaSuccess) return err;
   const bool short_waits = h->wait_ns < kWaitNs;
   err = launch_k(h->pdl, gather_kernel, dim3(h->num_sms * 4), dim3(256), 0, st, x,
-                 h->L.x_dtype == 1, T, H, k, S, w.perm, w.offsets + h->E, w.w,
+                 h->L.x_dtype == 1, T, H, k, S, w.inv, w.w,
                  (const float *)h->hnorm, w.xp, w.wperm, w.xcol, w.hcol);
   if (err != cudaSuccess) return err;
   moe_handle *hm = const_cast<moe_handle *>(h);
