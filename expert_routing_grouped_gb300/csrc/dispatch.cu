@@ -61,20 +61,15 @@ __device__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
 // chunk of 1024, __match_any_sync ranks a lane among the lanes of its warp
 // holding the same expert, and a per-(warp, expert) count table turns that
 // into a rank across the chunk.
-__global__ void __launch_bounds__(kThreads, 1) dispatch_rank_kernel(
-    const int32_t *__restrict__ idx, int A, int E, int32_t *__restrict__ inv,
-    int32_t *__restrict__ part, int32_t *__restrict__ status) {
-  pdl_enter();
-  idx = after_wait(idx);
-  inv = after_wait(inv);
-  part = after_wait(part);
-  status = after_wait(status);
+__device__ void rank_range(int c_idx, int C, const int32_t *__restrict__ idx, int A, int E,
+                           int32_t *__restrict__ inv, int32_t *__restrict__ part,
+                           int32_t *__restrict__ status) {
   extern __shared__ int smem[];
   int *run = smem;                 // [E] assignments of each expert so far in this range
   int *wc = run + E;               // [32][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int a0 = (int)((long long)A * blockIdx.x / gridDim.x);
-  const int a1 = (int)((long long)A * (blockIdx.x + 1) / gridDim.x);
+  const int a0 = (int)((long long)A * c_idx / C);
+  const int a1 = (int)((long long)A * (c_idx + 1) / C);
   for (int e = tid; e < E; e += kThreads) run[e] = 0;
   for (int i = tid; i < 32 * E; i += kThreads) wc[i] = 0;
   __syncthreads();
@@ -106,7 +101,15 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_rank_kernel(
     __syncthreads();
   }
   if (bad) atomicExch(status, kStatusBadExpert);
-  for (int x = tid; x < E; x += kThreads) part[(size_t)blockIdx.x * E + x] = run[x];
+  for (int x = tid; x < E; x += kThreads) part[(size_t)c_idx * E + x] = run[x];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) dispatch_rank_kernel(
+    const int32_t *__restrict__ idx, int A, int E, int32_t *__restrict__ inv,
+    int32_t *__restrict__ part, int32_t *__restrict__ status) {
+  pdl_enter();
+  rank_range(blockIdx.x, gridDim.x, after_wait(idx), A, E, after_wait(inv), after_wait(part),
+             after_wait(status));
 }
 
 // Phase 2, one CTA: per-expert totals over the C ranges, counts, offsets (a
@@ -116,20 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_rank_kernel(
 // shared expert, id E, appended last) and the tensor-core token blocks: one
 // entry per tile_m tokens of every non-empty group (the shared expert's
 // included), costliest first.
-__global__ void __launch_bounds__(kThreads, 1) dispatch_scan_kernel(
-    int T, int E, int n_shared, int tile_m, int C, int32_t *__restrict__ part,
-    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ active,
-    int32_t *__restrict__ n_active, int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
-    unsigned long long *__restrict__ usage) {
-  pdl_enter();
-  part = after_wait(part);
-  counts = after_wait(counts);
-  offsets = after_wait(offsets);
-  active = after_wait(active);
-  n_active = after_wait(n_active);
-  tiles = after_wait(tiles);
-  n_tiles = after_wait(n_tiles);
-  usage = after_wait(usage);
+__device__ void scan_ranges(int T, int E, int n_shared, int tile_m, int C,
+                            int32_t *__restrict__ part, int32_t *__restrict__ counts,
+                            int32_t *__restrict__ offsets, int32_t *__restrict__ active,
+                            int32_t *__restrict__ n_active, int32_t *__restrict__ tiles,
+                            int32_t *__restrict__ n_tiles, unsigned long long *__restrict__ usage) {
   __shared__ int warp_sums[32];
   __shared__ int total;
   const int tid = threadIdx.x;
@@ -205,26 +199,63 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_scan_kernel(
   if (tid == 0) n_tiles[0] = n_f + n_p;
 }
 
+__global__ void __launch_bounds__(kThreads, 1) dispatch_scan_kernel(
+    int T, int E, int n_shared, int tile_m, int C, int32_t *__restrict__ part,
+    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ active,
+    int32_t *__restrict__ n_active, int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
+    unsigned long long *__restrict__ usage) {
+  pdl_enter();
+  scan_ranges(T, E, n_shared, tile_m, C, after_wait(part), after_wait(counts),
+              after_wait(offsets), after_wait(active), after_wait(n_active), after_wait(tiles),
+              after_wait(n_tiles), after_wait(usage));
+}
+
 // Phase 3, the ranges of phase 1: assignment a of range c and expert e goes to
 // position part[c][e] + its rank: perm[pos] = a, inv[a] = pos.
-__global__ void __launch_bounds__(kThreads) dispatch_scatter_kernel(
-    const int32_t *__restrict__ idx, int A, int E, const int32_t *__restrict__ part,
-    int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
-  pdl_enter();
-  idx = after_wait(idx);
-  part = after_wait(part);
-  perm = after_wait(perm);
-  inv = after_wait(inv);
-  const int a0 = (int)((long long)A * blockIdx.x / gridDim.x);
-  const int a1 = (int)((long long)A * (blockIdx.x + 1) / gridDim.x);
+__device__ void scatter_range(int c_idx, int C, const int32_t *__restrict__ idx, int A, int E,
+                              const int32_t *__restrict__ part, int32_t *__restrict__ perm,
+                              int32_t *__restrict__ inv) {
+  const int a0 = (int)((long long)A * c_idx / C);
+  const int a1 = (int)((long long)A * (c_idx + 1) / C);
   for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
     const int e = idx[a];
     const int r = inv[a];
     if (e < 0 || e >= E || r < 0) continue;
-    const int pos = part[(size_t)blockIdx.x * E + e] + r;
+    const int pos = part[(size_t)c_idx * E + e] + r;
     perm[pos] = a;
     inv[a] = pos;
   }
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_scatter_kernel(
+    const int32_t *__restrict__ idx, int A, int E, const int32_t *__restrict__ part,
+    int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
+  pdl_enter();
+  scatter_range(blockIdx.x, gridDim.x, after_wait(idx), A, E, after_wait(part), after_wait(perm),
+                after_wait(inv));
+}
+
+// The three phases in one CTA, for a single range (A <= kThreads assignments):
+// one launch instead of three.  A CTA barrier between the phases makes each
+// phase's global writes visible to the next one's threads.
+__global__ void __launch_bounds__(kThreads, 1) dispatch_small_kernel(
+    const int32_t *__restrict__ idx, int T, int A, int E, int n_shared, int tile_m,
+    int32_t *__restrict__ inv, int32_t *__restrict__ part, int32_t *__restrict__ perm,
+    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ active,
+    int32_t *__restrict__ n_active, int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
+    unsigned long long *__restrict__ usage, int32_t *__restrict__ status) {
+  pdl_enter();
+  idx = after_wait(idx);
+  inv = after_wait(inv);
+  part = after_wait(part);
+  perm = after_wait(perm);
+  rank_range(0, 1, idx, A, E, inv, part, after_wait(status));
+  __syncthreads();
+  scan_ranges(T, E, n_shared, tile_m, 1, part, after_wait(counts), after_wait(offsets),
+              after_wait(active), after_wait(n_active), after_wait(tiles), after_wait(n_tiles),
+              after_wait(usage));
+  __syncthreads();
+  scatter_range(0, 1, idx, A, E, part, perm, inv);
 }
 
 }  // namespace
@@ -237,9 +268,12 @@ cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned lon
   const size_t smem = (size_t)(1 + 32) * E * sizeof(int);
   static bool attr_set = false;   // per process; the attribute is per function
   if (!attr_set) {
+    const int max_smem = (int)((1 + 32) * kMaxExperts * sizeof(int));
     cudaError_t err = cudaFuncSetAttribute(dispatch_rank_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)((1 + 32) * kMaxExperts * sizeof(int)));
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(dispatch_small_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
@@ -248,6 +282,10 @@ cudaError_t launch_dispatch(const moe_handle *h, int T, int tile_m, unsigned lon
   // logits when the dispatch runs, and the buffer has max(max_tokens, 128) >= C
   // rows of E entries.
   int32_t *part = reinterpret_cast<int32_t *>(w.z_part);
+  if (C == 1)
+    return launch_k(h->pdl, dispatch_small_kernel, dim3(1), dim3(kThreads), smem, st, w.idx, T, A,
+                    E, h->S, tile_m, w.inv, part, w.perm, w.counts, w.offsets, w.active,
+                    w.n_active, w.tiles, w.n_tiles, usage, w.status);
   cudaError_t err = launch_k(h->pdl, dispatch_rank_kernel, dim3(C), dim3(kThreads), smem, st,
                              w.idx, A, E, w.inv, part, w.status);
   if (err == cudaSuccess)
