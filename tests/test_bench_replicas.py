@@ -121,7 +121,7 @@ def test_algorithmic_units_match_the_published_per_layer_figures():
     assert fl == routed + shared + router
 
 
-def test_clock_records_are_judged_and_a_bad_region_is_measured_once_more():
+def test_clock_records_are_checked_and_a_bad_region_is_measured_once_more():
     """A timed region that saw a hardware or thermal slowdown, or sat well
     below the maximum SM clock with no reason given, is measured once more
     (single process); sw_power_cap is kept.  The second record is the one
