@@ -892,7 +892,10 @@ cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStrea
 
 cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  if (T == 1 && w2_mma_smem(h_stride) <= 113 * 1024) return launch_w2_mma(h, st);
+  // The MMA kernel at T = 1 when an item takes few tile iterations (K <= 4096:
+  // each iteration ends at a CTA barrier; at K = 6144 (W13) and 14336 (a
+  // Mixtral-shaped W2) the SIMT kernel measured faster).
+  if (T == 1 && h_stride <= 4096 && w2_mma_smem(h_stride) <= 113 * 1024) return launch_w2_mma(h, st);
 #define MOE_W2(NT)                                                                             \
   return launch_bf16<NT, 2, 1>(h, h->ws.hpl, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,     \
                                h->S ? h->H : 0, h->ex.w2q, h->ex.w2s, h->sh.w2q, h->sh.w2s,     \
