@@ -572,9 +572,11 @@ __global__ void __launch_bounds__(256) gemv_bf16_kernel(
 // (bf16 in, f32 accumulate): one instruction covers 16 x 16 weights and both
 // planes, which are its B columns 0 (hi) and 1 (lo), so the sum of the two
 // accumulator columns is the product with h.  The eight warps' partial tiles
-// of an item are summed in warp order (the same sum every run).  (The same
-// scheme on W13, K = H = 6144, was slower than the SIMT kernel: six CTA
-// barriers per item tie every warp to the slowest load; W2 has two.)
+// of an item are summed in warp order (the same sum every run).  Every tile
+// iteration ends at a CTA barrier that ties each warp to the slowest one's
+// loads, so the kernel serves items of at most four iterations (K <= 4096);
+// at K = 6144 (W13) and 14336 (a Mixtral-shaped W2) the SIMT kernel is
+// faster.
 // Fragment layout (PTX ISA, mma.m16n8k16 for 16-bit types), lane = 4 g + q:
 // A rows g and g + 8, B column g, accumulator rows g, g + 8 and columns 2q,
 // 2q + 1.  Inside a 64-wide group the K order is permuted alike for A and B:
