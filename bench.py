@@ -306,9 +306,12 @@ def bench_prefill(dev, steps, warmup, stream, name="glm_prefill", sync_all=None)
 
 def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None, sync_all=None):
     """The decode stack: per layer an RMS pre-norm and moe_forward_residual.
-    The timed steps replay one CUDA graph of the whole stack (the library's
-    launches are stream-ordered and capturable); a separate eager pass with
-    tracing on gives the per-stage breakdown."""
+    The first layer's pre-norm is a moe_rmsnorm_bf16 call; every other one is
+    computed by the previous layer's combine (moe_forward_residual_norm, the
+    same bits in one launch instead of two).  The timed steps replay one CUDA
+    graph of the whole stack (the library's launches are stream-ordered and
+    capturable); a separate eager pass with tracing on gives the per-stage
+    breakdown."""
     import torch
     import expert_routing_grouped_gb300 as moe
     import synth
@@ -322,9 +325,12 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
 
     def step(st):
         resid.copy_(x32)
-        for lay in built:
-            moe.rmsnorm_bf16(resid, T, wl.H, 1e-6, u, st)
-            lay.forward_residual(u, T, resid, st)
+        moe.rmsnorm_bf16(resid, T, wl.H, 1e-6, u, st)
+        for i, lay in enumerate(built):
+            if i + 1 < n_layers:   # this layer's combine also writes the next one's input
+                lay.forward_residual_norm(u, T, resid, 1e-6, u, st)
+            else:
+                lay.forward_residual(u, T, resid, st)
 
     # eager pass with tracing: stage breakdown and activated-expert counts
     for lay in built:
@@ -360,7 +366,7 @@ def bench_decode(dev, steps, warmup, stream, T=1, name="glm_decode", layers=None
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         step(torch.cuda.current_stream())
-    per_replay = sum(l.debug_view().launches for l in built) - launches0 + n_layers
+    per_replay = sum(l.debug_view().launches for l in built) - launches0 + 1   # + the first norm
     for _ in range(warmup):
         g.replay()
         g_plain.replay()

@@ -21,7 +21,8 @@ X_F32, X_BF16 = 0, 1
 
 MOE_DBG_IDX, MOE_DBG_W, MOE_DBG_COUNTS, MOE_DBG_OFFSETS, MOE_DBG_PERM, MOE_DBG_INV = range(6)
 
-EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual", "moe_forward_host",
+EXPORTS = ("moe_init", "moe_route", "moe_forward", "moe_forward_residual",
+           "moe_forward_residual_norm", "moe_forward_host",
            "moe_rmsnorm_bf16", "moe_set_option", "moe_debug_view", "moe_debug_read",
            "moe_stage_times", "moe_status", "moe_device_bytes", "moe_free", "moe_strerror",
            "moe_route_noalloc", "moe_usage_read", "moe_usage_reset", "moe_engine_id",
@@ -63,6 +64,7 @@ def _load():
         "moe_forward": (i, [P, P, i, P, P]),
         "moe_route": (i, [P, P, i, P]),
         "moe_forward_residual": (i, [P, P, i, P, P]),
+        "moe_forward_residual_norm": (i, [P, P, i, P, f, P, P]),
         "moe_forward_host": (i, [P, P, i, P, P]),
         "moe_rmsnorm_bf16": (i, [P, i, i, f, P, P]),
         "moe_set_option": (i, [P, i, i]),
@@ -143,6 +145,11 @@ class MoELayer:
     def forward_residual(self, x, T, resid, stream=None):
         return _check(lib.moe_forward_residual(self._handle, _ptr(x), T, _ptr(resid),
                                                _stream(stream)), "moe_forward_residual")
+
+    def forward_residual_norm(self, x, T, resid, eps, norm_out, stream=None):
+        return _check(lib.moe_forward_residual_norm(self._handle, _ptr(x), T, _ptr(resid),
+                                                    float(eps), _ptr(norm_out), _stream(stream)),
+                      "moe_forward_residual_norm")
 
     def forward_host(self, x_host, T, out_host, stream=None):
         return _check(lib.moe_forward_host(self._handle, _ptr(x_host), T, _ptr(out_host),

@@ -734,6 +734,65 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, int n
   }
 }
 
+// The combine of one token by a 1024-thread block, followed by the next
+// stacked layer's RMS pre-norm of the updated row (moe_forward_residual_norm):
+// out[t] (+)= sum of the token's expert rows as in combine_kernel (the same
+// order, so the same bits), then norm_out[t] = bf16(rmsnorm(out[t])) exactly
+// as moe_rmsnorm_bf16 computes it.  One launch in place of two; the row stays
+// in registers between the two steps (float4s past 2048, H > 8192, are read
+// back from out).
+__global__ void __launch_bounds__(1024) combine_norm_kernel(
+    int T, int H, int k, int n_shared, const int32_t *__restrict__ inv,
+    const float *__restrict__ y, float *__restrict__ out, int accumulate, float eps,
+    __nv_bfloat16 *__restrict__ norm_out) {
+  pdl_enter();
+  inv = after_wait(inv);
+  y = after_wait(y);
+  out = after_wait(out);
+  norm_out = after_wait(norm_out);
+  __shared__ float part[32];
+  const int t = blockIdx.x;
+  const int A = T * k;
+  const int n4 = H / 4;
+  float4 *orow = reinterpret_cast<float4 *>(out + (size_t)t * H);
+  auto combine4 = [&](int c) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int row = __ldcg(inv + t * k + j);
+      if (row < 0) continue;   // a slot the top-p trim dropped
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + (size_t)row * H) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (n_shared) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + (size_t)(A + t) * H) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (accumulate) {
+      const float4 prev = orow[c];
+      acc.x += prev.x;
+      acc.y += prev.y;
+      acc.z += prev.z;
+      acc.w += prev.w;
+    }
+    orow[c] = acc;
+    return acc;
+  };
+  float4 v[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = threadIdx.x + r * 1024;
+    v[r] = (i < n4) ? combine4(i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = threadIdx.x + 2048; i < n4; i += 1024) combine4(i);
+  rmsnorm_row_bf16(orow, v, H, eps, norm_out + (size_t)t * H, part);
+}
+
 // ------------------------------------------------- router on tensor cores --
 //
 // z[t][e] = sum_h x[t][h] * Wr[e][h] for bf16 x, with Wr held as three bf16
@@ -998,6 +1057,10 @@ cudaError_t launch_router_tc(const moe_handle *h, const void *x, int T, float *z
 
 cudaError_t launch_combine(const moe_handle *h, int T, float *out, bool accumulate,
                            cudaStream_t st) {
+  if (h->norm_out && T > 0)   // with the next layer's pre-norm: one block per token
+    return launch_k(h->pdl, combine_norm_kernel, dim3(T), dim3(1024), 0, st, T, h->H, h->k, h->S,
+                    h->ws.inv, h->ws.y, out, accumulate ? 1 : 0, h->norm_eps,
+                    reinterpret_cast<__nv_bfloat16 *>(h->norm_out));
   // One float4 per thread; no more CTAs than there is work (decode: a handful).
   const long long work = (long long)T * (h->H / 4);
   const int blocks = (int)std::min<long long>((long long)h->num_sms * 8, (work + 255) / 256);

@@ -34,42 +34,12 @@ __global__ void __launch_bounds__(1024) rmsnorm_bf16_kernel(const float *__restr
   const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)t * H);
   const int n4 = H / 4;
   float4 v[2];
-  float ss = 0.f;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int i = threadIdx.x + r * 1024;
     v[r] = (i < n4) ? row[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    ss = fmaf(v[r].x, v[r].x, ss);
-    ss = fmaf(v[r].y, v[r].y, ss);
-    ss = fmaf(v[r].z, v[r].z, ss);
-    ss = fmaf(v[r].w, v[r].w, ss);
   }
-  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {   // H > 8192
-    const float4 f = row[i];
-    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < 32; ++w) tot += part[w];
-  const float r = 1.0f / sqrtf(tot / (float)H + eps);
-  __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(out + (size_t)t * H);
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int i = threadIdx.x + rr * 1024;
-    if (i < n4) {
-      o2[2 * i] = __floats2bfloat162_rn(v[rr].x * r, v[rr].y * r);
-      o2[2 * i + 1] = __floats2bfloat162_rn(v[rr].z * r, v[rr].w * r);
-    }
-  }
-  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {
-    const float4 f = row[i];
-    o2[2 * i] = __floats2bfloat162_rn(f.x * r, f.y * r);
-    o2[2 * i + 1] = __floats2bfloat162_rn(f.z * r, f.w * r);
-  }
+  rmsnorm_row_bf16(row, v, H, eps, out + (size_t)t * H, part);
 }
 
 // Library weight layout, written once at init from the canonical layout.

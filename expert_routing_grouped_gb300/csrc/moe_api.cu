@@ -427,6 +427,27 @@ __attribute__((visibility("default"))) int moe_forward_residual(moe_handle *h, c
   return run_forward(h, x, T, resid, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
+__attribute__((visibility("default"))) int moe_forward_residual_norm(
+    moe_handle *h, const void *x, int T, float *resid, float eps, uint16_t *norm_out,
+    moe_stream_t stream) {
+  int rc = check_call(h, x, T, resid);
+  if (rc) return rc;
+  if (!(eps >= 0.f)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  // norm_out is written with 16-byte accesses and must not overlap resid,
+  // which the same kernel reads and writes (it may be x: x is no longer read
+  // when the combine runs).
+  const uintptr_t nb = reinterpret_cast<uintptr_t>(norm_out),
+                  rb = reinterpret_cast<uintptr_t>(resid);
+  const size_t nlen = (size_t)T * h->H * sizeof(uint16_t), rlen = (size_t)T * h->H * sizeof(float);
+  if (!norm_out || (nb & 15) || (nb < rb + rlen && rb < nb + nlen)) return MOE_ERR_ARG;
+  h->norm_out = norm_out;
+  h->norm_eps = eps;
+  rc = run_forward(h, x, T, resid, true, reinterpret_cast<cudaStream_t>(stream));
+  h->norm_out = nullptr;
+  return rc;
+}
+
 __attribute__((visibility("default"))) int moe_forward_host(moe_handle *h, const void *x_host,
                                                             int T, float *out_host,
                                                             moe_stream_t stream) {
@@ -459,7 +480,8 @@ __attribute__((visibility("default"))) int moe_rmsnorm_bf16(const float *x, int 
                                                             moe_stream_t stream) {
   if (T < 0 || H <= 0 || H % 8 || !(eps >= 0.f)) return MOE_ERR_ARG;
   if (T == 0) return MOE_OK;
-  if (!x || !out) return MOE_ERR_ARG;
+  if (!x || !out || ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15))
+    return MOE_ERR_ARG;
   return moe::launch_rmsnorm_bf16(x, T, H, eps, out, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? MOE_OK

@@ -115,6 +115,52 @@ static __device__ __forceinline__ T *after_wait(T *p) {
 // Address ranges to pull into L2 ahead of their use: the next layer's router
 // and shared expert, which that layer reads whatever it routes to.  Every
 // range starts on a 16-byte boundary and its length is a multiple of 16.
+// The f32 RMS pre-norm of one row by a 1024-thread block:
+// out_row = bf16(row / sqrt(mean(row^2) + eps)).  v[r] holds the row's float4
+// number threadIdx.x + 1024 r (zero past the row's end); float4s from 2048 on
+// (H > 8192) are read from row.  One definition for the stand-alone norm and
+// the one fused into the combine, so the two give the same bits: a fixed
+// per-thread fmaf order, then warp and block sums in a fixed order.
+static __device__ __forceinline__ void rmsnorm_row_bf16(const float4 *row, const float4 (&v)[2],
+                                                        int H, float eps,
+                                                        __nv_bfloat16 *out_row, float *part) {
+  const int n4 = H / 4;
+  float ss = 0.f;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    ss = fmaf(v[r].x, v[r].x, ss);
+    ss = fmaf(v[r].y, v[r].y, ss);
+    ss = fmaf(v[r].z, v[r].z, ss);
+    ss = fmaf(v[r].w, v[r].w, ss);
+  }
+  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {
+    const float4 f = row[i];
+    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, ss))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 32; ++w) tot += part[w];
+  const float r = 1.0f / sqrtf(tot / (float)H + eps);
+  __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(out_row);
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int i = threadIdx.x + rr * 1024;
+    if (i < n4) {
+      o2[2 * i] = __floats2bfloat162_rn(v[rr].x * r, v[rr].y * r);
+      o2[2 * i + 1] = __floats2bfloat162_rn(v[rr].z * r, v[rr].w * r);
+    }
+  }
+  for (int i = threadIdx.x + 2048; i < n4; i += 1024) {
+    const float4 f = row[i];
+    o2[2 * i] = __floats2bfloat162_rn(f.x * r, f.y * r);
+    o2[2 * i + 1] = __floats2bfloat162_rn(f.z * r, f.w * r);
+  }
+}
+
 struct L2Prefetch {
   static constexpr int kMax = 5;
   const char *ptr[kMax];
@@ -181,6 +227,10 @@ struct moe_handle {
   int pdl;                       // MOE_OPT_PDL
   int count_usage;               // MOE_OPT_USAGE
   unsigned long long wait_ns;    // MOE_OPT_WAIT_LIMIT_US, in ns (default 2 s)
+  // moe_forward_residual_norm: during that call, the combine also writes
+  // bf16(rmsnorm(resid)) here (else nullptr)
+  uint16_t *norm_out;
+  float norm_eps;
   int last_T;
   int last_regime;
   cudaStream_t last_stream;

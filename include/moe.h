@@ -191,6 +191,20 @@ int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
                      moe_stream_t stream);
 
 /*
+ * As moe_forward_residual, and then norm_out[t] = bf16(rmsnorm(resid[t]))
+ * from the updated resid, bit for bit what moe_rmsnorm_bf16(resid, T, H, eps,
+ * norm_out) would give: the next stacked layer's pre-norm, computed by the
+ * kernel that adds the layer output into resid (one launch in place of two;
+ * norm before each MoE layer: tutorial cf-1.com §2.1 step 1).  norm_out
+ * [T][H] bf16 bits, device, 16-byte aligned; it may be x (x is no longer
+ * read when it is written) but must not overlap resid.  eps >= 0.
+ * Returns as moe_forward_residual; MOE_ERR_ARG also for a null, misaligned
+ * or overlapping norm_out or a bad eps.
+ */
+int moe_forward_residual_norm(moe_handle *h, const void *x, int T, float *resid, float eps,
+                              uint16_t *norm_out, moe_stream_t stream);
+
+/*
  * Pre-norm between stacked layers: out_bf16[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)),
  * computed in f32 with no learned gain (the pages normalise with RMSNorm before
  * the MoE layer: tutorial cf-1.com §2.1 step 1; the norm stays f32: teardown

@@ -95,8 +95,19 @@ def test_null_handle_calls():
     assert moe.lib.moe_usage_read(None, None, 8) == -4
     assert moe.lib.moe_usage_reset(None) == -4
     moe.lib.moe_free(None)
+    assert moe.lib.moe_forward_residual_norm(None, None, 1, None, 1e-6, None, None) == -4
     assert moe.lib.moe_rmsnorm_bf16(None, 0, 64, 1e-6, None, None) == 0     # dry run
     assert moe.lib.moe_rmsnorm_bf16(None, 2, 64, 1e-6, None, None) == -4
+
+
+def test_rmsnorm_rejects_misaligned_pointers():
+    """x and out are accessed 16 bytes at a time: an address off the 16-byte
+    grid is refused before anything is launched (no device is needed)."""
+    import ctypes
+    import expert_routing_grouped_gb300 as moe
+    P = ctypes.c_void_p
+    assert moe.lib.moe_rmsnorm_bf16(P(0x10004), 2, 64, 1e-6, P(0x20000), None) == -4
+    assert moe.lib.moe_rmsnorm_bf16(P(0x10000), 2, 64, 1e-6, P(0x20008), None) == -4
 
 
 def test_strerror():

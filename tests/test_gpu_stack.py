@@ -89,9 +89,12 @@ def test_decode_stack_graph_replay_and_prefetch_bitwise(T):
     next-layer L2 prefetch links (moe_set_next_layer).  Both must leave the
     results untouched: the eager stack without links, the eager stack with
     links, and two replays of the captured stack with links agree bit for bit
-    (the eager stack itself is checked against the oracle above).  T = 1 runs
-    the GEMV path, whose W13 pass streams the shared expert before it waits
-    for the routing kernel; T = 4 the exact decode tensor-core kernel."""
+    (the eager stack itself is checked against the oracle above).  So do the
+    stack whose pre-norms after the first come from the previous layer's
+    combine (moe_forward_residual_norm), eager and replayed: that is the form
+    the bench times.  T = 1 runs the GEMV path, whose W13 pass streams the
+    shared expert before it waits for the routing kernel; T = 4 the exact
+    decode tensor-core kernel."""
     import torch
     import expert_routing_grouped_gb300 as moe
     dev = torch.device("cuda:0")
@@ -108,6 +111,15 @@ def test_decode_stack_graph_replay_and_prefetch_bitwise(T):
         for lay in layers:
             moe.rmsnorm_bf16(resid, T, H, 1e-6, xn, stream)
             lay.forward_residual(xn, T, resid, stream)
+
+    def stack_fused():
+        resid.copy_(x0)
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn, stream)
+        for i, lay in enumerate(layers):
+            if i + 1 < len(layers):
+                lay.forward_residual_norm(xn, T, resid, 1e-6, xn, stream)
+            else:
+                lay.forward_residual(xn, T, resid, stream)
 
     try:
         with torch.cuda.stream(stream):
@@ -132,8 +144,84 @@ def test_decode_stack_graph_replay_and_prefetch_bitwise(T):
             assert np.array_equal(resid.cpu().numpy(), plain)
         assert all(lay.status() == 0 for lay in layers)
         del g
+        with torch.cuda.stream(stream):
+            stack_fused()
+        torch.cuda.synchronize()
+        assert np.array_equal(resid.cpu().numpy(), plain)
+        gf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            stack_fused()
+        for _ in range(2):
+            resid.zero_()
+            xn.zero_()
+            gf.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(resid.cpu().numpy(), plain)
+        assert all(lay.status() == 0 for lay in layers)
+        del gf
     finally:
         for lay in layers:
             lay.set_next_layer(None)
+        for lay in layers:
+            lay.close()
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_forward_residual_norm_matches_separate_norm(T):
+    """moe_forward_residual_norm = moe_forward_residual followed by
+    moe_rmsnorm_bf16 of the updated residual, bit for bit, on each expert path
+    (T = 1 GEMV, T = 4 exact decode tensor-core kernel, T = 16 tensor-core
+    grouped GEMM), in place (norm_out = x) as the stacked layers use it; and a
+    null, misaligned or resid-overlapping norm_out, or a negative eps, is
+    rejected before anything is launched."""
+    import ctypes
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    dev = torch.device("cuda:0")
+    wl = synth.BY_NAME["glm_decode"]
+    H = wl.H
+    layers = [make_layer(wl, l, 16, dev)[0] for l in range(2)]
+    try:
+        x0 = torch.from_numpy(synth.bf16_to_f32(synth.x_rows(wl, T))).to(dev)
+        xn = torch.empty(T, H, dtype=torch.int16, device=dev)
+        # separate calls
+        resid = x0.clone()
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        layers[0].forward_residual(xn, T, resid)
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        torch.cuda.synchronize()
+        r1, n1 = resid.cpu().numpy(), xn.cpu().numpy()
+        layers[1].forward_residual(xn, T, resid)
+        torch.cuda.synchronize()
+        r2 = resid.cpu().numpy()
+        # fused, in place
+        resid.copy_(x0)
+        xn.zero_()
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        layers[0].forward_residual_norm(xn, T, resid, 1e-6, xn)
+        torch.cuda.synchronize()
+        assert np.array_equal(resid.cpu().numpy(), r1)
+        assert np.array_equal(xn.cpu().numpy(), n1)
+        layers[1].forward_residual(xn, T, resid)
+        torch.cuda.synchronize()
+        assert np.array_equal(resid.cpu().numpy(), r2)
+        assert all(lay.status() == 0 for lay in layers)
+        assert np.all(np.isfinite(r2))
+        # argument checks: nothing launched, resid untouched
+        h = layers[0]._handle
+        big = torch.empty(T * H + 16, dtype=torch.int16, device=dev)
+        P = ctypes.c_void_p
+        call = moe.lib.moe_forward_residual_norm
+        assert call(h, P(xn.data_ptr()), T, P(resid.data_ptr()), ctypes.c_float(1e-6), None,
+                    None) == moe.MOE_ERR_ARG
+        assert call(h, P(xn.data_ptr()), T, P(resid.data_ptr()), ctypes.c_float(1e-6),
+                    P(big.data_ptr() + 2), None) == moe.MOE_ERR_ARG
+        assert call(h, P(xn.data_ptr()), T, P(resid.data_ptr()), ctypes.c_float(1e-6),
+                    P(resid.data_ptr() + 16), None) == moe.MOE_ERR_ARG
+        assert call(h, P(xn.data_ptr()), T, P(resid.data_ptr()), ctypes.c_float(-1.0),
+                    P(big.data_ptr()), None) == moe.MOE_ERR_ARG
+        torch.cuda.synchronize()
+        assert np.array_equal(resid.cpu().numpy(), r2)
+    finally:
         for lay in layers:
             lay.close()
