@@ -360,6 +360,80 @@ __device__ __forceinline__ void group_mask(float key[EPL], int E, const RouteRul
   }
 }
 
+// The same selection as argmax_rounds for up to 8 candidates per lane, with
+// each round's warp argmax done by the hardware reductions: the keys become
+// order-preserving 32-bit integers (a NaN, and the padding past E, lowest;
+// -0 as +0), each lane sorts its own
+// (key, id, score) triples once, and a round is the warp maximum of the lanes'
+// first keys (redux.sync max), then the lowest id among the lanes that hold
+// it (redux.sync min) -- larger key first, lower id on ties.  The winning
+// lane drops its first triple.  Lane j < k ends with slot j's expert and
+// score.
+__device__ __forceinline__ uint32_t order_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  if (f != f) return 0u;
+  if (f == 0.f) return 0x80000000u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+template <int EPL>
+__device__ __forceinline__ void topk_redux(const float key[EPL], const float val[EPL], int E,
+                                           int k, int &my_idx, float &my_val) {
+  static_assert(EPL <= 8, "at most 8 candidates per lane");
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  uint32_t lb[8];   // this lane's candidates, first in order first
+  int li[8];
+  float lv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lb[i] = (i < EPL && lane + 32 * i < E) ? order_bits(key[i % EPL]) : 0u;
+    li[i] = i < EPL ? lane + 32 * i : 0x7fffffff;
+    lv[i] = i < EPL ? val[i % EPL] : 0.f;
+  }
+  // bitonic sort of the 8 triples: larger key first, lower id on ties
+#pragma unroll
+  for (int size = 2; size <= 8; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const int a = ((i & size) == 0) ? i : j, b = ((i & size) == 0) ? j : i;
+          const bool swap = lb[b] > lb[a] || (lb[b] == lb[a] && li[b] < li[a]);
+          const uint32_t tb = lb[a];
+          const int ti = li[a];
+          const float tv = lv[a];
+          lb[a] = swap ? lb[b] : lb[a];
+          li[a] = swap ? li[b] : li[a];
+          lv[a] = swap ? lv[b] : lv[a];
+          lb[b] = swap ? tb : lb[b];
+          li[b] = swap ? ti : li[b];
+          lv[b] = swap ? tv : lv[b];
+        }
+      }
+  my_idx = -1;
+  my_val = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t m = __reduce_max_sync(full, lb[0]);
+    const int win = (int)__reduce_min_sync(full, lb[0] == m ? (uint32_t)li[0] : 0x7fffffffu);
+    const float v = __shfl_sync(full, lv[0], win & 31);
+    if (lane == j) {
+      my_idx = win;
+      my_val = v;
+    }
+    const bool pop = li[0] == win;
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      lb[i] = pop ? lb[i + 1] : lb[i];
+      li[i] = pop ? li[i + 1] : li[i];
+      lv[i] = pop ? lv[i + 1] : lv[i];
+    }
+    lb[7] = pop ? 0u : lb[7];
+    li[7] = pop ? 0x7fffffff : li[7];
+  }
+}
+
 // k rounds of a warp argmax (larger key first, lower id on ties): lane j < k
 // ends with slot j's expert and score.
 template <int EPL>
@@ -462,7 +536,10 @@ __device__ __forceinline__ void topk_select(float key[EPL], float val[EPL], int 
   if (r.n_group > 1) group_mask<EPL>(key, E, r);
   int my_idx;
   float my_val;
-  argmax_rounds<EPL>(key, val, k, my_idx, my_val);
+  if constexpr (EPL <= 8)
+    topk_redux<EPL>(key, val, E, k, my_idx, my_val);
+  else
+    argmax_rounds<EPL>(key, val, k, my_idx, my_val);
   slot_weights<EPL>(my_idx, my_val, val, t, E, k, r, idx_out, w_out, nullptr);
 }
 
@@ -618,7 +695,10 @@ __global__ void __launch_bounds__(256) route_small_kernel(
     if (r.n_group > 1) group_mask<EPL>(key, E, r);
     int my_idx;
     float my_val;
-    argmax_rounds<EPL>(key, val, k, my_idx, my_val);
+    if constexpr (EPL <= 8)
+      topk_redux<EPL>(key, val, E, k, my_idx, my_val);
+    else
+      argmax_rounds<EPL>(key, val, k, my_idx, my_val);
     slot_weights<EPL>(my_idx, my_val, val, warp, E, k, r, idx, w, sidx);
   }
   __syncthreads();
