@@ -370,22 +370,27 @@ __global__ void __launch_bounds__(256) gemv_bf16_kernel(
   bool pre = false;                    // wv/sc already hold this item's first chunk
   uint4 wv[kRowsPerWarp];
   float sc[kRowsPerWarp];
-  // The work is dealt as contiguous ranges of [routed items, shared items].
-  // Before the wait the routed count is not known; the deal assumes the
-  // usual one, min(E, T k) distinct experts, so phase 0 takes this CTA's
-  // share of the shared items from that deal and phase 1 its routed share.
-  // When the routing turns out otherwise (repeated experts, a top-p trim)
-  // phase 1 deals the routed items evenly instead.
+  // The work is dealt as contiguous ranges of one sequence of the n routed
+  // and shared items, with the shared items spread through it (shared item s
+  // at position floor(s n / items_s)): about items_s CTAs then take one
+  // shared item each in phase 0, while the routing kernel runs, and as many
+  // fewer routed items in phase 1, instead of a few CTAs taking them all.
+  // Both parts of a range stay contiguous.  Before the wait the routed count
+  // is not known; the deal assumes the usual one, min(E, T k) distinct
+  // experts.  When the routing turns out otherwise (repeated experts, a
+  // top-p trim) phase 1 deals the routed items evenly instead.
   const long long r_guess = (long long)min(E, T * k) * items_r;
   const long long n_guess = r_guess + items_s;
   const long long g_lo = n_guess * blockIdx.x / gridDim.x;
   const long long g_hi = n_guess * (blockIdx.x + 1) / gridDim.x;
+  const long long s_lo = (g_lo * items_s + n_guess - 1) / n_guess;   // shared items before g_lo
+  const long long s_hi = (g_hi * items_s + n_guess - 1) / n_guess;
   for (int phase = early ? 0 : 1; phase < 2; ++phase) {
   // Phase 0: the shared expert's items (item_at with no routed experts maps
   // item i to the shared expert's 32-row group i).  Phase 1: after the wait,
   // the routed items (and, in W2, the shared expert's after them).
   int n_routed = 0, items = items_s;
-  int i0 = (int)(max(g_lo, r_guess) - r_guess), i1 = (int)(max(g_hi, r_guess) - r_guess);
+  int i0 = (int)s_lo, i1 = (int)s_hi;
   if (phase == 1) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     act = after_wait(act);
@@ -401,8 +406,8 @@ __global__ void __launch_bounds__(256) gemv_bf16_kernel(
     n_routed = n_active - has_shared;
     items = n_routed * items_r + (early ? 0 : has_shared * items_s);
     if (early && items == r_guess) {
-      i0 = (int)min(g_lo, r_guess);
-      i1 = (int)min(g_hi, r_guess);
+      i0 = (int)(g_lo - s_lo);
+      i1 = (int)(g_hi - s_hi);
     } else {
       i0 = (int)((long long)items * blockIdx.x / gridDim.x);
       i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
