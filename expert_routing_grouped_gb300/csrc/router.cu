@@ -414,6 +414,7 @@ __device__ __forceinline__ void topk_redux(const float key[EPL], const float val
       }
   my_idx = -1;
   my_val = 0.f;
+#pragma unroll 8
   for (int j = 0; j < k; ++j) {
     const uint32_t m = __reduce_max_sync(full, lb[0]);
     const int win = (int)__reduce_min_sync(full, lb[0] == m ? (uint32_t)li[0] : 0x7fffffffu);
@@ -497,6 +498,7 @@ __device__ __forceinline__ void slot_weights(int my_idx, float my_val, const flo
   float num = 0.f;
   if (lane < k) num = (r.mode != 1) ? expf(my_val - top) : my_val;
   float den = 0.f;
+#pragma unroll 8
   for (int j = 0; j < k; ++j) den += __shfl_sync(full, num, j);
   // Mode 2 divides by the sum over all experts (xor-butterfly: the same bits
   // on every lane).
