@@ -793,6 +793,240 @@ __global__ void __launch_bounds__(256, 2) gemv_w2_mma_kernel(
   }
 }
 
+// 8 bytes global -> registers, not kept in L1, evict-first in L2.
+__device__ __forceinline__ uint2 ld_stream8(const void *p, uint64_t pol) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
+// The single-token W2 GEMV with K split over the warps (T = 1, K = 512 G:
+// G 64-wide groups per warp).  The products, the exactness and the fragment
+// layout are those of gemv_w2_mma_kernel; the weights take another road.
+// An item is 32 rows of one expert; warp w takes its groups w G .. w G + G - 1
+// of both 16-row tiles, and each lane loads exactly its A fragments from
+// global memory, 8 bytes of rows g and g + 8 per group (the four lanes of a
+// row read one full 32-byte sector), with no shared tile and no barrier
+// between loads and MMAs.  The two tiles of an item are the units of a
+// two-deep register pipeline: the loads of the next unit are in flight while
+// a unit is multiplied.  At an item's end the eight warps' partial tiles go
+// through shared memory (double-buffered) and one CTA barrier; warps 0 and 1
+// sum them in warp order (the same sum every run) and write y.  An expert's
+// slot -- its id, rows, position and routing weight -- is read once, one
+// item ahead of its first item, and h is staged once per expert.
+template <int G>
+__global__ void __launch_bounds__(256, 2) gemv_w2_ks_kernel(
+    const __nv_bfloat16 *__restrict__ act, int act_stride, int k, int E, int K_r, int K_s,
+    int rows_r, int rows_s, const uint8_t *__restrict__ wq_r, const float *__restrict__ ws_r,
+    const uint8_t *__restrict__ wq_s, const float *__restrict__ ws_s,
+    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active_p,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    const float *__restrict__ wts, float *__restrict__ out_y, int out_stride,
+    const __grid_constant__ L2Prefetch pf) {
+  constexpr int PL = 2;   // h's planes = B columns 0 and 1
+  constexpr int K = 512 * G;
+  constexpr int T = 1;
+  l2_prefetch_share(pf);  // init-time weights: no wait needed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint4 smem_v[];
+  uint4 *xs = smem_v;                                                  // [PL][K/8], swizzled
+  float *xsum = reinterpret_cast<float *>(smem_v + PL * (K / 8));      // [K/32]
+  float2 *part = reinterpret_cast<float2 *>(xsum + K / 32);            // [2][8][2][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const uint64_t pol = l2_evict_first_policy();
+  const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
+  const int A = T * k;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  act = after_wait(act);
+  active = after_wait(active);
+  n_active_p = after_wait(n_active_p);
+  offsets = after_wait(offsets);
+  perm = after_wait(perm);
+  wts = after_wait(wts);
+  out_y = after_wait(out_y);
+  // [routed items, the shared expert's], contiguous ranges per CTA
+  const int n_active = *n_active_p;
+  const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
+  const int n_routed = n_active - has_shared;
+  const int routed_items = n_routed * items_r;
+  const int items = routed_items + has_shared * items_s;
+  const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+  const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+  // An expert's slot: routed slots a < n_routed hold items_r items each, the
+  // shared slot n_routed the rest.
+  struct Slot {
+    int a, e, p0;
+    const uint8_t *wq;
+    const float *ws;
+  };
+  auto slot_of = [&](int a) {
+    Slot sl;
+    sl.a = a;
+    if (a < n_routed) {
+      sl.e = active[a];
+      sl.wq = wq_r + (size_t)sl.e * rows_r * (K / 2);
+      sl.ws = ws_r + (size_t)sl.e * rows_r * (K / 64);
+      sl.p0 = offsets[sl.e];
+    } else {
+      sl.e = E;
+      sl.wq = wq_s;
+      sl.ws = ws_s;
+      sl.p0 = A;
+    }
+    return sl;
+  };
+  auto slot_index = [&](int item) { return item < routed_items ? item / items_r : n_routed; };
+  auto group_of = [&](int item) {
+    return item < routed_items ? item % items_r : item - routed_items;
+  };
+  // per-unit registers: rows g and g + 8 of the unit's tile, this warp's groups
+  uint2 wl0[G], wh0[G], wl1[G], wh1[G];
+  float sl0[G], sh0[G], sl1[G], sh1[G];
+  auto load_unit = [&](uint2 (&wl)[G], uint2 (&wh)[G], float (&sl)[G], float (&sh)[G],
+                       const Slot &sl_, int gi, int t) {
+    const size_t r0 = (size_t)gi * kRowsPerItem + 16 * t + g;
+    const uint8_t *p0 = sl_.wq + r0 * (K / 2) + warp * G * 32 + q * 8;
+    const uint8_t *p1 = p0 + (size_t)8 * (K / 2);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      wl[j] = ld_stream8(p0 + j * 32, pol);
+      wh[j] = ld_stream8(p1 + j * 32, pol);
+    }
+    const float *s0 = sl_.ws + r0 * (K / 64) + warp * G;
+    const float *s1 = s0 + 8 * (K / 64);
+    if constexpr (G == 4) {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(s0));
+      const float4 b = __ldg(reinterpret_cast<const float4 *>(s1));
+      sl[0] = a.x; sl[1] = a.y; sl[2] = a.z; sl[3] = a.w;
+      sh[0] = b.x; sh[1] = b.y; sh[2] = b.z; sh[3] = b.w;
+    } else {
+      const float2 a = __ldg(reinterpret_cast<const float2 *>(s0));
+      const float2 b = __ldg(reinterpret_cast<const float2 *>(s1));
+      sl[0] = a.x; sl[1] = a.y;
+      sh[0] = b.x; sh[1] = b.y;
+    }
+  };
+  // One unit's MMAs: this warp's groups of one 16-row tile; h's planes are
+  // the B columns 0 (hi) and 1 (lo).  Lanes q = 0 end with the rows' sums.
+  auto mul_unit = [&](const uint2 (&wl)[G], const uint2 (&wh)[G], const float (&sl)[G],
+                      const float (&sh)[G], float &acc0, float &acc1) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int gk = warp * G + j;   // group index in K
+      uint32_t b0[4] = {0u, 0u, 0u, 0u}, b1[4] = {0u, 0u, 0u, 0u};
+      if (g < PL) {
+        const int c = 2 * gk + (q >> 1), j0 = 2 * (q & 1), sw = (c >> 1) & 3;
+        const uint4 *src = xs + (size_t)g * (K / 8) + c * 4;
+        const uint4 u0 = src[j0 ^ sw], u1 = src[(j0 + 1) ^ sw];
+        b0[0] = u0.x; b0[1] = u0.y; b0[2] = u0.z; b0[3] = u0.w;
+        b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
+      }
+      __syncwarp();   // the MMAs below are warp-collective
+      const float xc = 136.0f * (xsum[2 * gk] + xsum[2 * gk + 1]);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4)
+        mma16816(d, nib_pair_bf16(wl[j].x >> (4 * s4)), nib_pair_bf16(wh[j].x >> (4 * s4)),
+                 nib_pair_bf16(wl[j].y >> (4 * s4)), nib_pair_bf16(wh[j].y >> (4 * s4)), b0[s4],
+                 b1[s4]);
+      acc0 = fmaf(sl[j], (d[0] + d[1]) - xc, acc0);
+      acc1 = fmaf(sh[j], (d[2] + d[3]) - xc, acc1);
+    }
+  };
+  if (i0 < i1) {
+    Slot cur = slot_of(slot_index(i0));
+    Slot nxt = cur;
+    int staged = -1, par = 0;
+    load_unit(wl0, wh0, sl0, sh0, cur, group_of(i0), 0);
+    load_unit(wl1, wh1, sl1, sh1, cur, group_of(i0), 1);
+    float w8 = 1.f;   // routing weights of cur and nxt (warps 0 and 1)
+    if (warp < 2 && cur.e < E) w8 = __ldcg(wts + __ldcg(perm + cur.p0));
+    float w8n = w8;
+    for (int item = i0; item < i1; ++item, par ^= 1) {
+      const int gi = group_of(item);
+      // the next item's slot, read one item ahead when the expert changes
+      const bool more = item + 1 < i1;
+      const int na = more ? slot_index(item + 1) : cur.a;
+      if (na != nxt.a) {
+        nxt = slot_of(na);
+        if (warp < 2) w8n = nxt.e < E ? __ldcg(wts + __ldcg(perm + nxt.p0)) : 1.f;
+      }
+      if (cur.a != staged) {
+        __syncthreads();   // previous readers of xs are done
+        // One thread per chunk: 64 bytes per plane in, swizzled out, the
+        // chunk sum over the planes.
+        for (int c = threadIdx.x; c < K / 32; c += blockDim.x) {
+          float sum = 0.f;
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl) {
+            const size_t row = (size_t)(2 * cur.p0 + pl);   // the position's plane pl
+            const uint4 *src = reinterpret_cast<const uint4 *>(act + row * act_stride) + c * 4;
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                sum += __uint_as_float(u[m] << 16) + __uint_as_float(u[m] & 0xFFFF0000u);
+            }
+            uint4 *dst = xs + (size_t)pl * (K / 8) + c * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j ^ ((c >> 1) & 3)] = v[j];
+          }
+          xsum[c] = sum;
+        }
+        __syncthreads();
+        staged = cur.a;
+      }
+      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      mul_unit(wl0, wh0, sl0, sh0, acc[0][0], acc[0][1]);
+      if (more) load_unit(wl0, wh0, sl0, sh0, nxt, group_of(item + 1), 0);
+      mul_unit(wl1, wh1, sl1, sh1, acc[1][0], acc[1][1]);
+      if (more) load_unit(wl1, wh1, sl1, sh1, nxt, group_of(item + 1), 1);
+      // The item's partial tiles; warp t sums tile t over the warps and
+      // writes it (lanes q = 0 hold columns 0 and 1).
+      float2 *pp = part + par * (kWarps * 2 * 32);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) pp[(warp * 2 + t) * 32 + lane] = make_float2(acc[t][0], acc[t][1]);
+      __syncthreads();
+      if (warp < 2 && q == 0) {
+        const int t = warp;
+        float r0 = 0.f, r1 = 0.f;
+        for (int v = 0; v < kWarps; ++v) {   // warp order: the same sum every run
+          const float2 pv = pp[(v * 2 + t) * 32 + lane];
+          r0 += pv.x;
+          r1 += pv.y;
+        }
+        out_y[(size_t)cur.p0 * out_stride + gi * kRowsPerItem + 16 * t + g] = w8 * r0;
+        out_y[(size_t)cur.p0 * out_stride + gi * kRowsPerItem + 16 * t + g + 8] = w8 * r1;
+      }
+      if (more && nxt.a != cur.a) {
+        cur = nxt;
+        w8 = w8n;
+      }
+    }
+  }
+}
+
+template <int G>
+cudaError_t launch_w2_ks(const moe_handle *h, cudaStream_t st) {
+  constexpr int K = 512 * G;
+  const size_t smem = (size_t)2 * K * 2 + K / 8 + (size_t)2 * kWarps * 2 * 32 * 8;
+  int per_sm = 1;
+  const cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, gemv_w2_ks_kernel<G>, kWarps * 32, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  return launch_k(h->pdl, gemv_w2_ks_kernel<G>, dim3(h->num_sms * per_sm), dim3(kWarps * 32),
+                  smem, st, h->ws.hpl, K, h->k, h->E, h->I, K, h->H, h->S ? h->H : 0,
+                  h->ex.w2q, h->ex.w2s, h->sh.w2q, h->sh.w2s, h->ws.active, h->ws.n_active,
+                  h->ws.offsets, h->ws.perm, h->ws.w, h->ws.y, h->H, next_layer_prefetch(h));
+}
+
 cudaError_t launch_w2_mma(const moe_handle *h, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
   const int K_s = h->S ? h->Is : h->I;
@@ -899,9 +1133,14 @@ cudaError_t launch_gemv_w13(const moe_handle *h, const void *x, int T, cudaStrea
 
 cudaError_t launch_gemv_w2(const moe_handle *h, int T, cudaStream_t st) {
   const int h_stride = h->I > h->Is ? h->I : h->Is;
-  // The MMA kernel at T = 1 when an item takes few tile iterations (K <= 4096:
-  // each iteration ends at a CTA barrier; at K = 6144 (W13) and 14336 (a
+  // T = 1: the K-split MMA kernel where routed and shared experts share a K
+  // of 1024 or 2048 (its register pipeline holds one item per lane); else the
+  // tiled MMA kernel when an item takes few tile iterations (K <= 4096: each
+  // iteration ends at a CTA barrier; at K = 6144 (W13) and 14336 (a
   // Mixtral-shaped W2) the SIMT kernel measured faster).
+  const int K_s = h->S ? h->Is : h->I;
+  if (T == 1 && K_s == h->I && h->I == 2048) return launch_w2_ks<4>(h, st);
+  if (T == 1 && K_s == h->I && h->I == 1024) return launch_w2_ks<2>(h, st);
   if (T == 1 && h_stride <= 4096 && w2_mma_smem(h_stride) <= 113 * 1024) return launch_w2_mma(h, st);
 #define MOE_W2(NT)                                                                             \
   return launch_bf16<NT, 2, 1>(h, h->ws.hpl, h_stride, T, h->I, h->S ? h->Is : h->I, h->H,     \
