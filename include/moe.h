@@ -196,8 +196,9 @@ int moe_forward_host(moe_handle *h, const void *x_host, int T, float *out_host,
  * norm_out) would give: the next stacked layer's pre-norm, computed by the
  * kernel that adds the layer output into resid (one launch in place of two;
  * norm before each MoE layer: tutorial cf-1.com §2.1 step 1).  norm_out
- * [T][H] bf16 bits, device, 16-byte aligned; it may be x (x is no longer
- * read when it is written) but must not overlap resid.  eps >= 0.
+ * [T][H] bf16 bits, device, 16-byte aligned: the input of a next layer
+ * whose x_dtype is bf16.  It may be x (x is no longer read when it is
+ * written) but must not overlap resid.  eps >= 0.
  * Returns as moe_forward_residual; MOE_ERR_ARG also for a null, misaligned
  * or overlapping norm_out or a bad eps.
  */
