@@ -670,12 +670,30 @@ def roofline_gemv(res, pk, src):
     by = na * 2 * wl.H * wl.I * 9 // 16 + T * wl.H * 2
     ach = by / (ms * 1e-3) / 1e9
     gemv = res.get("regime", 1) == 1
-    return {"kernel": "gemv_w13" if gemv else "decode_tc_w13", "bound": "hbm",
-            "achieved": round(ach, 1),
-            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-            "traffic": traffic("gemv_w13") if gemv and wl.name == "glm_decode" and T == 1 else None,
-            "peak_source": "%s hbm_gbs" % src,
-            "per_launch": "%.1f activated experts x 2*H*I*0.5625 B + x" % na}
+    out = {"kernel": "gemv_w13" if gemv else "decode_tc_w13", "bound": "hbm",
+           "achieved": round(ach, 1),
+           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+           "traffic": traffic("gemv_w13") if gemv and wl.name == "glm_decode" and T == 1 else None,
+           "peak_source": "%s hbm_gbs" % src,
+           "per_launch": "%.1f activated experts x 2*H*I*0.5625 B + x" % na}
+    ms2 = res["stage"].get("w2")
+    if ms2:
+        # the W2 pass beside it: the activated experts' down-projection rows
+        # and scales, plus h's two bf16 planes per activated expert
+        by2 = na * wl.H * wl.I * 9 // 16 + na * 2 * wl.I * 2
+        a2 = by2 / (ms2 * 1e-3) / 1e9
+        Is = wl.I_shared if wl.n_shared else wl.I
+        if not gemv:
+            name = "decode_tc_w2"
+        elif T == 1 and wl.I in (1024, 2048) and Is == wl.I:
+            name = "gemv_w2_ks"
+        elif T == 1 and max(wl.I, Is) <= 4096:
+            name = "gemv_w2_mma"
+        else:
+            name = "gemv_w2_simt"
+        out["w2"] = {"kernel": name, "achieved": round(a2, 1), "frac": round(a2 / pk["hbm_gbs"], 4),
+                     "per_launch": "%.1f activated experts x H*I*0.5625 B + h" % na}
+    return out
 
 
 def make_line(pre, dec, world, reduce_max, pk, src, steps, warmup):
