@@ -234,13 +234,16 @@ def test_forward_host_and_residual(dev):
     assert np.array_equal(resid.cpu().numpy(), (base + got).astype(np.float32))
 
 
-def test_rmsnorm_bf16_within_one_ulp(dev):
+@pytest.mark.parametrize("H", [6144, 10240])
+def test_rmsnorm_bf16_within_one_ulp(dev, H):
+    """H = 10240 takes the norm's path for rows past 8192 elements (read back
+    from the row, not held in registers)."""
     import torch
     import expert_routing_grouped_gb300 as moe
     rng = np.random.default_rng(0)
-    x = (rng.normal(0, 5, (5, 6144))).astype(np.float32)
-    out = torch.empty(5, 6144, dtype=torch.int16, device=dev)
-    moe.rmsnorm_bf16(torch.from_numpy(x).to(dev), 5, 6144, 1e-6, out)
+    x = (rng.normal(0, 5, (5, H))).astype(np.float32)
+    out = torch.empty(5, H, dtype=torch.int16, device=dev)
+    moe.rmsnorm_bf16(torch.from_numpy(x).to(dev), 5, H, 1e-6, out)
     torch.cuda.synchronize()
     got = synth.bf16_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
     ref = oracle.rmsnorm(x, 1e-6)

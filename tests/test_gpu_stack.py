@@ -18,6 +18,7 @@ import pytest
 import oracle
 import synth
 from gpu_inputs import make_layer, oracle_layer, rel_l2
+from synth.workloads import Workload
 from inputs import MARGIN, margin_x
 
 pytestmark = pytest.mark.gpu
@@ -225,3 +226,44 @@ def test_forward_residual_norm_matches_separate_norm(T):
     finally:
         for lay in layers:
             lay.close()
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_forward_residual_norm_wide_rows(T):
+    """The fused combine and norm on rows longer than 8192 elements (H =
+    10240: the norm reads the row's float4s past 2048 back from resid), on
+    the GEMV path: bit for bit the separate calls, and the layer output
+    within the GEMV tolerance of the oracle."""
+    import torch
+    import expert_routing_grouped_gb300 as moe
+    dev = torch.device("cuda:0")
+    wl = Workload("wide_rows", H=10240, E=8, k=2, I=1024, n_shared=1, I_shared=1024,
+                  router_mode=1, rsf=2.5, x_dtype=1, tokens=(T,), seed=77, bias="normal",
+                  bias_sigma=0.1)
+    H = wl.H
+    h, Wr, bias = make_layer(wl, 0, 4, dev)
+    try:
+        h.set_option(moe.MOE_OPT_REGIME, moe.REGIME_GEMV)
+        x_bits, _ = margin_x(wl, T, Wr, bias)
+        x0 = torch.from_numpy(synth.bf16_to_f32(x_bits).astype(np.float32)).to(dev)
+        xn = torch.empty(T, H, dtype=torch.int16, device=dev)
+        resid = x0.clone()
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        xn_in = xn.cpu().numpy().view(np.uint16).copy()
+        h.forward_residual(xn, T, resid)
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        torch.cuda.synchronize()
+        r1, n1 = resid.cpu().numpy(), xn.cpu().numpy()
+        resid.copy_(x0)
+        moe.rmsnorm_bf16(resid, T, H, 1e-6, xn)
+        h.forward_residual_norm(xn, T, resid, 1e-6, xn)
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        assert np.array_equal(resid.cpu().numpy(), r1)
+        assert np.array_equal(xn.cpu().numpy(), n1)
+        ref = oracle_layer(wl, 0, xn_in, Wr, bias)
+        delta = r1.astype(np.float64) - x0.cpu().numpy().astype(np.float64)
+        scale = np.abs(r1).max() * 2.0 ** -23 * np.sqrt(H)
+        assert np.linalg.norm(delta - ref["out"]) <= GEMV_TOL * np.linalg.norm(ref["out"]) + scale
+    finally:
+        h.close()
