@@ -97,6 +97,34 @@ def test_decode_roofline_names_the_kernel_of_its_path():
     assert gv["kernel"] == "gemv_w13"
     assert gv["achieved"] == pytest.approx((30 * 2 * 6144 * 2048 * 9 // 16 + 6144 * 2) / 0.1e-3 / 1e9,
                                            rel=1e-3)
+    assert "w2" not in gv   # no W2 stage time, no W2 entry
+
+
+def test_decode_roofline_reports_the_w2_pass_of_its_path():
+    """Beside W13, the W2 entry counts the activated experts' down-projection
+    rows and scales plus h's two bf16 planes, and names the kernel that the
+    path and shape select: the K-split MMA kernel for K = 1024 / 2048 shared
+    by routed and shared experts, the tiled one up to K = 4096, the SIMT
+    kernel beyond, the decode tensor-core kernel at 2-8 tokens."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    pk = {"hbm_gbs": 6792.4, "bf16_tflops": 1898.0, "bf16_tflops_sustained": 1707.1}
+    st = {"w13": 0.1, "w2": 0.05}
+    glm = {"wl": synth.BY_NAME["glm_decode"], "stage": st, "n_active": [9]}
+    w2 = bench.roofline_gemv(dict(glm, T=1, regime=1), pk, "measured")["w2"]
+    assert w2["kernel"] == "gemv_w2_ks"
+    by = 9 * 6144 * 2048 * 9 // 16 + 9 * 2 * 2048 * 2
+    assert w2["achieved"] == pytest.approx(by / 0.05e-3 / 1e9, rel=1e-3)
+    assert w2["frac"] == pytest.approx(w2["achieved"] / 6792.4, rel=1e-3)
+    assert bench.roofline_gemv(dict(glm, T=4, regime=3), pk, "measured")["w2"]["kernel"] == \
+        "decode_tc_w2"
+    mix = {"wl": synth.BY_NAME["mixtral"], "stage": st, "n_active": [2]}
+    assert bench.roofline_gemv(dict(mix, T=1, regime=1), pk, "measured")["w2"]["kernel"] == \
+        "gemv_w2_simt"
+    olm = {"wl": synth.BY_NAME["olmoe"], "stage": st, "n_active": [8]}
+    assert bench.roofline_gemv(dict(olm, T=1, regime=1), pk, "measured")["w2"]["kernel"] == \
+        "gemv_w2_ks"
 
 
 def test_algorithmic_units_match_the_published_per_layer_figures():
