@@ -838,6 +838,36 @@ __global__ void __launch_bounds__(256, 2) gemv_w2_ks_kernel(
   const uint64_t pol = l2_evict_first_policy();
   const int items_r = rows_r / kRowsPerItem, items_s = rows_s / kRowsPerItem;
   const int A = T * k;
+  // While the up-projection pass finishes, thread 0 reads the routing's
+  // outputs (written long before, but read here before the wait: they may in
+  // principle be a previous call's) and prefetches this CTA's first item into
+  // L2.  A hint only: everything below reads them again after the wait.
+  if (threadIdx.x == 0) {
+    const int na = __ldcg(n_active_p);
+    const int hs = (rows_s > 0 && na > 0) ? 1 : 0;
+    const int nr = na - hs;
+    const int its = nr * items_r + hs * items_s;
+    const int f = (int)((long long)its * blockIdx.x / gridDim.x);
+    const int l = (int)((long long)its * (blockIdx.x + 1) / gridDim.x);
+    if (f < l && nr >= 0 && nr <= E) {
+      const bool routed = f < nr * items_r;
+      const int e = routed ? __ldcg(active + f / items_r) : E;
+      const int gi = routed ? f % items_r : f - nr * items_r;
+      if ((routed ? (e >= 0 && e < E) : items_s > 0) && gi >= 0 &&
+          gi < (routed ? items_r : items_s)) {
+        const uint8_t *w = routed ? wq_r + (size_t)e * rows_r * (K / 2) : wq_s;
+        const float *sc = routed ? ws_r + (size_t)e * rows_r * (K / 64) : ws_s;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         w + (size_t)gi * kRowsPerItem * (K / 2)),
+                     "r"((uint32_t)(kRowsPerItem * (K / 2)))
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         sc + (size_t)gi * kRowsPerItem * (K / 64)),
+                     "r"((uint32_t)(kRowsPerItem * (K / 64) * 4))
+                     : "memory");
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   act = after_wait(act);
   active = after_wait(active);
@@ -846,9 +876,10 @@ __global__ void __launch_bounds__(256, 2) gemv_w2_ks_kernel(
   perm = after_wait(perm);
   wts = after_wait(wts);
   out_y = after_wait(out_y);
-  // [routed items, the shared expert's], contiguous ranges per CTA
+  // [routed items, the shared expert's], contiguous ranges per CTA (the
+  // routing lists the shared expert last whenever there is one)
   const int n_active = *n_active_p;
-  const int has_shared = (n_active > 0 && active[n_active - 1] == E) ? 1 : 0;
+  const int has_shared = (rows_s > 0 && n_active > 0) ? 1 : 0;
   const int n_routed = n_active - has_shared;
   const int routed_items = n_routed * items_r;
   const int items = routed_items + has_shared * items_s;
